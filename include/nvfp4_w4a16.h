@@ -1,0 +1,197 @@
+/*
+ * nvfp4_w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 NVFP4 weight-only GEMM library.
+ *
+ * The method: weights are NVFP4 -- 4-bit E2M1 codes (sign bit + magnitudes
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}), one float8_e4m3fn scale per 16 consecutive K
+ * elements, one FP32 global scale per tensor -- and activations stay BF16; the
+ * activation is never quantized.  Every forward step computes
+ *     W[n,k] = RN_bf16( e2m1(code[n,k]) * e4m3(scale[n,k/16]) * g )
+ *     Y[m,n] = RN_bf16( sum_k x'[m,k] * W[n,k] )       (FP32 accumulation)
+ * with x' = x, or x' = RN_bf16(x * pre_quant_scale) for AWQ checkpoints.
+ * Sources: "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper"
+ * (TensorRT-LLM PR 14775), Description and Changes table (on-the-fly NVFP4
+ * dequant: E2M1 codebook lookup, per-block FP8 scale, per-tensor scale;
+ * active-expert-only MoE dequant; CUDA-graph capturable); SGLang PR 40022,
+ * Motivation and Modifications (gs=16, E4M3 group scales, a real global scale
+ * stored as a divisor that must be inverted); "[None][fix] Apply the NVFP4_AWQ
+ * pre-quant scale in MegaMoE CuteDSL" (TensorRT-LLM PR 20823), Description
+ * (x * pre_quant_scale in BF16 before the GEMM, shape [1, hidden]; a zero-token
+ * chunk launches no kernel; an already-quantized activation is refused).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device unless
+ *    stated otherwise; all calls are asynchronous on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream).  The library never allocates, frees or
+ *    synchronizes (except nvfp4_device_status, which synchronizes `stream`).
+ *  - The caller owns every buffer.  BF16 tensors are passed as raw 16-bit
+ *    patterns (uint16_t / void*), row-major, densely packed.
+ *  - Arguments are validated before anything is launched; a failed check
+ *    returns a non-OK status, launches nothing and sets a message readable
+ *    with nvfp4_last_error() (thread-local).
+ *  - No call reads device memory back to the host, so every GEMM / MoE /
+ *    dequant call can be captured in a CUDA graph.
+ *  - Faults inside a kernel that the host cannot see (a repacked-weight header
+ *    whose magic or shape does not match the call, a pipeline wait that ran
+ *    out of its iteration limit) do not trap: the kernel skips its work and
+ *    records an error code in a per-device status word, which
+ *    nvfp4_device_status() returns.
+ */
+#ifndef NVFP4_W4A16_H
+#define NVFP4_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad flag, non-finite divisor */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K not a positive multiple of 16, sizes beyond the limits */
+    NVFP4_ERR_ALIGNMENT = 3,         /* a pointer not aligned as documented */
+    NVFP4_ERR_WORKSPACE = 4,         /* workspace missing or smaller than the query says */
+    NVFP4_ERR_CUDA = 5,              /* a CUDA runtime call failed (message has the CUDA error) */
+    NVFP4_ERR_TIMEOUT = 6,           /* device status: a pipeline wait exceeded its limit */
+    NVFP4_ERR_BAD_WEIGHT = 7         /* device status: repacked header magic/shape mismatch */
+} nvfp4_status;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int nvfp4_abi_version(void);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* nvfp4_last_error(void);
+
+/*
+ * Per-device status word written by kernels (0 = OK, else an nvfp4_status).
+ * Synchronizes `stream`, copies the word of the current device to *code_out
+ * and, if `clear` != 0, resets it to 0.
+ */
+nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Repack (once per weight tensor, at load time)                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of the repacked form of an N x K NVFP4 weight (0 if N <= 0, or K is
+ * not a positive multiple of 16).  The size is a multiple of 256.
+ */
+size_t nvfp4_repack_size(int64_t N, int64_t K);
+
+/*
+ * Rewrite a checkpoint-layout NVFP4 weight into the library's tiled layout.
+ * This is the "load" step (the pages' Marlin repack / derived-buffer refresh):
+ * a pure function of its inputs, so re-running it gives identical bytes.
+ *
+ *  packed       device, uint8 [N, K/2] row-major; byte (n, j) holds code (n, 2j)
+ *               in its low nibble and code (n, 2j+1) in its high nibble.
+ *  scales_e4m3  device, uint8 [N, K/16] row-major float8_e4m3fn codes.
+ *  global_scale FP32 per-tensor global scale, by value.
+ *  global_is_divisor  1: global_scale is stored as a divisor d (compressed-
+ *               tensors convention) and the multiplier is g = RN_fp32(1/d),
+ *               one IEEE division done on the host; 0: g = global_scale.
+ *               g must be finite and nonzero.
+ *  out          device, 256-byte aligned, out_bytes >= nvfp4_repack_size(N, K).
+ *
+ * Layout of `out` (all offsets in bytes):
+ *  [0, 256)      header: u32 magic 0x34504E56, u32 version, i64 N, i64 K,
+ *                i64 Np (N rounded up to 256), i64 Kp (K rounded up to 64),
+ *                f32 g, f32 global_scale, u32 global_is_divisor.
+ *  [256, 4352)   magnitude table: 256 entries of 16 bytes, entry s = the BF16
+ *                values RN_bf16(mag_j * e4m3(s) * g) of the 8 E2M1 magnitudes
+ *                j = 0..7, stored as 8 low bytes then 8 high bytes.
+ *  [4352, ...)   atoms of 16 rows x 64 k (576 bytes each), ordered by
+ *                256-row tile, then 64-k block, then 16-row block.  In an atom,
+ *                lane L = 4r + q (r < 8, q < 4) owns 16 code bytes at 16L
+ *                (rows r and r+8 of the block, k group q, 8 bytes each) and 2
+ *                scale bytes at 512 + 2L.  Each 32-bit code word holds 8
+ *                consecutive k: magnitude of element i in bits 4i..4i+2 and
+ *                the signs of elements 0..7 in bits 15, 31, 11, 27, 7, 23, 3, 19.
+ *                Rows >= N and k >= K are padded with code 0 and scale 0.
+ */
+nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
+                          float global_scale, int global_is_divisor,
+                          int64_t N, int64_t K,
+                          void* out, size_t out_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Standalone dequant                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * W (BF16, [N, K] row-major) from a repacked weight: exactly the operand the
+ * GEMM kernels feed to the tensor cores.
+ *  repacked  device, as written by nvfp4_repack for the same N, K.
+ *  out_bf16  device, N*K uint16, 4-byte aligned.
+ */
+nvfp4_status nvfp4_dequant(const void* repacked, int64_t N, int64_t K,
+                           uint16_t* out_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dense W4A16 GEMM                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Workspace bytes nvfp4_w4a16_gemm needs for this problem (may be 0).
+ */
+size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale);
+
+/*
+ * Y = X' . W^T with X' = X (pre_quant_scale == NULL) or RN_bf16(X * pre_quant_scale).
+ *  X               device BF16 [M, K] row-major, 16-byte aligned.
+ *  repacked        device, from nvfp4_repack(N, K).
+ *  pre_quant_scale device BF16 [K] or NULL (AWQ per-channel scale).
+ *  Y               device BF16 [M, N] row-major, 4-byte aligned.
+ *  workspace       device, >= nvfp4_w4a16_gemm_workspace(...) bytes, 256-byte
+ *                  aligned (may be NULL when that size is 0).  Contents on entry
+ *                  do not matter.
+ * M == 0 or N == 0 returns NVFP4_OK and launches nothing.  M <= 16 runs the
+ * split-K HBM-streaming decode kernel; larger M the tensor-core tile kernel.
+ */
+nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
+                              int64_t M, int64_t N, int64_t K, void* Y,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped top-k MoE layer (FC1 gate/up + SwiGLU, FC2, weighted combine)     */
+/* ------------------------------------------------------------------------ */
+
+size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t I);
+
+/*
+ * out[t] = RN_bf16( sum_j p[t,j] * FC2_e( RN_bf16( silu(g) * u ) ) ), e = idx[t,j],
+ * [g; u] = FC1_e(x'_t), for the top-k experts of each token.
+ *  X                 device BF16 [T, H].
+ *  router_logits     device FP32 [T, E].  Top-k on the logits, ties to the lower
+ *                    expert index, slots in descending-logit order; p = softmax
+ *                    over the k selected logits.
+ *  fc1               device: E repacked [2I, H] weights back to back, expert e at
+ *                    fc1 + e * nvfp4_repack_size(2I, H); rows [0, I) are the gate
+ *                    projection, rows [I, 2I) the up projection.
+ *  fc2               device: E repacked [H, I] weights, expert e at
+ *                    fc2 + e * nvfp4_repack_size(H, I).
+ *  fc1_pre_quant_scale  device BF16 [H] or NULL (AWQ scale on FC1's input).
+ *  out               device BF16 [T, H].
+ *  topk_idx_out      device int32 [T, topk] or NULL; topk_weight_out FP32 [T, topk]
+ *                    or NULL; perm_out int32 [T*topk] or NULL (routing slots t*topk+j
+ *                    sorted by expert, then token, then slot); offsets_out int32
+ *                    [E+1] or NULL (exclusive scan of per-expert counts).
+ * Only the weights of experts that received at least one token are read.
+ * T == 0 returns NVFP4_OK and launches nothing.  Limits: E <= 256, topk <= 16,
+ * topk <= E, H and I multiples of 64.
+ */
+nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
+                                     const void* fc1, const void* fc2,
+                                     const void* fc1_pre_quant_scale,
+                                     int64_t T, int E, int topk, int64_t H, int64_t I,
+                                     void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                     int32_t* perm_out, int32_t* offsets_out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_W4A16_H */

@@ -17,4 +17,4 @@ def pytest_configure(config):
 def lib():
     """The built C-ABI library (ctypes handle); built on demand."""
     from w4a16_nvfp4_weight_gb300 import _lib
-    return _lib.load()
+    return _lib.load(build_if_missing=True)

@@ -1,0 +1,100 @@
+"""The C-ABI library builds, loads, exports every function include/*.h
+declares, and rejects bad arguments on the host before touching the GPU."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from w4a16_nvfp4_weight_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("nvfp4_repack", "nvfp4_dequant", "nvfp4_w4a16_gemm", "nvfp4_w4a16_moe_grouped",
+              "nvfp4_repack_size", "nvfp4_last_error", "nvfp4_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in sorted(_declared_functions()):
+        assert hasattr(lib, n), f"{n} declared but not exported"
+    assert set(_lib.SIGNATURES) == _declared_functions()
+    assert lib.nvfp4_abi_version() == 1
+
+
+def test_repack_size():
+    lib = _lib.load(build_if_missing=True)
+    assert lib.nvfp4_repack_size(0, 64) == 0
+    assert lib.nvfp4_repack_size(4, 24) == 0                 # K % 16 != 0
+    assert lib.nvfp4_repack_size(-1, 64) == 0
+    # one 256-row tile, one 64-k block: header + table + 16 atoms
+    assert lib.nvfp4_repack_size(1, 16) == 4352 + 16 * 576
+    assert lib.nvfp4_repack_size(256, 64) == 4352 + 16 * 576
+    assert lib.nvfp4_repack_size(257, 80) == 4352 + 2 * 2 * 16 * 576
+    assert lib.nvfp4_repack_size(1000, 2064) % 256 == 0
+
+
+def _err(lib):
+    return lib.nvfp4_last_error().decode()
+
+
+def test_gemm_rejects_bad_arguments_on_host(lib):
+    V = ctypes.c_void_p
+    good = V(0x10000)
+    st = lib.nvfp4_w4a16_gemm(good, good, None, 4, 64, 24, good, None, 0, None)
+    assert st == 2 and "multiple of 16" in _err(lib)
+    st = lib.nvfp4_w4a16_gemm(good, good, None, -1, 64, 64, good, None, 0, None)
+    assert st == 1
+    st = lib.nvfp4_w4a16_gemm(None, good, None, 4, 64, 64, good, None, 0, None)
+    assert st == 1 and "null" in _err(lib)
+    st = lib.nvfp4_w4a16_gemm(V(0x10008), good, None, 4, 64, 64, good, None, 0, None)
+    assert st == 3 and "X must be 16-byte aligned" in _err(lib)
+    st = lib.nvfp4_w4a16_gemm(good, V(0x10010), None, 4, 64, 64, good, None, 0, None)
+    assert st == 3 and "256-byte" in _err(lib)
+    st = lib.nvfp4_w4a16_gemm(good, good, V(0x10002), 4, 64, 64, good, None, 0, None)
+    assert st == 3 and "pre_quant_scale" in _err(lib)
+    # zero rows / zero columns: OK, nothing launched (no device needed)
+    assert lib.nvfp4_w4a16_gemm(None, None, None, 0, 64, 64, None, None, 0, None) == 0
+    assert lib.nvfp4_w4a16_gemm(None, None, None, 4, 0, 64, None, None, 0, None) == 0
+
+
+def test_repack_and_dequant_reject_bad_arguments_on_host(lib):
+    V = ctypes.c_void_p
+    good = V(0x10000)
+    assert lib.nvfp4_repack(good, good, 448.0, 1, 16, 40, good, 1 << 20, None) == 2
+    assert lib.nvfp4_repack(None, good, 448.0, 1, 16, 64, good, 1 << 20, None) == 1
+    assert lib.nvfp4_repack(good, good, 448.0, 2, 16, 64, good, 1 << 20, None) == 1
+    assert lib.nvfp4_repack(good, good, 448.0, 1, 16, 64, V(0x10080), 1 << 20, None) == 3
+    assert lib.nvfp4_repack(good, good, 448.0, 1, 16, 64, good, 100, None) == 4
+    assert "needs" in _err(lib)
+    assert lib.nvfp4_repack(good, good, 0.0, 0, 16, 64, good, 1 << 20, None) == 1
+    assert lib.nvfp4_repack(good, good, 0.0, 1, 16, 64, good, 1 << 20, None) == 1   # 1/0
+    assert lib.nvfp4_repack(good, good, float("nan"), 1, 16, 64, good, 1 << 20, None) == 1
+    assert lib.nvfp4_dequant(good, 16, 40, good, None) == 2
+    assert lib.nvfp4_dequant(V(0x10010), 16, 64, good, None) == 3
+    assert lib.nvfp4_dequant(good, 16, 64, V(0x10004), None) == 3
+
+
+def test_python_binding_refuses_non_bf16_activations():
+    import torch
+    import w4a16_nvfp4_weight_gb300 as nv
+    w = nv.NVFP4Weight(torch.empty(16, dtype=torch.uint8), 16, 64)
+    with pytest.raises(nv.Nvfp4Error):
+        nv.gemm(torch.zeros(2, 64, dtype=torch.float8_e4m3fn), w)
+    with pytest.raises(nv.Nvfp4Error):
+        nv.gemm(torch.zeros(2, 64, dtype=torch.bfloat16), w)     # CPU tensor

@@ -1,0 +1,225 @@
+"""GPU parity of the dense path (repack, dequant, GEMM) against the CPU oracle.
+
+Dequantized weights are compared bit for bit; GEMM outputs within the parity
+bar (relative Frobenius <= 2e-3, max-abs <= 2e-2 * max|ref|) against the
+oracle's BF16-rounded output.  Small cases are checked element by element;
+the full workload sizes on sampled output features.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import w4a16_nvfp4_weight_gb300 as nv
+from oracle import dense, formats
+from tests import gpu_util as gu
+from w4a16_nvfp4_weight_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(lib):
+    torch.cuda.init()
+    yield
+
+
+def _unrepack(buf, N, K):
+    """Recover checkpoint codes/scales from the repacked bytes, following the
+    layout documented in include/nvfp4_w4a16.h."""
+    b = np.asarray(buf, dtype=np.uint8)
+    hdr = b[:256]
+    assert int(hdr[:4].view(np.uint32)[0]) == 0x34504E56
+    Np, Kp = -(-N // 256) * 256, -(-K // 64) * 64
+    KB = Kp // 64
+    sign_pos = [15, 31, 11, 27, 7, 23, 3, 19]
+    codes = np.zeros((Np, Kp), dtype=np.uint8)
+    scales = np.zeros((Np, Kp // 16), dtype=np.uint8)
+    atoms = b[4352:4352 + (Np // 16) * KB * 576].reshape(Np // 256, KB, 16, 576)
+    for lane in range(32):
+        r, q = lane // 4, lane % 4
+        words = atoms[:, :, :, 16 * lane:16 * lane + 16].copy().view(np.uint32)  # [nt,KB,16,4]
+        sc = atoms[:, :, :, 512 + 2 * lane:512 + 2 * lane + 2]
+        for h in range(2):
+            rows = (np.arange(Np // 256)[:, None, None] * 256 + np.arange(16)[None, None, :] * 16 + r + 8 * h)
+            for wi in range(2):
+                w = words[:, :, :, 2 * h + wi]
+                for i in range(8):
+                    mag = (w >> (4 * i)) & 7
+                    sgn = (w >> sign_pos[i]) & 1
+                    kk = np.arange(KB)[None, :, None] * 64 + q * 16 + wi * 8 + i
+                    codes[np.broadcast_to(rows, mag.shape), np.broadcast_to(kk, mag.shape)] = (mag | (sgn << 3)).astype(np.uint8)
+            kg = np.arange(KB)[None, :, None] * 4 + q
+            scales[np.broadcast_to(rows, sc[..., h].shape), np.broadcast_to(kg, sc[..., h].shape)] = sc[..., h]
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed[:N, :K // 2], scales[:N, :K // 16], codes, scales
+
+
+def test_repack_layout_and_determinism():
+    c = synth.gaussian_case(1, 720, 300, seed=7)
+    w1 = gu.repack_case(c)
+    w2 = gu.repack_case(c)
+    torch.cuda.synchronize()
+    b1, b2 = w1.buf.cpu().numpy(), w2.buf.cpu().numpy()
+    assert np.array_equal(b1, b2)
+    packed, scales, codes_pad, scales_pad = _unrepack(b1, c.N, c.K)
+    assert np.array_equal(packed, c.packed)
+    assert np.array_equal(scales, c.scales)
+    assert not codes_pad[c.N:].any() and not codes_pad[:, c.K:].any()
+    assert not scales_pad[c.N:].any() and not scales_pad[:, c.K // 16:].any()
+    g = np.frombuffer(b1[40:44].tobytes(), dtype=np.float32)[0]
+    assert g == np.float32(1.0) / np.float32(c.divisor)
+
+
+def _dequant_gpu(case):
+    w = gu.repack_case(case)
+    out = nv.dequant(w)
+    gu.check_device_status()
+    return gu.tensor_to_bits(out)
+
+
+def test_dequant_bit_exact_uniform_codes():
+    c = synth.uniform_codes_case()
+    got = _dequant_gpu(c)
+    want = dense.dequant(c.packed, c.scales, c.divisor, True, c.K)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("divisor,is_div", [(448.0, True), (3.0, True), (24366.764, True),
+                                            (1.0, False), (-0.37, False), (1.0e-30, True)])
+def test_dequant_bit_exact_every_scale_code(divisor, is_div):
+    """All 256 scale codes (negative, subnormal and NaN included) x all 16 codes."""
+    N, K = 256, 64
+    codes = np.tile(np.arange(16, dtype=np.uint8), (N, K // 16))
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    scales = np.repeat(np.arange(256, dtype=np.uint8)[:, None], K // 16, axis=1)
+    w = nv.repack(gu.u8(packed), gu.u8(scales), divisor, N, K, global_is_divisor=is_div)
+    got = gu.tensor_to_bits(nv.dequant(w))
+    gu.check_device_status()
+    want = dense.dequant(packed, scales, divisor, is_div, K)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("K,N", [(2064, 1000), (720, 3000), (16, 1), (48, 17), (4096, 512)])
+def test_dequant_bit_exact_tails(K, N):
+    c = synth.gaussian_case(1, K, N, seed=100 + K + N)
+    got = _dequant_gpu(c)
+    want = dense.dequant(c.packed, c.scales, c.divisor, True, c.K)
+    assert np.array_equal(got, want)
+
+
+def _gemm(case, awq=True):
+    w = gu.repack_case(case)
+    x = gu.bits_to_bf16_tensor(case.x_bits)
+    pqs = gu.bits_to_bf16_tensor(case.pqs_bits) if (awq and case.pqs_bits is not None) else None
+    y = nv.gemm(x, w, pre_quant_scale=pqs)
+    gu.check_device_status()
+    return gu.tensor_to_bits(y)
+
+
+def test_gemm_uniform_codes_4x256x256():
+    c = synth.uniform_codes_case()
+    y = _gemm(c)
+    _, ref = gu.oracle_linear(c)
+    gu.compare(y, ref, "4x256x256")
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+@pytest.mark.parametrize("K,N", [(256, 256), (2064, 1000), (720, 3000), (1024, 384)])
+def test_gemm_decode_small(M, K, N):
+    c = synth.gaussian_case(M, K, N, seed=1000 + 7 * M + K + N, awq=(M % 3 == 0))
+    y = _gemm(c)
+    _, ref = gu.oracle_linear(c)
+    gu.compare(y, ref, f"M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("M", [17, 100, 128, 300])
+@pytest.mark.parametrize("K,N", [(256, 256), (2064, 1000), (720, 3000)])
+def test_gemm_larger_m_small(M, K, N):
+    c = synth.gaussian_case(M, K, N, seed=2000 + M + K + N, awq=(M == 100))
+    y = _gemm(c)
+    _, ref = gu.oracle_linear(c)
+    gu.compare(y, ref, f"M={M} K={K} N={N}")
+
+
+def test_dropped_awq_scale_fails_the_bar():
+    c = synth.gaussian_case(8, 1024, 512, seed=77, awq=True)
+    y_no = _gemm(c, awq=False)
+    _, ref = gu.oracle_linear(c, awq=True)
+    with pytest.raises(AssertionError):
+        gu.compare(y_no, ref, "dropped AWQ")
+
+
+def test_zero_rows_launch_nothing():
+    c = synth.gaussian_case(1, 256, 256, seed=5)
+    w = gu.repack_case(c)
+    y = torch.full((0, 256), 1.0, dtype=torch.bfloat16, device="cuda")
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    nv.gemm(x, w, out=y)
+    gu.check_device_status()
+
+
+def test_mismatched_header_is_reported_not_trapped():
+    c = synth.gaussian_case(2, 256, 256, seed=6)
+    w = gu.repack_case(c)
+    bad = nv.NVFP4Weight(w.buf, 128, 256)          # header says N=256
+    x = gu.bits_to_bf16_tensor(c.x_bits)
+    y = torch.full((2, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    nv.gemm(x, bad, out=y)
+    assert nv.device_status(clear=True) == 7
+    assert torch.all(y == 3.0)
+    gu.check_device_status()
+
+
+def _sampled_rows(N, r, n=48):
+    rows = np.unique(np.concatenate([r.choice(N, size=n, replace=False), [0, N - 1]]))
+    return rows
+
+
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 14336), (14336, 4096), (5120, 25600)])
+def test_gemm_decode_full_size_sampled(K, N):
+    r = synth.rng(synth.seed_for(1, K + N))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(1, K * 7 + N))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = _sampled_rows(N, r)
+    for M in (1, 2, 4, 8, 16):
+        x_bits = synth.normal_bf16(r, (M, K))
+        y = nv.gemm(gu.bits_to_bf16_tensor(x_bits), w)
+        gu.check_device_status()
+        yb = gu.tensor_to_bits(y)
+        _, ref = dense.linear(x_bits, packed, scales, d, True, rows=rows)
+        gu.compare(yb[:, rows], ref, f"M={M} K={K} N={N}")
+        assert np.all(np.isfinite(formats.bf16_to_float(yb)))
+
+
+@pytest.mark.parametrize("K,N", [(5120, 13824), (13824, 5120), (8192, 28672)])
+def test_gemm_prefill_full_size_sampled(K, N):
+    r = synth.rng(synth.seed_for(2, K + N))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(2, K * 7 + N))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = _sampled_rows(N, r, n=24)
+    for M, awq in ((512, False), (2048, True), (8192, False)):
+        x_bits = synth.normal_bf16(r, (M, K))
+        pqs = synth.awq_scale_bits(r, K) if awq else None
+        y = nv.gemm(gu.bits_to_bf16_tensor(x_bits), w,
+                    pre_quant_scale=gu.bits_to_bf16_tensor(pqs) if awq else None)
+        gu.check_device_status()
+        yb = gu.tensor_to_bits(y)
+        _, ref = dense.linear(x_bits, packed, scales, d, True, pqs_bits=pqs, rows=rows)
+        gu.compare(yb[:, rows], ref, f"M={M} K={K} N={N} awq={awq}")
+        assert np.all(np.isfinite(formats.bf16_to_float(yb)))
+
+
+def test_lm_head_full_size_sampled():
+    K, N = 4096, 151936
+    r = synth.rng(synth.seed_for(4, 0))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(4, 1))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = _sampled_rows(N, r, n=64)
+    for M in (1, 8, 256):
+        x_bits = synth.normal_bf16(r, (M, K))
+        y = nv.gemm(gu.bits_to_bf16_tensor(x_bits), w)
+        gu.check_device_status()
+        yb = gu.tensor_to_bits(y)
+        _, ref = dense.linear(x_bits, packed, scales, d, True, rows=rows)
+        gu.compare(yb[:, rows], ref, f"LM head M={M}")

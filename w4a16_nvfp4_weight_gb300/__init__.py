@@ -1,0 +1,150 @@
+"""W4A16 NVFP4 weight-only GEMM for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/nvfp4_w4a16.h``: it allocates
+outputs with torch, passes raw device pointers and the current CUDA stream, and
+turns non-OK statuses into ``Nvfp4Error``.  Every step of the computation runs
+in the library's CUDA kernels; there is no Python or CPU fallback.
+
+    w = repack(packed_u8, scales_u8, divisor, N, K, global_is_divisor=True)
+    y = gemm(x_bf16, w)                       # [M, K] -> [M, N]
+    y = gemm(x_bf16, w, pre_quant_scale=s)    # AWQ checkpoints
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import Nvfp4Error
+
+__all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "dequant", "gemm",
+           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "device_status",
+           "abi_version"]
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _require_cuda(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise Nvfp4Error(1, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise Nvfp4Error(1, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise Nvfp4Error(1, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def abi_version():
+    return _lib.load().nvfp4_abi_version()
+
+
+def repack_size(N, K):
+    return int(_lib.load().nvfp4_repack_size(N, K))
+
+
+class NVFP4Weight:
+    """A repacked NVFP4 weight (device buffer) with its logical shape [N, K]."""
+
+    def __init__(self, buf, N, K):
+        self.buf, self.N, self.K = buf, int(N), int(K)
+
+    @property
+    def nbytes(self):
+        return self.buf.numel()
+
+
+def repack(packed, scales, global_scale, N, K, global_is_divisor=True, out=None):
+    """Checkpoint tensors (uint8 [N, K/2] codes, uint8 [N, K/16] E4M3 scales) ->
+    NVFP4Weight.  ``global_scale`` is a Python float (the stored value)."""
+    h = _lib.load()
+    _require_cuda(packed, "packed", torch.uint8)
+    _require_cuda(scales, "scales", torch.uint8)
+    size = int(h.nvfp4_repack_size(N, K))
+    if out is None:
+        out = torch.empty(max(size, 256), dtype=torch.uint8, device=packed.device)
+    _lib.check(h.nvfp4_repack(_ptr(packed), _ptr(scales), float(global_scale),
+                              1 if global_is_divisor else 0, N, K, _ptr(out), out.numel(), _stream()))
+    return NVFP4Weight(out, N, K)
+
+
+def dequant(w, out=None):
+    """BF16 [N, K] weight exactly as the GEMM kernels see it."""
+    h = _lib.load()
+    if out is None:
+        out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.buf.device)
+    _lib.check(h.nvfp4_dequant(_ptr(w.buf), w.N, w.K, _ptr(out), _stream()))
+    return out
+
+
+def gemm_workspace_size(M, N, K, has_pre_quant_scale=False):
+    return int(_lib.load().nvfp4_w4a16_gemm_workspace(M, N, K, 1 if has_pre_quant_scale else 0))
+
+
+def gemm(x, w, pre_quant_scale=None, out=None, workspace=None):
+    """Y[M, N] = X'[M, K] . W^T (BF16), X' = X or RN_bf16(X * pre_quant_scale)."""
+    h = _lib.load()
+    _require_cuda(x, "x", torch.bfloat16)
+    if x.dim() != 2 or x.shape[1] != w.K:
+        raise Nvfp4Error(2, f"x must be [M, {w.K}], got {tuple(x.shape)}")
+    if pre_quant_scale is not None:
+        _require_cuda(pre_quant_scale, "pre_quant_scale", torch.bfloat16)
+        if pre_quant_scale.numel() != w.K:
+            raise Nvfp4Error(2, f"pre_quant_scale must have {w.K} elements")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    need = gemm_workspace_size(M, w.N, w.K, pre_quant_scale is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(h.nvfp4_w4a16_gemm(_ptr(x), _ptr(w.buf), _ptr(pre_quant_scale), M, w.N, w.K,
+                                  _ptr(out), _ptr(workspace), ws_bytes, _stream()))
+    return out
+
+
+def moe_workspace_size(T, E, topk, H, I):
+    return int(_lib.load().nvfp4_w4a16_moe_workspace(T, E, topk, H, I))
+
+
+def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, out=None,
+                return_routing=False, workspace=None):
+    """Top-k MoE layer.  ``fc1``/``fc2``: uint8 device buffers holding E repacked
+    expert weights back to back ([2I, H] and [H, I] each)."""
+    h = _lib.load()
+    _require_cuda(x, "x", torch.bfloat16)
+    _require_cuda(router_logits, "router_logits", torch.float32)
+    T, H = x.shape
+    E = router_logits.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    dev = x.device
+    idx = wts = perm = offs = None
+    if return_routing:
+        idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
+        wts = torch.empty((T, topk), dtype=torch.float32, device=dev)
+        perm = torch.empty(T * topk, dtype=torch.int32, device=dev)
+        offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    need = moe_workspace_size(T, E, topk, H, I)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(h.nvfp4_w4a16_moe_grouped(
+        _ptr(x), _ptr(router_logits), _ptr(fc1), _ptr(fc2), _ptr(fc1_pre_quant_scale),
+        T, E, topk, H, I, _ptr(out), _ptr(idx), _ptr(wts), _ptr(perm), _ptr(offs),
+        _ptr(workspace), ws_bytes, _stream()))
+    if return_routing:
+        return out, dict(idx=idx, p=wts, perm=perm, offsets=offs)
+    return out
+
+
+def device_status(clear=True):
+    """Synchronize the current stream and return (and clear) the device status word."""
+    h = _lib.load()
+    v = ctypes.c_int(0)
+    _lib.check(h.nvfp4_device_status(ctypes.byref(v), 1 if clear else 0, _stream()))
+    return v.value

@@ -1,0 +1,168 @@
+// Host side of the C ABI: error reporting, the device status word, and the
+// dense GEMM entry point (argument validation and the decode / tile shape rule).
+//
+// Boundary behaviour follows the pages: validate shapes, strides and scales
+// with descriptive errors before launching ("[TRTLLM-12288][feat] Support
+// Nemotron-H nvfp4 ckpt on Hopper", review of the dequant wrappers and of the
+// FP8-input guard: fail fast instead of reading wrong addresses), keep the call
+// capturable in a CUDA graph (same page, Description), and refuse anything but
+// BF16 activations ("[None][fix] Apply the NVFP4_AWQ pre-quant scale in MegaMoE
+// CuteDSL": already-quantized inputs are rejected).
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_decode.cuh"
+#include "gemm_tc.cuh"
+
+namespace nvfp4 {
+
+namespace {
+thread_local char g_msg[512] = "";
+__device__ int g_status_word;
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::mutex g_mu;
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+}
+
+nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+nvfp4_status check_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return NVFP4_OK;
+    return fail(NVFP4_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+int* device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+// Split-K plan of the decode kernel for an M x N x K problem.
+struct DecodePlan {
+    int MT, splits, kbs;
+    bool ok;
+};
+
+DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
+    DecodePlan pl{};
+    pl.MT = M <= 8 ? 1 : 2;
+    const int64_t KB = round_up(K, kBlockK) / kBlockK;
+    const int64_t RG = ceil_div(N, 128);
+    const int64_t base = RG * ceil_div(M, 8 * pl.MT);
+    const int64_t target = 2LL * sm_count();
+    int64_t splits = std::min<int64_t>(std::min<int64_t>(8, KB), std::max<int64_t>(1, ceil_div(target, base)));
+    int64_t kbs = ceil_div(KB, splits);
+    // keep the activation slice small enough for two CTAs per SM when possible
+    const size_t soft = 100 * 1024, hard = 227 * 1024;
+    while (decode_smem_bytes(pl.MT, (int)kbs) > soft && splits < std::min<int64_t>(8, KB)) {
+        ++splits;
+        kbs = ceil_div(KB, splits);
+    }
+    splits = ceil_div(KB, kbs);
+    pl.splits = (int)splits;
+    pl.kbs = (int)kbs;
+    pl.ok = decode_smem_bytes(pl.MT, (int)kbs) <= hard;
+    return pl;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" int nvfp4_abi_version(void) { return 1; }
+
+extern "C" const char* nvfp4_last_error(void) { return g_msg; }
+
+extern "C" nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stream) {
+    if (!code_out) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_device_status: code_out is null");
+    int* p = device_status_ptr();
+    if (!p) return fail(NVFP4_ERR_CUDA, "nvfp4_device_status: status word unavailable");
+    nvfp4_status st = check_cuda(cudaStreamSynchronize((cudaStream_t)stream), "nvfp4_device_status: synchronize");
+    if (st != NVFP4_OK) return st;
+    int v = 0;
+    st = check_cuda(cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost), "nvfp4_device_status: read");
+    if (st != NVFP4_OK) return st;
+    if (clear) {
+        st = check_cuda(cudaMemset(p, 0, sizeof(int)), "nvfp4_device_status: clear");
+        if (st != NVFP4_OK) return st;
+    }
+    *code_out = v;
+    return NVFP4_OK;
+}
+
+extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
+    if (use_tc_path(M)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
+    return 0;
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
+                                         int64_t M, int64_t N, int64_t K, void* Y,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || N < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_w4a16_gemm: negative size M=%lld N=%lld", (long long)M, (long long)N);
+    if (K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_gemm: K=%lld must be a positive multiple of 16", (long long)K);
+    if (M == 0 || N == 0) return NVFP4_OK;          // nothing to compute, nothing launched
+    if (!X || !repacked || !Y) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_w4a16_gemm: null pointer (X=%p W=%p Y=%p)", X, repacked, Y);
+    if (!aligned(X, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: X must be 16-byte aligned");
+    if (!aligned(repacked, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: repacked weight must be 256-byte aligned");
+    if (!aligned(Y, 4)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: Y must be 4-byte aligned");
+    if (pre_quant_scale && !aligned(pre_quant_scale, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: pre_quant_scale must be 16-byte aligned");
+    const size_t need = nvfp4_w4a16_gemm_workspace(M, N, K, pre_quant_scale != nullptr);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+        return fail(NVFP4_ERR_WORKSPACE, "nvfp4_w4a16_gemm: workspace %zu bytes, needs %zu", workspace_bytes, need);
+    if (need > 0 && !aligned(workspace, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: workspace must be 256-byte aligned");
+    int* status = device_status_ptr();
+    if (!status) return fail(NVFP4_ERR_CUDA, "nvfp4_w4a16_gemm: no CUDA device");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (use_tc_path(M)) {
+        TcParams tp{};
+        tp.X = (const uint16_t*)X; tp.pqs = (const uint16_t*)pre_quant_scale;
+        tp.rp = (const uint8_t*)repacked; tp.Y = (uint16_t*)Y;
+        tp.M = M; tp.N = N; tp.K = K; tp.status = status;
+        tp.workspace = workspace; tp.workspace_bytes = workspace_bytes;
+        return launch_tc(tp, s);
+    }
+    const DecodePlan pl = plan_decode(M, N, K);
+    if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_gemm: K=%lld too large for the decode kernel", (long long)K);
+    DecodeParams p{};
+    p.X = (const uint16_t*)X; p.pqs = (const uint16_t*)pre_quant_scale;
+    p.rp = (const uint8_t*)repacked; p.Y = (uint16_t*)Y;
+    p.M = M; p.N = N; p.K = K;
+    p.KB = round_up(K, kBlockK) / kBlockK;
+    p.kbs = pl.kbs; p.splits = pl.splits; p.status = status;
+    return launch_decode(p, pl.MT, s);
+}

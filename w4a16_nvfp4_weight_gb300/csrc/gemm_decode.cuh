@@ -1,0 +1,27 @@
+// Launch interface of the split-K decode GEMM (few tokens).
+#pragma once
+#include "common.cuh"
+
+namespace nvfp4 {
+
+struct DecodeParams {
+    const uint16_t* X;        // BF16 [M, K]
+    const uint16_t* pqs;      // BF16 [K] AWQ pre-quant scale or nullptr
+    const uint8_t* rp;        // repacked weight
+    uint16_t* Y;              // BF16 [M, N]
+    int64_t M, N, K;
+    int64_t KB;               // 64-k blocks of the padded K
+    int kbs;                  // 64-k blocks per split
+    int splits;               // CTAs per cluster along K (<= 8)
+    int x_stride;             // shared-memory activation row stride (elements); set by the launcher
+    int* status;              // device status word
+};
+
+// Dynamic shared memory of one CTA for MT token tiles of 8 and kbs blocks.
+size_t decode_smem_bytes(int MT, int kbs);
+
+// MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
+// covered by a third grid dimension.
+nvfp4_status launch_decode(const DecodeParams& p, int MT, cudaStream_t stream);
+
+}  // namespace nvfp4
