@@ -1,0 +1,500 @@
+"""Throughput of the W4A16 NVFP4 weight-only GEMM on one GB300 (or N replicas).
+
+Default workload: the decode dense linears -- M in {1,2,4,8,16} x (K,N) in
+{(4096,4096),(4096,14336),(14336,4096),(5120,25600)}, weights quantized from
+N(0,0.02), activations ~N(0,1) BF16.  One step = the 20 GEMMs once, captured
+in a CUDA graph and replayed; every GEMM of a step reads its own weight copy
+(745 MB of distinct weights per step, larger than L2).  The metric is the
+algorithmic bytes moved per second (weights at 0.5625 B/element plus BF16
+activations in and out), with TFLOP/s beside it.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+                    [--workload decode|prefill|lmhead|moe|tails]
+
+Under torchrun each rank runs its own replica (the path has no data exchange);
+rank 0 prints one JSON line with the max-over-ranks time.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# The CPU baseline is the numpy oracle run single-threaded; pin BLAS before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+DECODE_SHAPES = [(4096, 4096), (4096, 14336), (14336, 4096), (5120, 25600)]
+DECODE_M = [1, 2, 4, 8, 16]
+
+
+def weight_bytes(N, K):
+    return N * K // 2 + N * K // 16 + 4
+
+
+def algo_bytes(M, N, K):
+    return weight_bytes(N, K) + 2 * M * K + 2 * M * N
+
+
+def flops(M, N, K):
+    return 2 * M * N * K
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                        bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                        source="measured")
+        except Exception:
+            pass
+    return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0,
+                source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["unsampled"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+# ------------------------------------------------------------------ inputs --
+def bits_tensor(bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def build_decode_workload(nv, synth, device):
+    """Weights (distinct copy per GEMM of a step) and activations."""
+    launches = []
+    base = {}
+    for si, (K, N) in enumerate(DECODE_SHAPES):
+        packed, scales, d = synth.weight_only(K, N, synth.seed_for(1, si))
+        w = nv.repack(torch.from_numpy(packed).to(device), torch.from_numpy(scales).to(device),
+                      float(d), N, K)
+        base[(K, N)] = (w, packed, scales, d)
+    r = synth.rng(synth.seed_for(1, 99))
+    for M in DECODE_M:
+        for (K, N) in DECODE_SHAPES:
+            w0 = base[(K, N)][0]
+            w = nv.NVFP4Weight(w0.buf.clone(), N, K)       # a copy per GEMM: no L2 reuse in a step
+            x_bits = synth.normal_bf16(r, (M, K))
+            launches.append(dict(M=M, K=K, N=N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits,
+                                 pqs=None, y=torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+    return launches, base
+
+
+def build_dense_workload(nv, synth, device, shapes, wl_index, awq=False):
+    launches, base = [], {}
+    r = synth.rng(synth.seed_for(wl_index, 99))
+    for si, (M, K, N) in enumerate(shapes):
+        if (K, N) not in base:
+            packed, scales, d = synth.weight_only(K, N, synth.seed_for(wl_index, si))
+            w = nv.repack(torch.from_numpy(packed).to(device), torch.from_numpy(scales).to(device),
+                          float(d), N, K)
+            base[(K, N)] = (w, packed, scales, d)
+        w = base[(K, N)][0]
+        x_bits = synth.normal_bf16(r, (M, K))
+        pqs_bits = synth.awq_scale_bits(r, K) if awq else None
+        launches.append(dict(M=M, K=K, N=N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits,
+                             pqs_bits=pqs_bits,
+                             pqs=bits_tensor(pqs_bits, device) if awq else None,
+                             y=torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+    return launches, base
+
+
+# --------------------------------------------------------------- GPU arm --
+def run_ours(args, rank, world, device):
+    import w4a16_nvfp4_weight_gb300 as nv
+    from w4a16_nvfp4_weight_gb300 import synth
+
+    nv._lib.load()
+    torch.cuda.set_device(device)
+    wl = args.workload
+    if wl == "decode":
+        launches, base = build_decode_workload(nv, synth, device)
+        config = {"workload": "decode dense linears M{1,2,4,8,16} x (K,N){(4096,4096),(4096,14336),"
+                              "(14336,4096),(5120,25600)}", "gemms_per_step": len(launches)}
+    elif wl == "prefill":
+        shapes = [(M, K, N) for M in (512, 2048, 8192) for (K, N) in ((5120, 13824), (13824, 5120), (8192, 28672))]
+        launches, base = build_dense_workload(nv, synth, device, shapes, 2, awq=args.awq)
+        config = {"workload": "prefill dense linears M{512,2048,8192} x (K,N){(5120,13824),(13824,5120),"
+                              "(8192,28672)}" + (" with AWQ" if args.awq else ""), "gemms_per_step": len(launches)}
+    elif wl == "lmhead":
+        shapes = [(M, 4096, 151936) for M in (1, 8, 256)]
+        launches, base = build_dense_workload(nv, synth, device, shapes, 4)
+        config = {"workload": "LM head M{1,8,256} x K=4096 x N=151936", "gemms_per_step": len(launches)}
+    elif wl == "tails":
+        shapes = [(M, K, N) for M in (1, 8, 256) for (K, N) in ((2064, 1000), (720, 3000))]
+        launches, base = build_dense_workload(nv, synth, device, shapes, 4)
+        config = {"workload": "odd shapes M{1,8,256} x (K,N){(2064,1000),(720,3000)}", "gemms_per_step": len(launches)}
+    else:
+        raise SystemExit(f"unknown workload {wl}")
+
+    for L in launches:
+        L["ws"] = None
+        need = nv.gemm_workspace_size(L["M"], L["N"], L["K"], L["pqs"] is not None)
+        if need:
+            L["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
+
+    def step():
+        for L in launches:
+            nv.gemm(L["x"], L["w"], pre_quant_scale=L["pqs"], out=L["y"], workspace=L["ws"])
+
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        step()
+        torch.cuda.synchronize()
+        assert nv.device_status() == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+    torch.cuda.synchronize()
+
+    bytes_step = sum(algo_bytes(L["M"], L["N"], L["K"]) for L in launches)
+    flops_step = sum(flops(L["M"], L["N"], L["K"]) for L in launches)
+    launches_per_step = sum(launch_count(nv, L) for L in launches)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    ms_step = ms / args.steps
+    assert nv.device_status() == 0
+
+    # per-launch kernel durations (CUDA events around graphs of back-to-back launches)
+    kern = kernel_timing(nv, launches, base, stream, device)
+
+    bw_unit = wl in ("decode", "lmhead", "tails")
+    e2e = run_e2e(nv, launches, stream, args, bw_unit)
+    pk = peaks()
+    if bw_unit:
+        unit, value = "GB/s", world * bytes_step / (ms_step * 1e-3) / 1e9
+        bound, ach_unit = "hbm", "GB/s"
+        achieved = kern["bytes"] / kern["seconds"] / 1e9
+        peak = pk["hbm"]
+    else:
+        unit, value = "TFLOP/s", world * flops_step / (ms_step * 1e-3) / 1e12
+        bound, ach_unit = "tensor", "TFLOP/s"
+        achieved = kern["flops"] / kern["seconds"] / 1e12
+        peak = pk["bf16_sustained"]
+    res = {
+        "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
+        "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; NVFP4 weights quantized from N(0,0.02), X~N(0,1))",
+        "config": dict(config, parallelism=f"replicas{world}" if world > 1 else "single GPU",
+                       l2="inputs larger than L2: each GEMM of a step reads its own weight copy "
+                          f"({sum(weight_bytes(L['N'], L['K']) for L in launches) / 1e6:.0f} MB per step)"),
+        "tflops": round(world * flops_step / (ms_step * 1e-3) / 1e12, 3),
+        "weight_gbs": round(world * sum(weight_bytes(L["N"], L["K"]) for L in launches) / (ms_step * 1e-3) / 1e9, 2),
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": ach_unit,
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{pk['source']} ({'HBM copy' if bound == 'hbm' else 'bf16 sustained'})",
+                     "kernel": "nvfp4::decode_kernel" if bound == "hbm" else "nvfp4::tc_gemm_kernel",
+                     "per_shape_us": kern["per_shape_us"]},
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"]},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    res["_base"] = base
+    return res
+
+
+def launch_count(nv, L):
+    """Library kernels one gemm call launches: the GEMM, plus the activation
+    scaling pass when an AWQ pre-quant scale is given."""
+    return 2 if L["pqs"] is not None else 1
+
+
+def kernel_timing(nv, launches, base, stream, device, reps=30):
+    """Average device time per launch of each shape, from CUDA events around a
+    graph of back-to-back launches that rotate over enough weight copies to
+    exceed 4x L2 (so each launch streams its weights from HBM)."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(device), "L2_cache_size") else 128 << 20
+    total_s, total_b, total_f = 0.0, 0, 0
+    per = {}
+    for L in launches:
+        key = (L["M"], L["K"], L["N"])
+        wb = weight_bytes(L["N"], L["K"])
+        copies = max(2, min(64, int(np.ceil(4 * l2 / wb))))
+        bufs = [L["w"]] + [nv.NVFP4Weight(L["w"].buf.clone(), L["N"], L["K"]) for _ in range(copies - 1)]
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    nv.gemm(L["x"], bufs[i % copies], pre_quant_scale=L["pqs"], out=L["y"], workspace=L["ws"])
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) * 1e-3 / (3 * reps)
+        per[f"{key[0]}x{key[1]}x{key[2]}"] = round(sec * 1e6, 3)
+        total_s += sec
+        total_b += algo_bytes(*key)
+        total_f += flops(*key)
+        del g, bufs
+    torch.cuda.empty_cache()
+    return dict(seconds=total_s, bytes=total_b, flops=total_f, per_shape_us=per)
+
+
+def run_e2e(nv, launches, stream, args, bw_unit):
+    """Same step through the public API with pinned host activations in and
+    host outputs back, copies inside the timed region."""
+    hx = [L["x"].cpu().pin_memory() for L in launches]
+    hy = [torch.empty(L["y"].shape, dtype=torch.bfloat16).pin_memory() for L in launches]
+    dx = [torch.empty_like(L["x"]) for L in launches]
+    steps = max(3, min(args.steps, 200))
+
+    def step():
+        for L, a, b, d in zip(launches, hx, hy, dx):
+            d.copy_(a, non_blocking=True)
+            y = nv.gemm(d, L["w"], pre_quant_scale=L["pqs"], out=L["y"], workspace=L["ws"])
+            b.copy_(y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = sum(2 * L["M"] * L["K"] for L in launches)
+    d2h = sum(2 * L["M"] * L["N"] for L in launches)
+    bytes_step = sum(algo_bytes(L["M"], L["N"], L["K"]) for L in launches)
+    flops_step = sum(flops(L["M"], L["N"], L["K"]) for L in launches)
+    v = bytes_step / (ms * 1e-3) / 1e9 if bw_unit else flops_step / (ms * 1e-3) / 1e12
+    return {"value": round(v, 2), "unit": "GB/s" if bw_unit else "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "path": "pinned host X -> device, nvfp4_w4a16_gemm via the Python binding, device Y -> pinned host"}
+
+
+# ----------------------------------------------------------- CPU baseline --
+def cpu_baseline(seconds_target=15.0, reps=None, base=None, rows_per_gemm=256):
+    """The oracle, as it stands, on a bounded sample of the decode workload:
+    every GEMM of a step restricted to a seeded subset of output rows."""
+    from oracle import dense
+    from w4a16_nvfp4_weight_gb300 import synth
+
+    r = synth.rng(4242)
+    cases = []
+    for si, (K, N) in enumerate(DECODE_SHAPES):
+        if base is not None:
+            _, packed, scales, d = base[(K, N)]
+        else:
+            packed, scales, d = synth.weight_only(K, N, synth.seed_for(1, si))
+        rows = np.sort(r.choice(N, size=rows_per_gemm, replace=False))
+        sub_p, sub_s = packed[rows], scales[rows]
+        for M in DECODE_M:
+            cases.append((M, K, sub_p, sub_s, d, synth.normal_bf16(r, (M, K))))
+    t0 = time.perf_counter()
+    n_sweeps = 0
+    b = 0
+    while True:
+        for (M, K, p, s, d, x) in cases:
+            dense.linear(x, p, s, d, True)
+            b += algo_bytes(M, rows_per_gemm, K)
+        n_sweeps += 1
+        el = time.perf_counter() - t0
+        if (reps is not None and n_sweeps >= reps) or (reps is None and el >= seconds_target):
+            break
+    return {"value": round(b / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_sweeps} sweep(s) of the 20 decode GEMMs restricted to {rows_per_gemm} seeded "
+                      f"output rows each (numpy float64 oracle, single thread), {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from w4a16_nvfp4_weight_gb300 import synth
+    base = {}
+    for si, (K, N) in enumerate(DECODE_SHAPES):
+        base[(K, N)] = (None,) + tuple(synth.weight_only(K, N, synth.seed_for(1, si)))
+    # size each step's sample so the whole run stays within about 90 s
+    t0 = time.perf_counter()
+    cpu_baseline(reps=1, base=base, rows_per_gemm=8)
+    per_row = (time.perf_counter() - t0) / 8
+    rows = int(max(1, min(256, 90.0 / (args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        cpu_baseline(reps=1, base=base, rows_per_gemm=rows)
+    t0 = time.perf_counter()
+    res = cpu_baseline(reps=args.steps, base=base, rows_per_gemm=rows)
+    el = time.perf_counter() - t0
+    return {
+        "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
+        "impl": "reference", "value": res["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"decode dense linears (bounded sample: {rows} output rows per GEMM)"},
+        "cpu_baseline": {"value": res["value"], "unit": "GB/s", "kind": "oracle", "cores": 1,
+                         "sample": res["sample"]},
+        "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def profile_case(args):
+    """One GEMM shape, 3 warm-up + 3 launches, for an ncu capture of its kernel."""
+    import w4a16_nvfp4_weight_gb300 as nv
+    from w4a16_nvfp4_weight_gb300 import synth
+    M, K, N = (int(v) for v in args.profile.split(","))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(9, 0))
+    w = nv.repack(torch.from_numpy(packed).cuda(), torch.from_numpy(scales).cuda(), float(d), N, K)
+    r = synth.rng(7)
+    x = bits_tensor(synth.normal_bf16(r, (M, K)), "cuda")
+    pqs = bits_tensor(synth.awq_scale_bits(r, K), "cuda") if args.awq else None
+    for _ in range(6):
+        y = nv.gemm(x, w, pre_quant_scale=pqs)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    print(json.dumps({"profile": [M, K, N], "awq": bool(args.awq), "ok": True}))
+
+
+# ------------------------------------------------------------ distributed --
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails"])
+    ap.add_argument("--awq", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None, metavar="M,K,N",
+                    help="run one GEMM shape 3 times after 3 warm-ups (for ncu captures); no timing")
+    args = ap.parse_args()
+    if args.profile:
+        profile_case(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    device = torch.device("cuda", local)
+    res = run_ours(args, rank, world, device)
+    base = res.pop("_base")
+    if rank == 0:
+        if not args.no_cpu_baseline and args.workload == "decode":
+            res["cpu_baseline"] = cpu_baseline(base=base)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

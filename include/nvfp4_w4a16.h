@@ -108,7 +108,7 @@ size_t nvfp4_repack_size(int64_t N, int64_t K);
  *                (rows r and r+8 of the block, k group q, 8 bytes each) and 2
  *                scale bytes at 512 + 2L.  Each 32-bit code word holds 8
  *                consecutive k: magnitude of element i in bits 4i..4i+2 and
- *                the signs of elements 0..7 in bits 15, 31, 11, 27, 7, 23, 3, 19.
+ *                the signs of elements 0..7 in bits 7, 15, 23, 31, 3, 11, 19, 27.
  *                Rows >= N and k >= K are padded with code 0 and scale 0.
  */
 nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
@@ -124,7 +124,7 @@ nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
  * W (BF16, [N, K] row-major) from a repacked weight: exactly the operand the
  * GEMM kernels feed to the tensor cores.
  *  repacked  device, as written by nvfp4_repack for the same N, K.
- *  out_bf16  device, N*K uint16, 4-byte aligned.
+ *  out_bf16  device, N*K uint16, 16-byte aligned.
  */
 nvfp4_status nvfp4_dequant(const void* repacked, int64_t N, int64_t K,
                            uint16_t* out_bf16, void* stream);
@@ -149,6 +149,11 @@ size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_q
  *                  do not matter.
  * M == 0 or N == 0 returns NVFP4_OK and launches nothing.  M <= 16 runs the
  * split-K HBM-streaming decode kernel; larger M the tensor-core tile kernel.
+ * The GEMM kernels use programmatic dependent launch: they may begin reading
+ * the repacked weight before the preceding kernel of the stream has finished
+ * (only if that kernel itself allows its dependents to start early), and read
+ * X / write Y only after it has.  So a kernel that rewrites the repacked
+ * weight must not be such an early-release kernel directly before the GEMM.
  */
 nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
                               int64_t M, int64_t N, int64_t K, void* Y,

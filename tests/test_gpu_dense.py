@@ -32,7 +32,7 @@ def _unrepack(buf, N, K):
     assert int(hdr[:4].view(np.uint32)[0]) == 0x34504E56
     Np, Kp = -(-N // 256) * 256, -(-K // 64) * 64
     KB = Kp // 64
-    sign_pos = [15, 31, 11, 27, 7, 23, 3, 19]
+    sign_pos = [7, 15, 23, 31, 3, 11, 19, 27]
     codes = np.zeros((Np, Kp), dtype=np.uint8)
     scales = np.zeros((Np, Kp // 16), dtype=np.uint8)
     atoms = b[4352:4352 + (Np // 16) * KB * 576].reshape(Np // 256, KB, 16, 576)
@@ -223,3 +223,16 @@ def test_lm_head_full_size_sampled():
         yb = gu.tensor_to_bits(y)
         _, ref = dense.linear(x_bits, packed, scales, d, True, rows=rows)
         gu.compare(yb[:, rows], ref, f"LM head M={M}")
+
+
+def test_gemm_bitwise_deterministic_across_runs():
+    """Many waves of split-K clusters (ring reuse in every CTA): repeated runs must
+    agree bit for bit -- the split-K reduction has a fixed order."""
+    M, K, N = 64, 5120, 13824
+    packed, scales, d = synth.weight_only(K, N, 11)
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    x = gu.bits_to_bf16_tensor(synth.normal_bf16(synth.rng(5), (M, K)))
+    outs = [gu.tensor_to_bits(nv.gemm(x, w)) for _ in range(5)]
+    gu.check_device_status()
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])

@@ -80,24 +80,22 @@ struct DecodePlan {
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
     DecodePlan pl{};
     pl.MT = M <= 8 ? 1 : 2;
+    const int64_t TOK = 8 * pl.MT;
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
     const int64_t RG = ceil_div(N, 128);
-    const int64_t base = RG * ceil_div(M, 8 * pl.MT);
-    const int64_t target = 2LL * sm_count();
-    int64_t splits = std::min<int64_t>(std::min<int64_t>(8, KB), std::max<int64_t>(1, ceil_div(target, base)));
-    int64_t kbs = ceil_div(KB, splits);
-    // keep the activation slice small enough for two CTAs per SM when possible
-    const size_t soft = 100 * 1024, hard = 227 * 1024;
-    while (decode_smem_bytes(pl.MT, (int)kbs) > soft && splits < std::min<int64_t>(8, KB)) {
-        ++splits;
-        kbs = ceil_div(KB, splits);
-    }
+    const int64_t base = RG * ceil_div(M, TOK);
+    // two resident CTAs per SM: split K until the grid covers them
+    int64_t splits = std::min<int64_t>(std::min<int64_t>(8, KB), std::max<int64_t>(1, ceil_div(2LL * sm_count(), base)));
+    const int64_t kbs = ceil_div(KB, splits);
     splits = ceil_div(KB, kbs);
     pl.splits = (int)splits;
     pl.kbs = (int)kbs;
-    pl.ok = decode_smem_bytes(pl.MT, (int)kbs) <= hard;
+    pl.ok = true;
     return pl;
 }
+
+// Bytes of the AWQ-scaled activation copy the decode path keeps in the workspace.
+size_t awq_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
 
 }  // namespace nvfp4
 
@@ -127,7 +125,7 @@ extern "C" nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stre
 extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
     if (use_tc_path(M)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
-    return 0;
+    return has_pre_quant_scale ? awq_bytes(M, K) : 0;
 }
 
 extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
@@ -158,8 +156,16 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, co
     }
     const DecodePlan pl = plan_decode(M, N, K);
     if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_gemm: K=%lld too large for the decode kernel", (long long)K);
+    const uint16_t* xin = (const uint16_t*)X;
+    if (pre_quant_scale) {
+        // x' = RN_bf16(x * pre_quant_scale) into the workspace, then the GEMM reads x'
+        nvfp4_status st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)pre_quant_scale,
+                                           (uint16_t*)workspace, M, K, s);
+        if (st != NVFP4_OK) return st;
+        xin = (const uint16_t*)workspace;
+    }
     DecodeParams p{};
-    p.X = (const uint16_t*)X; p.pqs = (const uint16_t*)pre_quant_scale;
+    p.X = xin; p.pqs = nullptr;
     p.rp = (const uint8_t*)repacked; p.Y = (uint16_t*)Y;
     p.M = M; p.N = N; p.K = K;
     p.KB = round_up(K, kBlockK) / kBlockK;

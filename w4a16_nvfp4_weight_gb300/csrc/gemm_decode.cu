@@ -1,16 +1,26 @@
 // Decode-shaped W4A16 GEMM (few tokens): split-K, HBM-streaming, with the
 // dequant fused into the tensor-core operand registers.
 //
-// The weight is the only large operand, so every byte of it is read once with
-// 128-bit streaming loads.  Each warp owns 16 weight rows; per 64-k atom a lane
-// loads 16 code bytes and 2 scale bytes, looks its two group tables up in
-// shared memory and expands the codes straight into mma.sync A fragments
-// (weights on the M side, tokens on the N side).  Within a 16-element group
-// the MMA's k order is permuted so that one lane consumes one whole group of
-// one row per four MMAs; the activation fragments follow the same permutation,
-// so the dot products are unchanged.  K is split across the CTAs of a thread
-// block cluster, which reduce their FP32 partials through distributed shared
-// memory in rank order: deterministic, and no global workspace.
+// The weight is the only large operand, so every byte of it is read once.  A
+// CTA owns 128 weight rows (8 consumer warps x 16 rows) and one K slice.  A
+// producer warp streams the slice through a 3-stage shared-memory ring with
+// bulk (TMA) copies: per stage three 64-k blocks of weights (3 x 4608
+// contiguous bytes) and the matching activation chunk, one copy per token
+// row.  Per 64-k atom a lane reads 16 code bytes and 2 scale bytes, looks its
+// two group tables up and expands the codes straight into mma.sync A
+// fragments (weights on the M side, tokens on the N side).  Within a
+// 16-element group the MMA's k order is permuted so that one lane consumes one
+// whole group of one row per four MMAs; the activation fragments follow the
+// same permutation, so the dot products are unchanged.  K is split across the
+// CTAs of a thread-block cluster, which reduce their FP32 partials through
+// distributed shared memory in rank order: deterministic, and no global
+// workspace.  The AWQ pre-quant scale, when present, is applied by a small
+// pass that writes x' = RN_bf16(x * s) into the workspace first.
+//
+// The kernel is launched with programmatic dependent launch: it lets the next
+// kernel of the stream start early, and it streams its first weight stages
+// before waiting for the previous kernel; activations are read only after
+// that wait.
 //
 // Method: "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper"
 // (Description / Changes table: dequantize the NVFP4 weight each forward step
@@ -20,6 +30,7 @@
 
 #include "common.cuh"
 #include "gemm_decode.cuh"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -35,15 +46,31 @@ __device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], 
 
 namespace {
 
-constexpr int kWarps = 8;                     // 8 x 16 = 128 weight rows per CTA
+constexpr int kWarps = 8;                      // consumer warps: 8 x 16 = 128 weight rows
+constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
 constexpr int kRowsPerCta = kWarps * kAtomRows;
-constexpr int kUnroll = 4;                    // atoms in flight per warp
+constexpr int kStages = 3;
+constexpr int kBlocksPerStage = 3;             // 64-k blocks per ring stage
+constexpr uint32_t kBlockBytes = kWarps * kAtomBytes;          // 4608: 128 rows x 64 k, contiguous
+constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
+constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;      // activation row stride in a stage (+16 B)
 
-// Process one atom held in registers: expand and issue 4 x MT MMAs.
+__host__ __device__ constexpr size_t x_stage_bytes(int tok) { return (size_t)tok * kXRowElems * 2; }
+__host__ __device__ constexpr size_t stage_bytes(int tok) { return kWeightStageBytes + x_stage_bytes(tok); }
+
+struct Smem {
+    // offsets in bytes from the dynamic shared memory base
+    static constexpr size_t bars = 0;              // full[S], empty[S], lut_bar
+    static constexpr size_t flag = 120;            // header accepted (written by the producer)
+    static constexpr size_t lut = 128;
+    static constexpr size_t ring = lut + kLutBytes;
+};
+
+// Expand one atom held in registers and issue 4 x MT MMAs; xrow points at this
+// lane's token row and group inside the stage's activation chunk.
 template <int MT>
 __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const uint4* lut,
-                                         const uint16_t* xs, int x_stride, int kl, int lane,
-                                         float acc[MT][4]) {
+                                         const uint16_t* xrow, float acc[MT][4]) {
     const Lut t0 = lut_from_uint4(lut[sc2 & 0xFF]);
     const Lut t1 = lut_from_uint4(lut[(sc2 >> 8) & 0xFF]);
     uint32_t ra[8], rb[8];
@@ -51,26 +78,34 @@ __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const 
     expand8(codes.y, t0, ra + 4);
     expand8(codes.z, t1, rb);
     expand8(codes.w, t1, rb + 4);
-    const int g = lane >> 2, q = lane & 3;
     #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t a[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
-        #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const uint2 b = *reinterpret_cast<const uint2*>(xs + (mt * 8 + g) * x_stride + kl + q * 16 + 4 * j);
-            mma_bf16_16816(acc[mt], a, b.x, b.y);
-        }
+    for (int mt = 0; mt < MT; ++mt) {
+        const uint4 b01 = *reinterpret_cast<const uint4*>(xrow + mt * 8 * kXRowElems);
+        const uint4 b23 = *reinterpret_cast<const uint4*>(xrow + mt * 8 * kXRowElems + 8);
+        const uint32_t a0[4] = {ra[0], rb[0], ra[1], rb[1]};
+        const uint32_t a1[4] = {ra[2], rb[2], ra[3], rb[3]};
+        const uint32_t a2[4] = {ra[4], rb[4], ra[5], rb[5]};
+        const uint32_t a3[4] = {ra[6], rb[6], ra[7], rb[7]};
+        mma_bf16_16816(acc[mt], a0, b01.x, b01.y);
+        mma_bf16_16816(acc[mt], a1, b01.z, b01.w);
+        mma_bf16_16816(acc[mt], a2, b23.x, b23.y);
+        mma_bf16_16816(acc[mt], a3, b23.z, b23.w);
     }
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads)
 decode_kernel(const DecodeParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint4* lut = reinterpret_cast<uint4*>(smem);
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + kLutBytes);
-    float* part = reinterpret_cast<float*>(smem + kLutBytes + (size_t)MT * 8 * p.x_stride * 2);
+    extern __shared__ __align__(128) uint8_t smem[];
     constexpr int TOK = 8 * MT;
+    constexpr size_t kStageBytes = stage_bytes(TOK);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::bars);
+    uint64_t* empty = full + kStages;
+    uint64_t* lut_bar = empty + kStages;
+    volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + Smem::flag);
+    uint4* lut = reinterpret_cast<uint4*>(smem + Smem::lut);
+    uint8_t* ring = smem + Smem::ring;
+    float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -78,47 +113,34 @@ decode_kernel(const DecodeParams p) {
     const int split = blockIdx.y;
     const int64_t m0 = (int64_t)blockIdx.z * TOK;
 
-    // Every CTA reads the same header, so all CTAs of a cluster agree.
-    const Header* hdr = reinterpret_cast<const Header*>(p.rp);
-    if (hdr->magic != kMagic || hdr->N != p.N || hdr->K != p.K) {
-        if (tid == 0) record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
-        return;
-    }
-
-    for (int i = tid; i < 256; i += blockDim.x)
-        lut[i] = reinterpret_cast<const uint4*>(p.rp + kHeaderBytes)[i];
-
     const int kb0 = split * p.kbs;
     const int kb1 = min(kb0 + p.kbs, (int)p.KB);
-    const int nk = (kb1 - kb0) * kBlockK;           // local k extent
-    // Stage this split's activation slice (zero beyond M and K), applying the
-    // AWQ pre-quant scale when present.
-    const int chunks = nk / 8;
-    for (int i = tid; i < TOK * chunks; i += blockDim.x) {
-        const int t = i / chunks, c = i % chunks;
-        const int64_t m = m0 + t;
-        const int64_t k = (int64_t)kb0 * kBlockK + c * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < p.M && k < p.K) {
-            v = *reinterpret_cast<const uint4*>(p.X + m * p.K + k);
-            if (p.pqs != nullptr) {
-                const uint4 s = *reinterpret_cast<const uint4*>(p.pqs + k);
-                uint32_t xv[4] = {v.x, v.y, v.z, v.w};
-                const uint32_t sv[4] = {s.x, s.y, s.z, s.w};
-                #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint16_t lo = awq_mul_bf16((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
-                    const uint16_t hi = awq_mul_bf16((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
-                    xv[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-                }
-                v = make_uint4(xv[0], xv[1], xv[2], xv[3]);
-            }
+    const int nkb = kb1 - kb0;
+    const int nst = (nkb + kBlocksPerStage - 1) / kBlocksPerStage;
+    const int64_t m_left = p.M - m0;
+    const int rows_x = (int)(m_left < TOK ? m_left : TOK);           // token rows with data (>= 1)
+    const int64_t nt = ((int64_t)rg * kRowsPerCta) / kTileRows;
+    const int rb0 = (rg * kRowsPerCta) % kTileRows / kAtomRows;      // 0 or 8
+    const uint8_t* wsrc = p.rp + kTilesOffset + atom_offset(nt, kb0, rb0, p.KB);
+    const size_t kb_stride = (size_t)kAtomsPerTileK * kAtomBytes;
+
+    if (tid == 0) {
+        pdl_launch_dependents();          // the next GEMM may start its weight prefetch
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
         }
-        uint16_t* dst = xs + t * p.x_stride + c * 8;
-        // x_stride is a multiple of 4 elements: 8-byte aligned rows
-        reinterpret_cast<uint2*>(dst)[0] = make_uint2(v.x, v.y);
-        reinterpret_cast<uint2*>(dst)[1] = make_uint2(v.z, v.w);
+        mbar_init(lut_bar, 1);
+        fence_mbar_init();
     }
+    // Zero every activation chunk once: token rows without data and the k tail
+    // past K are never written by a copy, so they read as zeros (or, for the
+    // k tail, as earlier values of the same row, which meet zero weights).
+    for (int s = 0; s < kStages; ++s) {
+        uint4* xsb = reinterpret_cast<uint4*>(ring + s * kStageBytes + kWeightStageBytes);
+        for (int i = tid; i < (int)(x_stage_bytes(TOK) / 16); i += kThreads) xsb[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();      // these generic writes before later bulk copies into the same bytes
     __syncthreads();
 
     float acc[MT][4];
@@ -127,77 +149,168 @@ decode_kernel(const DecodeParams p) {
         #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
 
-    const int64_t rbg = (int64_t)rg * kWarps + warp;          // global 16-row block
-    if (rbg * kAtomRows < p.N) {
-        const int64_t nt = rbg / kAtomsPerTileK, rb = rbg % kAtomsPerTileK;
-        const uint8_t* tiles = p.rp + kTilesOffset;
-        const size_t kb_stride = (size_t)kAtomsPerTileK * kAtomBytes;
-        const uint8_t* a0 = tiles + atom_offset(nt, kb0, rb, p.KB);
-        int kb = kb0;
-        for (; kb + kUnroll <= kb1; kb += kUnroll) {
-            uint4 c[kUnroll];
-            uint32_t s[kUnroll];
-            #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const uint8_t* a = a0 + (size_t)(kb - kb0 + u) * kb_stride;
-                c[u] = ldg_stream(a + 16 * lane);
-                s[u] = ldg_u16(a + kAtomCodeBytes + 2 * lane);
+    if (warp == kWarps) {
+        // ---------------- producer: weights and activation chunks through the ring
+        if (lane == 0) {
+            // Check the header before touching the rest of the buffer; every CTA
+            // sees the same header, so a mismatch skips the whole cluster.
+            const Header* hdr = reinterpret_cast<const Header*>(p.rp);
+            const bool hdr_ok = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            *hdr_flag = hdr_ok ? 1 : 0;
+            if (!hdr_ok) {
+                record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
+                mbar_arrive(lut_bar);              // release the consumers; nothing is copied
+            } else {
+                // Weights and the magnitude table do not depend on the preceding
+                // kernel in the stream, activations may: the first stages' weight
+                // copies go out before the programmatic-launch wait, every
+                // activation copy after it.
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                bulk_g2s(lut, p.rp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                auto stage_blocks = [&](int i) { return min(kBlocksPerStage, nkb - i * kBlocksPerStage); };
+                auto stage_xk = [&](int i) {
+                    const int64_t kx_left = p.K - (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
+                    const int full_k = stage_blocks(i) * kBlockK;
+                    return (int)(kx_left < full_k ? kx_left : full_k);          // multiple of 16
+                };
+                auto issue_weights = [&](int i) {
+                    const int s = i % kStages, nb = stage_blocks(i);
+                    uint8_t* st = ring + s * kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * kBlockBytes + (size_t)rows_x * stage_xk(i) * 2));
+                    for (int b = 0; b < nb; ++b)
+                        bulk_g2s(st + b * kBlockBytes, wsrc + (size_t)(i * kBlocksPerStage + b) * kb_stride,
+                                 kBlockBytes, &full[s]);
+                };
+                auto issue_x = [&](int i) {
+                    const int s = i % kStages, xk = stage_xk(i);
+                    const int64_t kx = (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
+                    uint16_t* xsb = reinterpret_cast<uint16_t*>(ring + s * kStageBytes + kWeightStageBytes);
+                    for (int t = 0; t < rows_x; ++t)
+                        bulk_g2s(xsb + t * kXRowElems, p.X + (m0 + t) * p.K + kx, (uint32_t)xk * 2, &full[s]);
+                };
+                const int first = min(nst, kStages);
+                for (int i = 0; i < first; ++i) issue_weights(i);
+                pdl_wait_previous();
+                for (int i = 0; i < first; ++i) issue_x(i);
+                int issued = first;
+                bool ok = true;
+                for (int i = first; i < nst && ok; ++i) {
+                    const int s = i % kStages;
+                    ok = mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.status);
+                    if (!ok) break;
+                    issue_weights(i);
+                    issue_x(i);
+                    ++issued;
+                }
+                // never leave a copy in flight into this CTA's shared memory
+                mbar_wait(lut_bar, 0, p.status);
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&full[i % kStages], (i / kStages) & 1, p.status);
             }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers
+        const bool rows_valid = (int64_t)rg * kRowsPerCta + warp * kAtomRows < p.N;
+        const int g = lane >> 2, q = lane & 3;
+        bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        const bool work = rows_valid;
+        for (int i = 0; i < nst && ok; ++i) {
+            const int s = i % kStages;
+            if (!mbar_wait(&full[s], (i / kStages) & 1, p.status)) break;
+            const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
+            const uint8_t* st = ring + s * kStageBytes;
+            uint4 codes[kBlocksPerStage];
+            uint32_t sc[kBlocksPerStage];
             #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                atom_mma<MT>(c[u], s[u], lut, xs, p.x_stride, (kb - kb0 + u) * kBlockK, lane, acc);
+            for (int b = 0; b < kBlocksPerStage; ++b) {
+                const uint8_t* a = st + b * kBlockBytes + warp * kAtomBytes;
+                codes[b] = *reinterpret_cast<const uint4*>(a + 16 * lane);
+                sc[b] = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
+            }
+            if (work) {
+                const uint16_t* xrow = reinterpret_cast<const uint16_t*>(st + kWeightStageBytes) +
+                                       g * kXRowElems + q * 16;
+                #pragma unroll
+                for (int b = 0; b < kBlocksPerStage; ++b)
+                    if (b < nb) atom_mma<MT>(codes[b], sc[b], lut, xrow + b * kBlockK, acc);
+            }
+            fence_proxy_async();           // reads of the stage before the next bulk copy into it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
-        for (; kb < kb1; ++kb) {
-            const uint8_t* a = a0 + (size_t)(kb - kb0) * kb_stride;
-            const uint4 c = ldg_stream(a + 16 * lane);
-            const uint32_t s = ldg_u16(a + kAtomCodeBytes + 2 * lane);
-            atom_mma<MT>(c, s, lut, xs, p.x_stride, (kb - kb0) * kBlockK, lane, acc);
-        }
-    }
 
-    // Partials: part[row][token], row = warp*16 + (g or g+8), token = mt*8 + 2c (+1)
-    {
-        const int g = lane >> 2, c = lane & 3;
+        // Push each partial to the CTA that reduces it: output e = token * 128 + row
+        // belongs to rank e / share and lands in that rank's slot for this rank.
+        const int c = lane & 3;
+        const int total = kRowsPerCta * TOK;
+        const int share = (total + p.splits - 1) / p.splits;
         #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            float* r0 = part + (warp * 16 + g) * TOK + mt * 8 + 2 * c;
-            float* r8 = part + (warp * 16 + g + 8) * TOK + mt * 8 + 2 * c;
-            r0[0] = acc[mt][0]; r0[1] = acc[mt][1];
-            r8[0] = acc[mt][2]; r8[1] = acc[mt][3];
+            #pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int row = warp * 16 + g + (v >= 2 ? 8 : 0);
+                const int t = mt * 8 + 2 * c + (v & 1);
+                const int e = t * kRowsPerCta + row;
+                float* dst = cluster.map_shared_rank(part, e / share);
+                dst[split * share + e % share] = acc[mt][v];
+            }
         }
     }
-    cluster.sync();
+    cluster.sync();     // all partials have landed in their reducing CTA
 
-    // Each CTA of the cluster reduces a contiguous share of the outputs, summing
-    // the partials of ranks 0..splits-1 in order.
-    const int total = kRowsPerCta * TOK;
-    const int splits = p.splits;
-    const int share = (total + splits - 1) / splits;
-    const int e0 = split * share, e1 = min(total, e0 + share);
-    for (int e = e0 + tid; e < e1; e += blockDim.x) {
-        const int t = e / kRowsPerCta, row = e % kRowsPerCta;      // consecutive e -> consecutive n
-        float sum = 0.0f;
-        for (int r = 0; r < splits; ++r) {
-            const float* peer = cluster.map_shared_rank(part, r);
-            sum += peer[row * TOK + t];
+    // Reduce this rank's share from local shared memory, ranks in order.
+    if (*hdr_flag != 0) {
+        const int total = kRowsPerCta * TOK;
+        const int share = (total + p.splits - 1) / p.splits;
+        const int e0 = split * share, e1 = min(total, e0 + share);
+        for (int e = e0 + tid; e < e1; e += kThreads) {
+            float sum = 0.0f;
+            for (int r = 0; r < p.splits; ++r) sum += part[r * share + (e - e0)];
+            const int t = e / kRowsPerCta, row = e % kRowsPerCta;      // consecutive e -> consecutive n
+            const int64_t n = (int64_t)rg * kRowsPerCta + row;
+            const int64_t m = m0 + t;
+            if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_bf16_bits(sum);
         }
-        const int64_t n = (int64_t)rg * kRowsPerCta + row;
-        const int64_t m = m0 + t;
-        if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_bf16_bits(sum);
     }
-    cluster.sync();   // keep this CTA's partials alive until every peer has read them
+}
+
+// x' = RN_bf16(x * pre_quant_scale), one thread per 8 elements.
+__global__ void awq_scale_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
+                                 uint16_t* __restrict__ Xs, int64_t M, int64_t K) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (i >= M * K) return;
+    const int64_t k = i % K;
+    const uint4 v = *reinterpret_cast<const uint4*>(X + i);
+    const uint4 s = *reinterpret_cast<const uint4*>(pqs + k);
+    const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t sv[4] = {s.x, s.y, s.z, s.w};
+    uint32_t o[4];
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint16_t lo = awq_mul_bf16((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
+        const uint16_t hi = awq_mul_bf16((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
+        o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    *reinterpret_cast<uint4*>(Xs + i) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int MT, int kbs) {
-    const int x_stride = kbs * kBlockK + 4;
-    return kLutBytes + (size_t)MT * 8 * x_stride * 2 + (size_t)kRowsPerCta * MT * 8 * 4;
+nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* Xs, int64_t M, int64_t K,
+                              cudaStream_t stream) {
+    const int64_t n8 = M * K / 8;
+    awq_scale_kernel<<<(unsigned)ceil_div(n8, 256), 256, 0, stream>>>(X, pqs, Xs, M, K);
+    return check_cuda(cudaGetLastError(), "AWQ activation scaling: launch");
+}
+
+size_t decode_smem_bytes(int MT, int /*kbs*/) {
+    // partial slots: splits x ceil(128 * TOK / splits) floats <= 128 * TOK + 7
+    return Smem::ring + kStages * stage_bytes(8 * MT) + ((size_t)kRowsPerCta * MT * 8 + 8) * 4;
 }
 
 nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream) {
     DecodeParams p = p_in;
-    p.x_stride = p.kbs * kBlockK + 4;
     const size_t smem = decode_smem_bytes(MT, p.kbs);
     const void* fn = MT == 1 ? (const void*)decode_kernel<1> : (const void*)decode_kernel<2>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -206,16 +319,18 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream
     const int64_t mchunks = ceil_div(p.M, 8 * MT);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rgs, (unsigned)p.splits, (unsigned)mchunks);
-    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)p.splits;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (MT == 1) e = cudaLaunchKernelEx(&cfg, decode_kernel<1>, p);
     else e = cudaLaunchKernelEx(&cfg, decode_kernel<2>, p);
     return check_cuda(e, "decode GEMM: launch");

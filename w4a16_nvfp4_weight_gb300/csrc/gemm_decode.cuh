@@ -6,14 +6,13 @@ namespace nvfp4 {
 
 struct DecodeParams {
     const uint16_t* X;        // BF16 [M, K]
-    const uint16_t* pqs;      // BF16 [K] AWQ pre-quant scale or nullptr
+    const uint16_t* pqs;      // unused by the kernel: AWQ scaling runs first (launch_awq_scale)
     const uint8_t* rp;        // repacked weight
     uint16_t* Y;              // BF16 [M, N]
     int64_t M, N, K;
     int64_t KB;               // 64-k blocks of the padded K
     int kbs;                  // 64-k blocks per split
     int splits;               // CTAs per cluster along K (<= 8)
-    int x_stride;             // shared-memory activation row stride (elements); set by the launcher
     int* status;              // device status word
 };
 
@@ -23,5 +22,9 @@ size_t decode_smem_bytes(int MT, int kbs);
 // MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
 // covered by a third grid dimension.
 nvfp4_status launch_decode(const DecodeParams& p, int MT, cudaStream_t stream);
+
+// Xs = RN_bf16(X * pqs) for an M x K activation (K a multiple of 16).
+nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* Xs, int64_t M, int64_t K,
+                              cudaStream_t stream);
 
 }  // namespace nvfp4

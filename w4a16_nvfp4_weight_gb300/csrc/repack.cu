@@ -83,7 +83,7 @@ __global__ void lut_kernel(uint8_t* out, float g, int64_t N, int64_t K, int64_t 
 
 // Natural order word (nibble i = code of element i) -> sign-split word.
 __device__ __forceinline__ uint32_t to_sign_split(uint32_t w) {
-    const int sign_pos[8] = {15, 31, 11, 27, 7, 23, 3, 19};
+    const int sign_pos[8] = {7, 15, 23, 31, 3, 11, 19, 27};
     uint32_t out = w & 0x77777777u;
     #pragma unroll
     for (int i = 0; i < 8; ++i) out |= ((w >> (4 * i + 3)) & 1u) << sign_pos[i];
