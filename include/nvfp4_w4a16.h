@@ -185,7 +185,9 @@ size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t 
  *                    [E+1] or NULL (exclusive scan of per-expert counts).
  * Only the weights of experts that received at least one token are read.
  * T == 0 returns NVFP4_OK and launches nothing.  Limits: E <= 256, topk <= 16,
- * topk <= E, H and I multiples of 64.
+ * topk <= E, H and I multiples of 64, T * topk / 8 + E below 65536 (one call).
+ * workspace: >= nvfp4_w4a16_moe_workspace(...) bytes, 256-byte aligned; it holds
+ * the routing tables, the intermediate activations and the FP32 per-slot rows.
  */
 nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
                                      const void* fc1, const void* fc2,

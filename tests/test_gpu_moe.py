@@ -1,0 +1,133 @@
+"""GPU parity of the grouped top-k MoE layer against the CPU oracle.
+
+Routing indices, the permutation and the per-expert offsets are compared bit
+for bit; routing weights to float32 rounding; the layer output within the
+parity bar (relative Frobenius <= 2e-3, max-abs <= 2e-2 * max|ref|) against the
+oracle's BF16 output.  The full 128-expert layer is checked on sampled tokens.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import w4a16_nvfp4_weight_gb300 as nv
+from oracle import moe as omoe
+from tests import gpu_util as gu
+from w4a16_nvfp4_weight_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_experts(weights, N, K):
+    """Repack E expert matrices back to back into one device buffer."""
+    size = nv.repack_size(N, K)
+    buf = torch.empty(len(weights) * size, dtype=torch.uint8, device="cuda")
+    for e, (p, s, d) in enumerate(weights):
+        nv.repack(gu.u8(p), gu.u8(s), float(d), N, K, out=buf[e * size:(e + 1) * size])
+    return buf
+
+
+def _run(c, awq=False):
+    fc1 = _device_experts(c.fc1, 2 * c.I, c.H)
+    fc2 = _device_experts(c.fc2, c.H, c.I)
+    x = gu.bits_to_bf16_tensor(c.x_bits)
+    logits = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
+    pqs = gu.bits_to_bf16_tensor(c.pqs_bits) if awq else None
+    out, r = nv.moe_grouped(x, logits, fc1, fc2, c.topk, c.I, fc1_pre_quant_scale=pqs, return_routing=True)
+    gu.check_device_status()
+    return gu.tensor_to_bits(out), {k: v.cpu().numpy() for k, v in r.items()}
+
+
+def _oracle(c, awq=False, tokens=None):
+    return omoe.moe_layer(c.x_bits, c.logits, [(p, s, d, True) for p, s, d in c.fc1],
+                          [(p, s, d, True) for p, s, d in c.fc2], c.topk,
+                          pqs_bits=c.pqs_bits if awq else None, tokens=tokens)
+
+
+def _check_routing(got, ref, T, topk, E):
+    assert np.array_equal(got["idx"].reshape(T, topk), ref["idx"])
+    assert np.array_equal(got["offsets"], ref["offsets"])
+    assert np.array_equal(got["perm"], ref["perm"])
+    assert np.allclose(got["p"].reshape(T, topk), ref["p"], rtol=2e-6, atol=1e-7)
+
+
+def _small_case(T, E, topk, H, I, seed, awq=False):
+    r = synth.rng(seed + 77)
+    fc1 = [synth.quantize(synth.normal_weight(r, 2 * I, H)) for _ in range(E)]
+    fc2 = [synth.quantize(synth.normal_weight(r, H, I)) for _ in range(E)]
+    return synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=awq)
+
+
+@pytest.mark.parametrize("T,E,topk,H,I", [(3, 4, 2, 64, 64), (64, 16, 4, 256, 128), (37, 8, 3, 192, 320),
+                                          (5, 1, 1, 128, 64), (200, 32, 8, 128, 64)])
+def test_moe_small_full_compare(T, E, topk, H, I):
+    c = _small_case(T, E, topk, H, I, seed=T * 31 + E)
+    out, routing = _run(c)
+    ref = _oracle(c)
+    _check_routing(routing, ref, T, topk, E)
+    gu.compare(out, ref["out_bits"], f"MoE T={T} E={E} k={topk}")
+
+
+def test_moe_awq_and_dropped_scale_control():
+    c = _small_case(10, 8, 2, 128, 64, seed=5, awq=True)
+    out, routing = _run(c, awq=True)
+    ref = _oracle(c, awq=True)
+    _check_routing(routing, ref, 10, 2, 8)
+    gu.compare(out, ref["out_bits"], "MoE AWQ")
+    out_plain, _ = _run(c, awq=False)
+    with pytest.raises(AssertionError):
+        gu.compare(out_plain, ref["out_bits"], "MoE dropped AWQ")
+
+
+def test_moe_ties_pick_lower_expert():
+    c = _small_case(4, 8, 3, 64, 64, seed=9)
+    c.logits[:] = 0.0
+    c.logits[1, [5, 2, 7]] = 1.5          # three-way tie at the top
+    c.logits[2, :] = -0.0
+    out, routing = _run(c)
+    ref = _oracle(c)
+    _check_routing(routing, ref, 4, 3, 8)
+    assert routing["idx"].reshape(4, 3)[1].tolist() == [2, 5, 7]
+    gu.compare(out, ref["out_bits"], "MoE ties")
+
+
+def test_moe_zero_tokens_launch_nothing():
+    c = _small_case(0, 4, 2, 64, 64, seed=1)
+    fc1 = _device_experts(c.fc1, 128, 64)
+    fc2 = _device_experts(c.fc2, 64, 64)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((0, 4), dtype=torch.float32, device="cuda")
+    out = nv.moe_grouped(x, logits, fc1, fc2, 2, 64)
+    assert out.shape == (0, 64)
+    gu.check_device_status()
+
+
+def test_moe_deterministic():
+    c = _small_case(64, 16, 4, 256, 128, seed=3)
+    a, _ = _run(c)
+    b, _ = _run(c)
+    assert np.array_equal(a, b)
+
+
+@pytest.fixture(scope="module")
+def full_experts():
+    """The 128-expert layer: FC1 [1536 x 2048], FC2 [2048 x 768] per expert."""
+    E, H, I = 128, 2048, 768
+    fc1, fc2 = synth.moe_weights(E, H, I, synth.seed_for(3, 500))
+    return E, H, I, fc1, fc2, _device_experts(fc1, 2 * I, H), _device_experts(fc2, H, I)
+
+
+@pytest.mark.parametrize("T", [1, 16, 256, 4096])
+def test_moe_full_size_sampled(full_experts, T):
+    E, H, I, fc1, fc2, d1, d2 = full_experts
+    c = synth.moe_case(T, synth.seed_for(3, T), E=E, topk=8, H=H, I=I, weights=(fc1, fc2))
+    x = gu.bits_to_bf16_tensor(c.x_bits)
+    logits = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
+    out, r = nv.moe_grouped(x, logits, d1, d2, 8, I, return_routing=True)
+    gu.check_device_status()
+    out = gu.tensor_to_bits(out)
+    routing = {k: v.cpu().numpy() for k, v in r.items()}
+    tokens = sorted(set([0, T - 1, T // 2]))
+    ref = _oracle(c, tokens=tokens)
+    _check_routing(routing, ref, T, 8, E)
+    gu.compare(out[tokens], ref["out_bits"], f"MoE T={T} sampled")

@@ -125,6 +125,9 @@ inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // nonzero nvfp4_status there instead of trapping); nullptr on failure.
 int* device_status_ptr();
 
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
 // Kernels record the first error only.
 __device__ __forceinline__ void record_status(int* status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);

@@ -1,13 +1,562 @@
-// Grouped top-k MoE layer (placeholder until the routed-expert kernels land).
+// Grouped top-k MoE layer with W4A16 NVFP4 experts.
+//
+//   route    -- one warp per token: top-k of the FP32 router logits (ties to
+//               the lower expert index, slots in descending-logit order) and
+//               p = softmax over the k selected logits.
+//   permute  -- one CTA: per-expert counts, offsets (exclusive scan), a stable
+//               counting sort of the routing slots t*k+j by expert (so by
+//               expert, then token, then slot), its inverse, and a list of
+//               work items (expert, first permuted row, rows <= TOK).
+//   fc1      -- per work item and 64 intermediate columns: the gate rows and
+//               the matching up rows of the expert's FC1 weight, streamed like
+//               the dense decode kernel (bulk-copy ring, split-K across a
+//               cluster, push-based reduction); the epilogue applies
+//               h = RN_bf16(silu(g) * u) and writes H in permuted row order.
+//   fc2      -- the same over FC2 with H as input; the epilogue scales by the
+//               slot's routing weight and writes FP32 rows per routing slot.
+//   combine  -- out[t] = RN_bf16(sum over slots j of the FP32 rows), in slot
+//               order.
+// Only experts that received tokens have work items, so only their weights are
+// read.  Nothing is read back to the host: the grid is sized by an upper bound
+// on the number of work items, surplus CTAs exit at once, and the whole layer
+// can be captured in a CUDA graph.
+//
+// Method: "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper"
+// (Changes table, MoE row: dequantize only the active experts, then a BF16
+// fused MoE); SGLang PR 40022 (review: gated experts carry a fused gate/up FC1);
+// "[None][fix] Apply the NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL"
+// (Description: FC1's activation is multiplied by the pre-quant scale before
+// the GEMM; a zero-token chunk launches no kernel).
+#include <algorithm>
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+#include "gemm_decode.cuh"
+#include "ptx.cuh"
+#include "stream_mma.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopk = 16;
+
+// ------------------------------------------------------------------- route --
+__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int topk,
+                             int32_t* __restrict__ idx, float* __restrict__ wts) {
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    float l[kMaxExperts / 32];
+    uint32_t used = 0;
+    #pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        l[i] = e < E ? logits[t * E + e] : 0.0f;
+        if (e >= E) used |= 1u << i;
+    }
+    float sel_v[kMaxTopk];
+    int sel_e[kMaxTopk];
+    for (int j = 0; j < topk; ++j) {
+        bool found = false;
+        float v = 0.0f;
+        int b = 0x7fffffff;
+        #pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane + 32 * i;
+            if (!((used >> i) & 1u) && (!found || l[i] > v || (l[i] == v && e < b))) {
+                v = l[i]; b = e; found = true;
+            }
+        }
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+            const int ob = __shfl_xor_sync(0xffffffffu, b, off);
+            const bool of = __shfl_xor_sync(0xffffffffu, found ? 1 : 0, off) != 0;
+            if (of && (!found || ov > v || (ov == v && ob < b))) { v = ov; b = ob; found = true; }
+        }
+        if ((b & 31) == lane) used |= 1u << (b >> 5);
+        sel_v[j] = v;
+        sel_e[j] = b;
+    }
+    if (lane == 0) {
+        // the first selected logit is the largest
+        float sum = 0.0f;
+        for (int j = 0; j < topk; ++j) sum += expf(sel_v[j] - sel_v[0]);
+        for (int j = 0; j < topk; ++j) {
+            idx[t * topk + j] = sel_e[j];
+            wts[t * topk + j] = expf(sel_v[j] - sel_v[0]) / sum;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- permute --
+constexpr int kPermThreads = 1024;
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
+               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+               int4* __restrict__ items, int32_t* __restrict__ n_items) {
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int base[kMaxExperts];
+    __shared__ int item_base[kMaxExperts];
+    __shared__ int wcnt[kPermThreads / 32][kMaxExperts];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < n; i += kPermThreads) atomicAdd(&cnt[idx[i]], 1);
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0, items_run = 0;
+        for (int e = 0; e < E; ++e) {
+            offsets[e] = run;
+            base[e] = run;
+            item_base[e] = items_run;
+            run += cnt[e];
+            items_run += (cnt[e] + tok - 1) / tok;
+        }
+        offsets[E] = run;
+        *n_items = items_run;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kPermThreads) {
+        const int c = cnt[e];
+        for (int r = 0, k = 0; r < c; r += tok, ++k)
+            items[item_base[e] + k] = make_int4(e, base[e] + r, min(tok, c - r), 0);
+    }
+    // Stable placement, 1024 slots at a time: a slot's position is its expert's
+    // running base plus the number of earlier slots with the same expert in
+    // this chunk (earlier warps, then earlier lanes of its own warp).
+    for (int64_t c0 = 0; c0 < n; c0 += kPermThreads) {
+        const int64_t i = c0 + tid;
+        const int e = i < n ? idx[i] : -1;
+        for (int k = tid; k < (kPermThreads / 32) * E; k += kPermThreads) wcnt[k / E][k % E] = 0;
+        __syncthreads();
+        const uint32_t mask = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(mask & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wcnt[w][e] = __popc(mask);
+        __syncthreads();
+        if (e >= 0) {
+            int pos = base[e] + rank;
+            for (int w2 = 0; w2 < w; ++w2) pos += wcnt[w2][e];
+            perm[pos] = (int32_t)i;
+            inv[i] = pos;
+        }
+        __syncthreads();
+        for (int k = tid; k < E; k += kPermThreads) {
+            int s = 0;
+            for (int w2 = 0; w2 < kPermThreads / 32; ++w2) s += wcnt[w2][k];
+            base[k] += s;
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------- grouped streaming linear --
+constexpr int kWarps = 8;                      // 8 x 16 = 128 weight rows per CTA
+constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
+constexpr int kStages = 3;
+constexpr int kBlocksPerStage = 3;
+constexpr uint32_t kBlockBytes = kWarps * kAtomBytes;          // 4608 per 64-k block
+constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
+constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;
+
+__host__ __device__ constexpr size_t moe_stage_bytes(int tok) {
+    return kWeightStageBytes + (size_t)tok * kXRowElems * 2;
+}
+constexpr size_t kRingOffset = 128;
+
+struct MoeLinParams {
+    const uint8_t* w;          // E repacked weights, expert e at w + e * w_stride
+    size_t w_stride;
+    int64_t N, K, KB;          // weight rows / inner dimension / 64-k blocks
+    int kbs, splits;
+    const uint16_t* X;         // gated: token activations [T, K]; else: H rows [T*k, K]
+    const int32_t* perm;       // [T*k]
+    int topk;
+    const int4* items;         // (expert, first permuted row, rows, -)
+    const int32_t* n_items;
+    int64_t I;                 // gated: intermediate size (gate rows [0, I), up rows [I, 2I))
+    uint16_t* H;               // gated output [T*k, I]
+    float* Yp;                 // ungated output [T*k, N], scaled by the routing weight
+    const float* wts;          // [T*k] routing weights
+    int* status;
+};
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+
+template <int MT, bool GATED>
+__global__ void __launch_bounds__(kThreads)
+moe_linear_kernel(const MoeLinParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int TOK = 8 * MT;
+    constexpr size_t kStageBytes = moe_stage_bytes(TOK);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kStages;
+    uint64_t* lut_bar = empty + kStages;
+    volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + 120);
+    uint4* lut = reinterpret_cast<uint4*>(smem + kRingOffset);
+    uint8_t* ring = smem + kRingOffset + kLutBytes;
+    float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
+    const int split = blockIdx.y;
+    const int item_id = blockIdx.z;
+    if (item_id >= *p.n_items) return;         // the same for every CTA of the cluster
+    const int4 item = p.items[item_id];
+    const int e = item.x, r0 = item.y, nrows = item.z;
+    const uint8_t* wexp = p.w + (size_t)e * p.w_stride;
+
+    const int kb0 = split * p.kbs;
+    const int kb1 = min(kb0 + p.kbs, (int)p.KB);
+    const int nkb = kb1 - kb0;
+    const int nst = (nkb + kBlocksPerStage - 1) / kBlocksPerStage;
+    // weight rows of this CTA: gated -> 64 gate rows + the 64 matching up rows
+    // (two runs of four atoms); ungated -> 128 consecutive rows (one run of eight)
+    const int64_t row_a = GATED ? (int64_t)cgi * 64 : (int64_t)cgi * 128;
+    const int64_t row_b = GATED ? p.I + (int64_t)cgi * 64 : 0;
+    auto atom_src = [&](int64_t row0, int kb) {
+        const int64_t rbg = row0 / kAtomRows;
+        return wexp + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, kb, rbg % kAtomsPerTileK, p.KB);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        mbar_init(lut_bar, 1);
+        fence_mbar_init();
+    }
+    for (int s = 0; s < kStages; ++s) {
+        uint4* xsb = reinterpret_cast<uint4*>(ring + s * kStageBytes + kWeightStageBytes);
+        for (int i = tid; i < TOK * kXRowElems / 8; i += kThreads) xsb[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();
+    __syncthreads();
+
+    float acc[MT][4];
+    #pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+        #pragma unroll
+        for (int v = 0; v < 4; ++v) acc[mt][v] = 0.0f;
+
+    if (warp == kWarps) {
+        if (lane == 0) {
+            const Header* hdr = reinterpret_cast<const Header*>(wexp);
+            const bool hdr_ok = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            *hdr_flag = hdr_ok ? 1 : 0;
+            if (!hdr_ok) {
+                record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
+                mbar_arrive(lut_bar);
+            } else {
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                bulk_g2s(lut, wexp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                // activation row of each of this item's routed rows
+                const uint16_t* xrow[TOK];
+                for (int t = 0; t < nrows; ++t) {
+                    const int64_t r = r0 + t;
+                    const int64_t src_row = GATED ? (int64_t)(p.perm[r] / p.topk) : r;
+                    xrow[t] = p.X + src_row * p.K;
+                }
+                int issued = 0;
+                bool ok = true;
+                for (int i = 0; i < nst && ok; ++i) {
+                    const int s = i % kStages;
+                    if (i >= kStages) ok = mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.status);
+                    if (!ok) break;
+                    const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
+                    const int64_t kx = (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
+                    const int64_t kx_left = p.K - kx;
+                    const int xk = (int)(kx_left < nb * kBlockK ? kx_left : nb * kBlockK);
+                    uint8_t* st = ring + s * kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * kBlockBytes + (size_t)nrows * xk * 2));
+                    for (int b = 0; b < nb; ++b) {
+                        const int kb = kb0 + i * kBlocksPerStage + b;
+                        if (GATED) {
+                            bulk_g2s(st + b * kBlockBytes, atom_src(row_a, kb), kBlockBytes / 2, &full[s]);
+                            bulk_g2s(st + b * kBlockBytes + kBlockBytes / 2, atom_src(row_b, kb), kBlockBytes / 2, &full[s]);
+                        } else {
+                            bulk_g2s(st + b * kBlockBytes, atom_src(row_a, kb), kBlockBytes, &full[s]);
+                        }
+                    }
+                    uint16_t* xsb = reinterpret_cast<uint16_t*>(st + kWeightStageBytes);
+                    for (int t = 0; t < nrows; ++t)
+                        bulk_g2s(xsb + t * kXRowElems, xrow[t] + kx, (uint32_t)xk * 2, &full[s]);
+                    ++issued;
+                }
+                mbar_wait(lut_bar, 0, p.status);
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&full[i % kStages], (i / kStages) & 1, p.status);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int g = lane >> 2, q = lane & 3;
+        bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        const bool rows_valid = GATED || row_a + warp * kAtomRows < p.N;
+        for (int i = 0; i < nst && ok; ++i) {
+            const int s = i % kStages;
+            if (!mbar_wait(&full[s], (i / kStages) & 1, p.status)) break;
+            const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
+            const uint8_t* st = ring + s * kStageBytes;
+            uint4 codes[kBlocksPerStage];
+            uint32_t sc[kBlocksPerStage];
+            #pragma unroll
+            for (int b = 0; b < kBlocksPerStage; ++b) {
+                const uint8_t* a = st + b * kBlockBytes + warp * kAtomBytes;
+                codes[b] = *reinterpret_cast<const uint4*>(a + 16 * lane);
+                sc[b] = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
+            }
+            if (rows_valid) {
+                const uint16_t* xr = reinterpret_cast<const uint16_t*>(st + kWeightStageBytes) + g * kXRowElems + q * 16;
+                #pragma unroll
+                for (int b = 0; b < kBlocksPerStage; ++b)
+                    if (b < nb) atom_mma<MT, kXRowElems>(codes[b], sc[b], lut, xr + b * kBlockK, acc);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // push partials to the reducing CTA
+        const int c = lane & 3;
+        if (GATED) {
+            // pair (token t, column jj): gate partial from warps 0-3, up from warps 4-7
+            const int total = TOK * 64;
+            const int share = (total + p.splits - 1) / p.splits;
+            #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                #pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int row = warp * 16 + g + (v >= 2 ? 8 : 0);
+                    const int t = mt * 8 + 2 * c + (v & 1);
+                    const int jj = row & 63, half = row >> 6;
+                    const int ei = t * 64 + jj;
+                    float* dst = cluster.map_shared_rank(part, ei / share);
+                    dst[(split * share + ei % share) * 2 + half] = acc[mt][v];
+                }
+        } else {
+            const int total = TOK * 128;
+            const int share = (total + p.splits - 1) / p.splits;
+            #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                #pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int row = warp * 16 + g + (v >= 2 ? 8 : 0);
+                    const int t = mt * 8 + 2 * c + (v & 1);
+                    const int ei = t * 128 + row;
+                    float* dst = cluster.map_shared_rank(part, ei / share);
+                    dst[split * share + ei % share] = acc[mt][v];
+                }
+        }
+    }
+    cluster.sync();
+
+    if (*hdr_flag != 0) {
+        if (GATED) {
+            const int total = TOK * 64;
+            const int share = (total + p.splits - 1) / p.splits;
+            const int e0 = split * share, e1 = min(total, e0 + share);
+            for (int ei = e0 + tid; ei < e1; ei += kThreads) {
+                float gsum = 0.0f, usum = 0.0f;
+                for (int r = 0; r < p.splits; ++r) {
+                    gsum += part[(r * share + (ei - e0)) * 2 + 0];
+                    usum += part[(r * share + (ei - e0)) * 2 + 1];
+                }
+                const int t = ei / 64, jj = ei % 64;
+                if (t < nrows)
+                    p.H[(int64_t)(r0 + t) * p.I + (int64_t)cgi * 64 + jj] = f32_to_bf16_bits(silu_f(gsum) * usum);
+            }
+        } else {
+            const int total = TOK * 128;
+            const int share = (total + p.splits - 1) / p.splits;
+            const int e0 = split * share, e1 = min(total, e0 + share);
+            for (int ei = e0 + tid; ei < e1; ei += kThreads) {
+                float sum = 0.0f;
+                for (int r = 0; r < p.splits; ++r) sum += part[r * share + (ei - e0)];
+                const int t = ei / 128, row = ei % 128;
+                const int64_t n = row_a + row;
+                if (t < nrows && n < p.N) {
+                    const int32_t slot = p.perm[r0 + t];
+                    p.Yp[(int64_t)slot * p.N + n] = p.wts[slot] * sum;
+                }
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- combine --
+__global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk, int64_t H,
+                               uint16_t* __restrict__ out) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= T * H) return;
+    const int64_t t = i / H, n = i % H;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < topk; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(Yp + (t * topk + j) * H + n);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    const uint32_t lo = (uint32_t)f32_to_bf16_bits(s.x) | ((uint32_t)f32_to_bf16_bits(s.y) << 16);
+    const uint32_t hi = (uint32_t)f32_to_bf16_bits(s.z) | ((uint32_t)f32_to_bf16_bits(s.w) << 16);
+    *reinterpret_cast<uint2*>(out + i) = make_uint2(lo, hi);
+}
+
+size_t moe_lin_smem(int MT, bool gated) {
+    const int tok = 8 * MT;
+    const size_t part = gated ? ((size_t)tok * 64 + 8) * 2 : (size_t)tok * 128 + 8;
+    return kRingOffset + kLutBytes + kStages * moe_stage_bytes(tok) + part * 4;
+}
+
+template <int MT, bool GATED>
+nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_items, cudaStream_t s) {
+    const size_t smem = moe_lin_smem(MT, GATED);
+    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return check_cuda(e, "MoE linear: shared memory attribute");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, (unsigned)p.splits, max_items);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)p.splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED>, p);
+    return check_cuda(e, GATED ? "MoE FC1: launch" : "MoE FC2: launch");
+}
+
+struct MoeLayout {
+    size_t idx, wts, offsets, perm, inv, items, n_items, xs, h, yp, total;
+    int tok, mt;
+    int64_t max_items;
+};
+
+MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq) {
+    MoeLayout L{};
+    const int64_t n = T * topk;
+    L.mt = (n / std::max(E, 1)) > 8 ? 2 : 1;        // rows per expert on average
+    L.tok = 8 * L.mt;
+    L.max_items = ceil_div(n, L.tok) + std::min<int64_t>(E, n);
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)round_up((int64_t)bytes, 256); return o; };
+    L.idx = take(n * 4);
+    L.wts = take(n * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm = take(n * 4);
+    L.inv = take(n * 4);
+    L.items = take(L.max_items * 16);
+    L.n_items = take(4);
+    L.xs = awq ? take(T * H * 2) : 0;
+    L.h = take(n * I * 2);
+    L.yp = take(n * H * 4);
+    L.total = off;
+    return L;
+}
+
+int moe_splits(int64_t base_ctas, int64_t KB, int kbs_min) {
+    int64_t splits = std::max<int64_t>(1, ceil_div(2LL * sm_count(), std::max<int64_t>(base_ctas, 1)));
+    splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / kbs_min)));
+    return (int)splits;
+}
+
+}  // namespace
+}  // namespace nvfp4
 
 using namespace nvfp4;
 
-extern "C" size_t nvfp4_w4a16_moe_workspace(int64_t, int, int, int64_t, int64_t) { return 0; }
+extern "C" size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t I) {
+    if (T <= 0 || E <= 0 || topk <= 0 || H <= 0 || I <= 0) return 0;
+    // the AWQ activation copy is always budgeted so one size fits both calls
+    return moe_layout(T, E, topk, H, I, true).total;
+}
 
-extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void*, const float*, const void*, const void*,
-                                                const void*, int64_t, int, int, int64_t, int64_t,
-                                                void*, int32_t*, float*, int32_t*, int32_t*,
-                                                void*, size_t, void*) {
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_moe_grouped: not available");
+extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
+                                                const void* fc1, const void* fc2,
+                                                const void* fc1_pre_quant_scale,
+                                                int64_t T, int E, int topk, int64_t H, int64_t I,
+                                                void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                                int32_t* perm_out, int32_t* offsets_out,
+                                                void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "nvfp4_w4a16_moe_grouped";
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
+    if (E < 1 || E > kMaxExperts) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: E=%d outside [1, %d]", fn, E, kMaxExperts);
+    if (topk < 1 || topk > kMaxTopk || topk > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: topk=%d outside [1, min(E, %d)]", fn, topk, kMaxTopk);
+    if (H <= 0 || I <= 0 || H % 64 != 0 || I % 64 != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: H=%lld and I=%lld must be positive multiples of 64", fn, (long long)H, (long long)I);
+    if (T == 0) return NVFP4_OK;                  // a zero-token chunk launches no kernel
+    if (!X || !router_logits || !fc1 || !fc2 || !out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(X, 16) || !aligned(out, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: X and out must be 16-byte aligned", fn);
+    if (!aligned(router_logits, 4)) return fail(NVFP4_ERR_ALIGNMENT, "%s: router_logits must be 4-byte aligned", fn);
+    if (!aligned(fc1, 256) || !aligned(fc2, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: expert weights must be 256-byte aligned", fn);
+    if (fc1_pre_quant_scale && !aligned(fc1_pre_quant_scale, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: fc1_pre_quant_scale must be 16-byte aligned", fn);
+    if (moe_layout(T, E, topk, H, I, false).max_items > 65535)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: T=%lld routes too many rows for one call", fn, (long long)T);
+    const size_t need = nvfp4_w4a16_moe_workspace(T, E, topk, H, I);
+    if (!workspace || workspace_bytes < need) return fail(NVFP4_ERR_WORKSPACE, "%s: workspace %zu bytes, needs %zu", fn, workspace_bytes, need);
+    if (!aligned(workspace, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: workspace must be 256-byte aligned", fn);
+    int* status = device_status_ptr();
+    if (!status) return fail(NVFP4_ERR_CUDA, "%s: no CUDA device", fn);
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    const MoeLayout L = moe_layout(T, E, topk, H, I, fc1_pre_quant_scale != nullptr);
+    const int64_t n = T * topk;
+    int32_t* idx = topk_idx_out ? topk_idx_out : (int32_t*)(ws + L.idx);
+    float* wts = topk_weight_out ? topk_weight_out : (float*)(ws + L.wts);
+    int32_t* offsets = offsets_out ? offsets_out : (int32_t*)(ws + L.offsets);
+    int32_t* perm = perm_out ? perm_out : (int32_t*)(ws + L.perm);
+    int32_t* inv = (int32_t*)(ws + L.inv);
+    int4* items = (int4*)(ws + L.items);
+    int32_t* n_items = (int32_t*)(ws + L.n_items);
+    uint16_t* hbuf = (uint16_t*)(ws + L.h);
+    float* yp = (float*)(ws + L.yp);
+    nvfp4_status st;
+
+    const uint16_t* xin = (const uint16_t*)X;
+    if (fc1_pre_quant_scale) {
+        st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H, s);
+        if (st != NVFP4_OK) return st;
+        xin = (const uint16_t*)(ws + L.xs);
+    }
+    route_kernel<<<(unsigned)ceil_div(T, 8), 256, 0, s>>>(router_logits, T, E, topk, idx, wts);
+    if ((st = check_cuda(cudaGetLastError(), "MoE route: launch")) != NVFP4_OK) return st;
+    permute_kernel<<<1, kPermThreads, 0, s>>>(idx, n, E, L.tok, offsets, perm, inv, items, n_items);
+    if ((st = check_cuda(cudaGetLastError(), "MoE permute: launch")) != NVFP4_OK) return st;
+
+    // expected work items in flight, for the split-K choice
+    const int64_t est_items = std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
+    MoeLinParams p1{};
+    p1.w = (const uint8_t*)fc1; p1.w_stride = nvfp4_repack_size(2 * I, H);
+    p1.N = 2 * I; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
+    p1.splits = moe_splits((I / 64) * est_items, p1.KB, 4);
+    p1.kbs = (int)ceil_div(p1.KB, p1.splits);
+    p1.splits = (int)ceil_div(p1.KB, p1.kbs);
+    p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
+    p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
+    st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s)
+                   : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s);
+    if (st != NVFP4_OK) return st;
+
+    MoeLinParams p2{};
+    p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
+    p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
+    p2.splits = moe_splits(ceil_div(H, 128) * est_items, p2.KB, 4);
+    p2.kbs = (int)ceil_div(p2.KB, p2.splits);
+    p2.splits = (int)ceil_div(p2.KB, p2.kbs);
+    p2.X = hbuf; p2.perm = perm; p2.topk = topk; p2.items = items; p2.n_items = n_items;
+    p2.I = I; p2.Yp = yp; p2.wts = wts; p2.status = status;
+    st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s)
+                   : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s);
+    if (st != NVFP4_OK) return st;
+
+    combine_kernel<<<(unsigned)ceil_div(T * H / 4, 256), 256, 0, s>>>(yp, T, topk, H, (uint16_t*)out);
+    return check_cuda(cudaGetLastError(), "MoE combine: launch");
 }
