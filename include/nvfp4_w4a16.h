@@ -197,6 +197,31 @@ nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
                                      int32_t* perm_out, int32_t* offsets_out,
                                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Allocation-free variant of nvfp4_w4a16_moe_grouped (no counterpart in the
+ * source pages: it exists for callers that cannot allocate device memory, such
+ * as a plugin whose host framework gives it no workspace, or code running
+ * while allocation is not allowed).  Same arguments and results, minus the
+ * workspace: the layer runs on a scratch array of
+ * nvfp4_w4a16_moe_noalloc_scratch_bytes() bytes (16 MiB) that is a static
+ * device variable of this library, so every GPU that loads the library holds
+ * it until the process exits.  Problems whose nvfp4_w4a16_moe_workspace()
+ * exceeds that size are rejected with NVFP4_ERR_UNSUPPORTED_SHAPE (with
+ * E=128, topk=8, H=2048, I=768 that allows up to T=204 tokens per call).  The entry point itself calls
+ * no allocating routine.  The first call on a device looks the scratch address
+ * up (cudaGetSymbolAddress, which may load the library's device code), so make
+ * that first call before any stream capture.  Every call shares the one array;
+ * nothing in it has to start at zero, but calls that overlap on the GPU (on
+ * different streams) race on it and give wrong results.
+ */
+size_t nvfp4_w4a16_moe_noalloc_scratch_bytes(void);
+nvfp4_status nvfp4_w4a16_moe_grouped_noalloc(const void* X, const float* router_logits,
+                                             const void* fc1, const void* fc2,
+                                             const void* fc1_pre_quant_scale,
+                                             int64_t T, int E, int topk, int64_t H, int64_t I,
+                                             void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                             int32_t* perm_out, int32_t* offsets_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

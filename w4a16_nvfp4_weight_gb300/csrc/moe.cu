@@ -28,6 +28,7 @@
 // (Description: FC1's activation is multiplied by the pre-quant scale before
 // the GEMM; a zero-token chunk launches no kernel).
 #include <algorithm>
+#include <mutex>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -559,4 +560,67 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
 
     combine_kernel<<<(unsigned)ceil_div(T * H / 4, 256), 256, 0, s>>>(yp, T, topk, H, (uint16_t*)out);
     return check_cuda(cudaGetLastError(), "MoE combine: launch");
+}
+
+// ------------------------------------------------- allocation-free variant --
+// For callers that cannot allocate device memory themselves -- for example a
+// plugin whose host framework hands it no workspace, or code that runs while
+// an allocator is locked during graph construction -- this entry point runs
+// the same layer on a fixed scratch area that lives in the library's own
+// device memory.
+namespace nvfp4 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;     // 16 MiB
+__device__ __align__(256) uint8_t g_moe_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+uint8_t* g_noalloc_ptr[kMaxScratchDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).
+nvfp4_status noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return check_cuda(e, "nvfp4_w4a16_moe_grouped_noalloc: current device");
+    if (dev < 0 || dev >= kMaxScratchDevices)
+        return fail(NVFP4_ERR_CUDA, "nvfp4_w4a16_moe_grouped_noalloc: device %d not supported", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_moe_noalloc_scratch);
+        if (e != cudaSuccess) return check_cuda(e, "nvfp4_w4a16_moe_grouped_noalloc: scratch address");
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" size_t nvfp4_w4a16_moe_noalloc_scratch_bytes(void) { return nvfp4::kNoAllocScratchBytes; }
+
+extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_noalloc(const void* X, const float* router_logits,
+                                                        const void* fc1, const void* fc2,
+                                                        const void* fc1_pre_quant_scale,
+                                                        int64_t T, int E, int topk, int64_t H, int64_t I,
+                                                        void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                                        int32_t* perm_out, int32_t* offsets_out, void* stream) {
+    const size_t need = nvfp4_w4a16_moe_workspace(T, E, topk, H, I);
+    if (need > nvfp4::kNoAllocScratchBytes)
+        return nvfp4::fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                           "nvfp4_w4a16_moe_grouped_noalloc: T=%lld E=%d topk=%d H=%lld I=%lld needs %zu bytes "
+                           "of scratch, more than the built-in %zu; use nvfp4_w4a16_moe_grouped with a workspace",
+                           (long long)T, E, topk, (long long)H, (long long)I, need, nvfp4::kNoAllocScratchBytes);
+    if (T <= 0 || need == 0)    // nothing to run, or arguments the regular entry point rejects
+        return nvfp4_w4a16_moe_grouped(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out,
+                                       topk_idx_out, topk_weight_out, perm_out, offsets_out, nullptr, 0, stream);
+    uint8_t* scratch = nullptr;
+    const nvfp4_status st = nvfp4::noalloc_scratch(&scratch);
+    if (st != NVFP4_OK) return st;
+    return nvfp4_w4a16_moe_grouped(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out,
+                                   topk_idx_out, topk_weight_out, perm_out, offsets_out, scratch,
+                                   nvfp4::kNoAllocScratchBytes, stream);
 }
