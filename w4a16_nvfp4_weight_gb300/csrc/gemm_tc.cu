@@ -1,13 +1,314 @@
-// Tensor-core tile GEMM (placeholder until the tcgen05 kernel lands).
+// Tensor-core tile GEMM for the W4A16 NVFP4 linear at larger M (prefill, LM
+// head): dequant-fused, TMA-fed, tcgen05 MMAs accumulating in tensor memory.
+//
+// One CTA computes a (128*SUBM) x 256 output tile over the whole K:
+//   warp 0      producer: per 64-k block, TMA tile loads of the activation
+//               (128 rows x 64 k, 128-byte swizzle, zero fill past M and K)
+//               and one bulk copy of the weight block (256 rows x 64 k of codes
+//               and scales, 9216 contiguous bytes) into a 3-stage ring;
+//   warp 1      allocates 256*SUBM tensor-memory columns and issues, per block,
+//               SUBM x 4 tcgen05 BF16 MMAs (M=128, N=256, K=16) from shared
+//               memory into the FP32 accumulators; commits release the stages;
+//   warps 2..9  expand the weight codes through the magnitude table into the
+//               BF16 B operand (256 x 64, 128-byte swizzled K-major layout) of a
+//               2-stage ring, then run the epilogue: tensor memory -> registers
+//               -> BF16 -> global, rows/columns past M/N clipped.
+// The weight tile is dequantized once per CTA and shared by the SUBM M
+// sub-tiles, so the dequant (integer pipe) work per FLOP halves at SUBM = 2.
+//
+// Method: "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper"
+// (Description / Changes table: NVFP4 weights dequantized per step, BF16 GEMM);
+// AWQ: "[None][fix] Apply the NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL"
+// (the activation is scaled in BF16 before the GEMM; done by a pre-pass here).
+#include <cuda.h>
+
+#include <mutex>
+
 #include "common.cuh"
+#include "gemm_decode.cuh"
 #include "gemm_tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace nvfp4 {
+namespace {
 
-bool use_tc_path(int64_t) { return false; }
-size_t tc_workspace_bytes(int64_t, int64_t, int64_t, bool) { return 0; }
-nvfp4_status launch_tc(const TcParams&, cudaStream_t) {
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tile GEMM not available");
+constexpr int kTcThreads = 320;                  // 10 warps
+constexpr int kDeqWarps = 8;
+constexpr int kS1 = 3;                           // activation + raw-weight ring
+constexpr int kS2 = 2;                           // dequantized-weight ring
+constexpr int kBN = 256;
+constexpr uint32_t kATileBytes = 128 * 64 * 2;   // 16 KB per 128-row sub-tile
+constexpr uint32_t kBRawBytes = kAtomsPerTileK * kAtomBytes;   // 9216
+constexpr uint32_t kBDeqBytes = kBN * 64 * 2;    // 32 KB
+
+template <int SUBM>
+struct TcSmem {
+    static constexpr size_t a = 0;                                            // 1024-aligned
+    static constexpr size_t bdeq = a + (size_t)kS1 * SUBM * kATileBytes;      // 1024-aligned
+    static constexpr size_t braw = bdeq + (size_t)kS2 * kBDeqBytes;
+    static constexpr size_t lut = braw + (size_t)kS1 * kBRawBytes;
+    static constexpr size_t bars = lut + kLutBytes;
+    static constexpr size_t misc = bars + 16 * 8;
+    static constexpr size_t total = misc + 64;
+};
+
+struct TcKParams {
+    const uint8_t* rp;
+    uint16_t* Y;
+    int64_t M, N, K, KB;
+    int* status;
+};
+
+// Byte offset of the 16-byte chunk c (0..7) of row n in a 128-byte swizzled
+// K-major tile.
+__device__ __forceinline__ uint32_t sw128_offset(int n, int c) {
+    return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+}
+
+template <int SUBM>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled operand tiles
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = TcSmem<SUBM>;
+    uint8_t* a_ring = smem + L::a;
+    uint8_t* bdeq_ring = smem + L::bdeq;
+    uint8_t* braw_ring = smem + L::braw;
+    uint4* lut = reinterpret_cast<uint4*>(smem + L::lut);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+    uint64_t* tma_full = bars;                    // [kS1]
+    uint64_t* tma_empty = bars + kS1;             // [kS1]
+    uint64_t* deq_full = bars + 2 * kS1;          // [kS2]
+    uint64_t* deq_empty = bars + 2 * kS1 + kS2;   // [kS2]
+    uint64_t* acc_full = bars + 2 * kS1 + 2 * kS2;
+    uint64_t* lut_bar = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
+    volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t n0 = (int64_t)blockIdx.x * kBN;
+    const int64_t m0 = (int64_t)blockIdx.y * 128 * SUBM;
+    const int nkb = (int)p.KB;
+
+    if (tid == 0) {
+        for (int s = 0; s < kS1; ++s) {
+            mbar_init(&tma_full[s], 1);
+            mbar_init(&tma_empty[s], 1 + kDeqWarps);   // MMA commit + every dequant warp
+        }
+        for (int s = 0; s < kS2; ++s) {
+            mbar_init(&deq_full[s], kDeqWarps);
+            mbar_init(&deq_empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(lut_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 256 * SUBM);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t idesc = umma_idesc_bf16(128, kBN);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const Header* hdr = reinterpret_cast<const Header*>(p.rp);
+            const bool ok_hdr = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            *hdr_flag = ok_hdr ? 1 : 0;
+            if (!ok_hdr) {
+                record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
+                mbar_arrive(lut_bar);
+            } else {
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                bulk_g2s(lut, p.rp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                const uint8_t* wtile = p.rp + kTilesOffset + atom_offset(blockIdx.x, 0, 0, p.KB);
+                int issued = 0;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int s = kb % kS1;
+                    if (kb >= kS1 && !mbar_wait(&tma_empty[s], ((kb / kS1) - 1) & 1, p.status)) break;
+                    mbar_arrive_expect_tx(&tma_full[s], SUBM * kATileBytes + kBRawBytes);
+                    for (int mi = 0; mi < SUBM; ++mi)
+                        tma_load_2d(a_ring + ((size_t)s * SUBM + mi) * kATileBytes, &tmap_x, kb * 64,
+                                    (int)(m0 + mi * 128), &tma_full[s]);
+                    bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes, kBRawBytes,
+                             &tma_full[s]);
+                    ++issued;
+                }
+                // no copy may still target this CTA when it exits
+                mbar_wait(lut_bar, 0, p.status);
+                for (int kb = issued > kS1 ? issued - kS1 : 0; kb < issued; ++kb)
+                    mbar_wait(&tma_full[kb % kS1], (kb / kS1) & 1, p.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s1 = kb % kS1, s2 = kb % kS2;
+                ok = mbar_wait(&tma_full[s1], (kb / kS1) & 1, p.status) &&
+                     mbar_wait(&deq_full[s2], (kb / kS2) & 1, p.status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t a_base = smem_u32(a_ring + (size_t)s1 * SUBM * kATileBytes);
+                const uint32_t b_base = smem_u32(bdeq_ring + (size_t)s2 * kBDeqBytes);
+                #pragma unroll
+                for (int mi = 0; mi < SUBM; ++mi)
+                    #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ss(tmem + mi * kBN, sw128_kmajor_desc(a_base + mi * kATileBytes + kk * 32),
+                                     sw128_kmajor_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+                umma_commit(&tma_empty[s1]);
+                umma_commit(&deq_empty[s2]);
+            }
+            umma_commit(acc_full);          // also waits out every MMA issued above
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ dequant, then epilogue
+        const int dw = warp - 2;                        // 0..7: atoms 2dw, 2dw+1 of each block
+        const int r = lane >> 2, q = lane & 3;
+        bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s1 = kb % kS1, s2 = kb % kS2;
+            ok = mbar_wait(&tma_full[s1], (kb / kS1) & 1, p.status);
+            if (ok && kb >= kS2) ok = mbar_wait(&deq_empty[s2], ((kb / kS2) - 1) & 1, p.status);
+            if (!ok) break;
+            const uint8_t* raw = braw_ring + (size_t)s1 * kBRawBytes;
+            uint8_t* dst = bdeq_ring + (size_t)s2 * kBDeqBytes;
+            #pragma unroll
+            for (int ai = 0; ai < 2; ++ai) {
+                const int atom = 2 * dw + ai;
+                const uint8_t* a = raw + atom * kAtomBytes;
+                const uint4 codes = *reinterpret_cast<const uint4*>(a + 16 * lane);
+                const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
+                const Lut t0 = lut_from_uint4(lut[sc2 & 0xFF]);
+                const Lut t1 = lut_from_uint4(lut[(sc2 >> 8) & 0xFF]);
+                uint32_t e0[8], e1[8];
+                expand8(codes.x, t0, e0);
+                expand8(codes.y, t0, e0 + 4);
+                expand8(codes.z, t1, e1);
+                expand8(codes.w, t1, e1 + 4);
+                const int row0 = atom * kAtomRows + r, row1 = row0 + 8;
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row0, 2 * q)) = make_uint4(e0[0], e0[1], e0[2], e0[3]);
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row0, 2 * q + 1)) = make_uint4(e0[4], e0[5], e0[6], e0[7]);
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row1, 2 * q)) = make_uint4(e1[0], e1[1], e1[2], e1[3]);
+                *reinterpret_cast<uint4*>(dst + sw128_offset(row1, 2 * q + 1)) = make_uint4(e1[4], e1[5], e1[6], e1[7]);
+            }
+            fence_proxy_async();       // B writes visible to the MMA; raw reads before the next copy
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&deq_full[s2]);
+                mbar_arrive(&tma_empty[s1]);
+            }
+        }
+        // epilogue: lane quarter from the hardware warp index, column half from dw
+        if (*hdr_flag != 0 && mbar_wait(acc_full, 0, p.status)) {
+            tc_fence_after_sync();
+            const int quarter = warp & 3, half = dw >> 2;
+            const int64_t mrow = m0 + quarter * 32 + lane;
+            const bool vec_ok = (p.N % 8) == 0;
+            #pragma unroll 1
+            for (int mi = 0; mi < SUBM; ++mi) {
+                const int64_t m = mrow + mi * 128;
+                #pragma unroll 1
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    const int col = half * 128 + c16 * 16;
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + mi * kBN + col, v);
+                    tmem_ld_wait();
+                    if (m >= p.M) continue;
+                    const int64_t n = n0 + col;
+                    uint32_t packed[8];
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        packed[i] = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i])) |
+                                    ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i + 1])) << 16);
+                    uint16_t* yrow = p.Y + m * p.N;
+                    if (vec_ok && n + 16 <= p.N) {
+                        *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        *reinterpret_cast<uint4*>(yrow + n + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    } else {
+                        for (int i = 0; i < 16 && n + i < p.N; ++i)
+                            yrow[n + i] = (uint16_t)(packed[i >> 1] >> ((i & 1) * 16));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 256 * SUBM);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+template <int SUBM>
+nvfp4_status launch_tc_impl(const uint16_t* X, const TcKParams& kp, cudaStream_t stream) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(NVFP4_ERR_CUDA, "tile GEMM: cuTensorMapEncodeTiled unavailable");
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)kp.K, (cuuint64_t)kp.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)kp.K * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "tile GEMM: tensor map encode failed (%d)", (int)cr);
+    const size_t smem = TcSmem<SUBM>::total + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SUBM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return check_cuda(e, "tile GEMM: shared memory attribute");
+    const dim3 grid((unsigned)ceil_div(kp.N, kBN), (unsigned)ceil_div(kp.M, 128 * SUBM), 1);
+    tc_gemm_kernel<SUBM><<<grid, kTcThreads, smem, stream>>>(tmap, kp);
+    return check_cuda(cudaGetLastError(), "tile GEMM: launch");
+}
+
+size_t awq_ws_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
+
+}  // namespace
+
+bool use_tc_path(int64_t M) { return M > 16; }
+
+size_t tc_workspace_bytes(int64_t M, int64_t, int64_t K, bool has_pqs) { return has_pqs ? awq_ws_bytes(M, K) : 0; }
+
+nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
+    const uint16_t* X = p.X;
+    if (p.pqs) {
+        nvfp4_status st = launch_awq_scale(p.X, p.pqs, (uint16_t*)p.workspace, p.M, p.K, stream);
+        if (st != NVFP4_OK) return st;
+        X = (const uint16_t*)p.workspace;
+    }
+    TcKParams kp{};
+    kp.rp = p.rp; kp.Y = p.Y; kp.M = p.M; kp.N = p.N; kp.K = p.K;
+    kp.KB = round_up(p.K, kBlockK) / kBlockK;
+    kp.status = p.status;
+    return p.M <= 128 ? launch_tc_impl<1>(X, kp, stream) : launch_tc_impl<2>(X, kp, stream);
 }
 
 }  // namespace nvfp4
