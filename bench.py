@@ -122,6 +122,34 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
+# DRAM traffic per launch of the dominant kernel, from a committed ncu summary:
+# dram bytes read + written / algorithmic bytes of the captured launch, valid
+# only while the kernel's sources are unchanged since the capture.
+PROFILE_FOR = {
+    "decode": ("profiles/decode_kernel_lmhead_m8_and_16x5120x25600.md",
+               ["gemm_decode.cu", "stream_mma.cuh", "common.cuh", "ptx.cuh"]),
+    "tensor": ("profiles/tc_gemm_kernel_prefill_2048x5120x13824.md",
+               ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "ptx.cuh"]),
+}
+
+
+def traffic_ratio(kind):
+    import hashlib
+    path, srcs = PROFILE_FOR[kind]
+    try:
+        text = open(os.path.join(ROOT, path)).read()
+        kv = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("traffic_ratio:", "kernel_sources_sha:")))
+        h = hashlib.sha256()
+        for f in srcs:
+            h.update(open(os.path.join(ROOT, "w4a16_nvfp4_weight_gb300", "csrc", f), "rb").read())
+        if h.hexdigest()[:16] != kv["kernel_sources_sha"].strip():
+            return None
+        return float(kv["traffic_ratio"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------------ inputs --
 def bits_tensor(bits, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
@@ -191,6 +219,8 @@ def run_ours(args, rank, world, device):
         shapes = [(M, K, N) for M in (1, 8, 256) for (K, N) in ((2064, 1000), (720, 3000))]
         launches, base = build_dense_workload(nv, synth, device, shapes, 4)
         config = {"workload": "odd shapes M{1,8,256} x (K,N){(2064,1000),(720,3000)}", "gemms_per_step": len(launches)}
+    elif wl == "moe":
+        return run_moe(args, rank, world, device, nv, synth)
     else:
         raise SystemExit(f"unknown workload {wl}")
 
@@ -247,6 +277,8 @@ def run_ours(args, rank, world, device):
     kern = kernel_timing(nv, launches, base, stream, device)
 
     bw_unit = wl in ("decode", "lmhead", "tails")
+    ratio = traffic_ratio("decode" if bw_unit else "tensor")
+    traffic = None if ratio is None else round(ratio * kern["bytes"] / len(launches))
     e2e = run_e2e(nv, launches, stream, args, bw_unit)
     pk = peaks()
     if bw_unit:
@@ -271,7 +303,9 @@ def run_ours(args, rank, world, device):
         "tflops": round(world * flops_step / (ms_step * 1e-3) / 1e12, 3),
         "weight_gbs": round(world * sum(weight_bytes(L["N"], L["K"]) for L in launches) / (ms_step * 1e-3) / 1e9, 2),
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": ach_unit,
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_note": "bytes per launch: DRAM/algorithmic ratio of a committed ncu capture "
+                                     "(profiles/) times this workload's mean algorithmic bytes per launch",
                      "peak_source": f"{pk['source']} ({'HBM copy' if bound == 'hbm' else 'bf16 sustained'})",
                      "kernel": "nvfp4::decode_kernel" if bound == "hbm" else "nvfp4::tc_gemm_kernel",
                      "per_shape_us": kern["per_shape_us"]},
@@ -282,6 +316,112 @@ def run_ours(args, rank, world, device):
     }
     res["_base"] = base
     return res
+
+
+MOE_E, MOE_TOPK, MOE_H, MOE_I = 128, 8, 2048, 768
+MOE_T = (1, 16, 256, 4096)
+
+
+def run_moe(args, rank, world, device, nv, synth):
+    """The MoE layer (128 experts, top-8, hidden 2048, intermediate 768) at
+    T = 1, 16, 256, 4096 tokens, one call each per step."""
+    fc1, fc2 = synth.moe_weights(MOE_E, MOE_H, MOE_I, synth.seed_for(3, 500))
+
+    def experts(ws, N, K):
+        size = nv.repack_size(N, K)
+        buf = torch.empty(len(ws) * size, dtype=torch.uint8, device=device)
+        for e, (p, sc, d) in enumerate(ws):
+            nv.repack(torch.from_numpy(p).to(device), torch.from_numpy(sc).to(device), float(d), N, K,
+                      out=buf[e * size:(e + 1) * size])
+        return buf, size
+
+    d1, sz1 = experts(fc1, 2 * MOE_I, MOE_H)
+    d2, sz2 = experts(fc2, MOE_H, MOE_I)
+    calls = []
+    for T in MOE_T:
+        c = synth.moe_case(T, synth.seed_for(3, T), E=MOE_E, topk=MOE_TOPK, H=MOE_H, I=MOE_I, weights=(fc1, fc2))
+        x = bits_tensor(c.x_bits, device)
+        lg = torch.from_numpy(np.ascontiguousarray(c.logits)).to(device)
+        ws = torch.empty(nv.moe_workspace_size(T, MOE_E, MOE_TOPK, MOE_H, MOE_I), dtype=torch.uint8, device=device)
+        out = torch.empty((T, MOE_H), dtype=torch.bfloat16, device=device)
+        offs = torch.empty(MOE_E + 1, dtype=torch.int32, device=device)
+        calls.append(dict(T=T, x=x, lg=lg, ws=ws, out=out, offs=offs))
+
+    def call(C):
+        # routing tables come back through offsets_out so the bench can count active experts
+        h = nv._lib.load()
+        nv._lib.check(h.nvfp4_w4a16_moe_grouped(
+            nv._ptr(C["x"]), nv._ptr(C["lg"]), nv._ptr(d1), nv._ptr(d2), None, C["T"], MOE_E, MOE_TOPK,
+            MOE_H, MOE_I, nv._ptr(C["out"]), None, None, None, nv._ptr(C["offs"]), nv._ptr(C["ws"]),
+            C["ws"].numel(), nv._stream()))
+
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for C in calls:
+            call(C)
+        torch.cuda.synchronize()
+        assert nv.device_status() == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for C in calls:
+                call(C)
+    torch.cuda.synchronize()
+    for C in calls:
+        # algorithmic bytes: the routed experts' FC1 + FC2 weights (0.5625 B per weight)
+        # plus the BF16 input and output rows
+        counts = np.diff(C["offs"].cpu().numpy())
+        C["experts"] = int((counts > 0).sum())
+        C["bytes"] = C["experts"] * (3 * MOE_I * MOE_H) * 9 // 16 + 2 * 2 * C["T"] * MOE_H
+        C["flops"] = C["T"] * MOE_TOPK * (2 * 2 * MOE_I * MOE_H + 2 * MOE_H * MOE_I)
+    bytes_step = sum(C["bytes"] for C in calls)
+    flops_step = sum(C["flops"] for C in calls)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+    per = {}
+    for C in calls:
+        with torch.cuda.stream(stream):
+            gg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gg, stream=stream):
+                for _ in range(10):
+                    call(C)
+            gg.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gg.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 10
+        per[f"T={C['T']}"] = {"us": round(us, 2), "experts": C["experts"],
+                              "GB/s": round(C["bytes"] / us / 1e3, 1), "TFLOP/s": round(C["flops"] / us / 1e6, 2)}
+    pk = peaks()
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    return {
+        "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": "MoE layer E=128 top-8 H=2048 I=768 at T{1,16,256,4096}",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": "the 4 calls of a step read 128 experts (604 MB) of distinct weights, larger than L2"},
+        "tflops": round(world * flops_step / (ms_step * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(value / pk["hbm"], 4), "traffic": None, "peak_source": pk["source"],
+                     "per_call": per},
+        "gpu_launches": 5 * len(calls) * args.steps,
+        "_base": None,
+    }
 
 
 def launch_count(nv, L):
@@ -462,7 +602,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails", "moe"])
     ap.add_argument("--awq", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, metavar="M,K,N",
