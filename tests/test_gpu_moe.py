@@ -58,8 +58,12 @@ def _small_case(T, E, topk, H, I, seed, awq=False):
     return synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=awq)
 
 
+# (64,16,4,256,128), (300,8,2,256,256), (100,4,3,384,128) and (1024,4,2,128,128) route
+# >= 16 rows per expert and take the tensor-core tile path (128- and 256-row items);
+# the others take the streaming path.
 @pytest.mark.parametrize("T,E,topk,H,I", [(3, 4, 2, 64, 64), (64, 16, 4, 256, 128), (37, 8, 3, 192, 320),
-                                          (5, 1, 1, 128, 64), (200, 32, 8, 128, 64)])
+                                          (5, 1, 1, 128, 64), (200, 32, 8, 128, 64), (300, 8, 2, 256, 256),
+                                          (100, 4, 3, 384, 128), (1024, 4, 2, 128, 128)])
 def test_moe_small_full_compare(T, E, topk, H, I):
     c = _small_case(T, E, topk, H, I, seed=T * 31 + E)
     out, routing = _run(c)
@@ -77,6 +81,17 @@ def test_moe_awq_and_dropped_scale_control():
     out_plain, _ = _run(c, awq=False)
     with pytest.raises(AssertionError):
         gu.compare(out_plain, ref["out_bits"], "MoE dropped AWQ")
+
+
+def test_moe_tile_path_awq_and_dropped_scale_control():
+    c = _small_case(300, 8, 2, 256, 256, seed=15, awq=True)
+    out, routing = _run(c, awq=True)
+    ref = _oracle(c, awq=True)
+    _check_routing(routing, ref, 300, 2, 8)
+    gu.compare(out, ref["out_bits"], "MoE tile path AWQ")
+    out_plain, _ = _run(c, awq=False)
+    with pytest.raises(AssertionError):
+        gu.compare(out_plain, ref["out_bits"], "MoE tile path dropped AWQ")
 
 
 def test_moe_ties_pick_lower_expert():

@@ -52,10 +52,19 @@ struct TcSmem {
     static constexpr size_t total = misc + 64;
 };
 
+enum class TcMode { kDense, kMoeFc1, kMoeFc2 };
+
 struct TcKParams {
-    const uint8_t* rp;
-    uint16_t* Y;
-    int64_t M, N, K, KB;
+    const uint8_t* rp;        // dense: the repacked weight; MoE: expert 0 of the stacked weights
+    size_t w_stride;          // MoE: bytes between experts
+    uint16_t* Y;              // dense: [M, N] BF16; MoE FC1: H [rows, I] BF16
+    float* Yp;                // MoE FC2: [slots, N] FP32, scaled by the routing weight
+    const int4* items;        // MoE: (expert, first row, rows, -) work list
+    const int32_t* n_items;
+    const int32_t* perm;      // MoE FC2: permuted row -> routing slot
+    const float* wts;         // MoE FC2: routing weights per slot
+    int64_t M, N, K, KB;      // dense M; weight rows N (FC1: 2I) and inner K
+    int64_t I;                // MoE FC1: intermediate size
     int* status;
 };
 
@@ -65,7 +74,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int c) {
     return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
 }
 
-template <int SUBM>
+__device__ __forceinline__ float silu_tc(float v) { return v / (1.0f + expf(-v)); }
+
+template <int SUBM, TcMode MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -87,8 +98,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t n0 = (int64_t)blockIdx.x * kBN;
-    const int64_t m0 = (int64_t)blockIdx.y * 128 * SUBM;
+    constexpr bool kMoe = MODE != TcMode::kDense;
+    // dense: output tile (m0, n0); MoE: work item (expert, first permuted row,
+    // rows) and output columns n0 (FC1: intermediate columns j0 = 128 * bx)
+    int64_t m0, m_end;
+    const uint8_t* wbase = p.rp;
+    if constexpr (kMoe) {
+        if ((int)blockIdx.y >= *p.n_items) return;      // uniform across the CTA
+        const int4 item = p.items[blockIdx.y];
+        wbase = p.rp + (size_t)item.x * p.w_stride;
+        m0 = item.y;
+        m_end = (int64_t)item.y + item.z;
+    } else {
+        m0 = (int64_t)blockIdx.y * 128 * SUBM;
+        m_end = p.M;
+    }
+    const int64_t n0 = (int64_t)blockIdx.x * (MODE == TcMode::kMoeFc1 ? kBN / 2 : kBN);
     const int nkb = (int)p.KB;
 
     if (tid == 0) {
@@ -117,7 +142,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const Header* hdr = reinterpret_cast<const Header*>(p.rp);
+            const Header* hdr = reinterpret_cast<const Header*>(wbase);
             const bool ok_hdr = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
             *hdr_flag = ok_hdr ? 1 : 0;
             if (!ok_hdr) {
@@ -125,8 +150,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 mbar_arrive(lut_bar);
             } else {
                 mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
-                bulk_g2s(lut, p.rp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
-                const uint8_t* wtile = p.rp + kTilesOffset + atom_offset(blockIdx.x, 0, 0, p.KB);
+                bulk_g2s(lut, wbase + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                // FC1: 128 gate rows j0.. and the 128 matching up rows I + j0.. (two
+                // half tiles); otherwise one 256-row tile
+                auto half_tile = [&](int64_t row0) {
+                    const int64_t rbg = row0 / kAtomRows;
+                    return wbase + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, 0, rbg % kAtomsPerTileK, p.KB);
+                };
+                const uint8_t* wtile = half_tile(n0);
+                const uint8_t* wtile_up = MODE == TcMode::kMoeFc1 ? half_tile(p.I + n0) : nullptr;
                 int issued = 0;
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int s = kb % kS1;
@@ -135,8 +167,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                     for (int mi = 0; mi < SUBM; ++mi)
                         tma_load_2d(a_ring + ((size_t)s * SUBM + mi) * kATileBytes, &tmap_x, kb * 64,
                                     (int)(m0 + mi * 128), &tma_full[s]);
-                    bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes, kBRawBytes,
-                             &tma_full[s]);
+                    if constexpr (MODE == TcMode::kMoeFc1) {
+                        bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes,
+                                 kBRawBytes / 2, &tma_full[s]);
+                        bulk_g2s(braw_ring + (size_t)s * kBRawBytes + kBRawBytes / 2,
+                                 wtile_up + (size_t)kb * kBRawBytes, kBRawBytes / 2, &tma_full[s]);
+                    } else {
+                        bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes, kBRawBytes,
+                                 &tma_full[s]);
+                    }
                     ++issued;
                 }
                 // no copy may still target this CTA when it exits
@@ -213,30 +252,72 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
             tc_fence_after_sync();
             const int quarter = warp & 3, half = dw >> 2;
             const int64_t mrow = m0 + quarter * 32 + lane;
-            const bool vec_ok = (p.N % 8) == 0;
             #pragma unroll 1
             for (int mi = 0; mi < SUBM; ++mi) {
                 const int64_t m = mrow + mi * 128;
-                #pragma unroll 1
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    const int col = half * 128 + c16 * 16;
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem + ((uint32_t)(quarter * 32) << 16) + mi * kBN + col, v);
-                    tmem_ld_wait();
-                    if (m >= p.M) continue;
-                    const int64_t n = n0 + col;
-                    uint32_t packed[8];
-                    #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        packed[i] = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i])) |
-                                    ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i + 1])) << 16);
-                    uint16_t* yrow = p.Y + m * p.N;
-                    if (vec_ok && n + 16 <= p.N) {
-                        *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        *reinterpret_cast<uint4*>(yrow + n + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    } else {
-                        for (int i = 0; i < 16 && n + i < p.N; ++i)
-                            yrow[n + i] = (uint16_t)(packed[i >> 1] >> ((i & 1) * 16));
+                const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + mi * kBN;
+                if constexpr (MODE == TcMode::kDense) {
+                    const bool vec_ok = (p.N % 8) == 0;
+                    #pragma unroll 1
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const int col = half * 128 + c16 * 16;
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(trow + col, v);
+                        tmem_ld_wait();
+                        if (m >= m_end) continue;
+                        const int64_t n = n0 + col;
+                        uint32_t packed[8];
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            packed[i] = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i])) |
+                                        ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i + 1])) << 16);
+                        uint16_t* yrow = p.Y + m * p.N;
+                        if (vec_ok && n + 16 <= p.N) {
+                            *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            *reinterpret_cast<uint4*>(yrow + n + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        } else {
+                            for (int i = 0; i < 16 && n + i < p.N; ++i)
+                                yrow[n + i] = (uint16_t)(packed[i >> 1] >> ((i & 1) * 16));
+                        }
+                    }
+                } else if constexpr (MODE == TcMode::kMoeFc1) {
+                    // columns [0,128) are gate, [128,256) up; this warp does 64 of the 128
+                    #pragma unroll 1
+                    for (int c16 = 0; c16 < 4; ++c16) {
+                        const int col = half * 64 + c16 * 16;
+                        uint32_t g[16], u[16];
+                        tmem_ld_32x32b_x16(trow + col, g);
+                        tmem_ld_32x32b_x16(trow + 128 + col, u);
+                        tmem_ld_wait();
+                        if (m >= m_end) continue;
+                        uint32_t packed[8];
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float h0 = silu_tc(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                            const float h1 = silu_tc(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                            packed[i] = (uint32_t)f32_to_bf16_bits(h0) | ((uint32_t)f32_to_bf16_bits(h1) << 16);
+                        }
+                        uint16_t* hrow = p.Y + m * p.I + n0 + col;      // I and n0 are multiples of 64
+                        *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        *reinterpret_cast<uint4*>(hrow + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                } else {
+                    const int32_t slot = m < m_end ? p.perm[m] : 0;
+                    const float w = m < m_end ? p.wts[slot] : 0.0f;
+                    #pragma unroll 1
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const int col = half * 128 + c16 * 16;
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(trow + col, v);
+                        tmem_ld_wait();
+                        const int64_t n = n0 + col;
+                        if (m >= m_end || n >= p.N) continue;
+                        float* yrow = p.Yp + (int64_t)slot * p.N + n;    // N a multiple of 64
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            *reinterpret_cast<float4*>(yrow + 4 * i) =
+                                make_float4(w * __uint_as_float(v[4 * i]), w * __uint_as_float(v[4 * i + 1]),
+                                            w * __uint_as_float(v[4 * i + 2]), w * __uint_as_float(v[4 * i + 3]));
                     }
                 }
             }
@@ -268,24 +349,30 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int SUBM>
-nvfp4_status launch_tc_impl(const uint16_t* X, const TcKParams& kp, cudaStream_t stream) {
+nvfp4_status encode_rows_map(CUtensorMap* tmap, const uint16_t* X, int64_t rows, int64_t K) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(NVFP4_ERR_CUDA, "tile GEMM: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap tmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)kp.K, (cuuint64_t)kp.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)kp.K * 2};
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {64, 128};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult cr = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+    CUresult cr = enc(tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "tile GEMM: tensor map encode failed (%d)", (int)cr);
+    return NVFP4_OK;
+}
+
+template <int SUBM, TcMode MODE>
+nvfp4_status launch_tc_impl(const uint16_t* X, int64_t x_rows, const TcKParams& kp, dim3 grid, cudaStream_t stream) {
+    CUtensorMap tmap;
+    nvfp4_status st = encode_rows_map(&tmap, X, x_rows, kp.K);
+    if (st != NVFP4_OK) return st;
     const size_t smem = TcSmem<SUBM>::total + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SUBM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SUBM, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "tile GEMM: shared memory attribute");
-    const dim3 grid((unsigned)ceil_div(kp.N, kBN), (unsigned)ceil_div(kp.M, 128 * SUBM), 1);
-    tc_gemm_kernel<SUBM><<<grid, kTcThreads, smem, stream>>>(tmap, kp);
+    tc_gemm_kernel<SUBM, MODE><<<grid, kTcThreads, smem, stream>>>(tmap, kp);
     return check_cuda(cudaGetLastError(), "tile GEMM: launch");
 }
 
@@ -308,7 +395,25 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     kp.rp = p.rp; kp.Y = p.Y; kp.M = p.M; kp.N = p.N; kp.K = p.K;
     kp.KB = round_up(p.K, kBlockK) / kBlockK;
     kp.status = p.status;
-    return p.M <= 128 ? launch_tc_impl<1>(X, kp, stream) : launch_tc_impl<2>(X, kp, stream);
+    const unsigned gx = (unsigned)ceil_div(p.N, kBN);
+    if (p.M <= 128) return launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128)), stream);
+    return launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256)), stream);
+}
+
+nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
+    TcKParams kp{};
+    kp.rp = m.w; kp.w_stride = m.w_stride; kp.items = m.items; kp.n_items = m.n_items;
+    kp.perm = m.perm; kp.wts = m.wts; kp.I = m.I; kp.status = m.status;
+    kp.N = m.N; kp.K = m.K; kp.KB = round_up(m.K, kBlockK) / kBlockK;
+    const bool fc1 = m.fc1;
+    kp.Y = m.H; kp.Yp = m.Yp;
+    const unsigned gx = fc1 ? (unsigned)(m.I / 128) : (unsigned)ceil_div(m.N, kBN);
+    const dim3 grid(gx, (unsigned)m.max_items);
+    if (m.subm == 1)
+        return fc1 ? launch_tc_impl<1, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, stream)
+                   : launch_tc_impl<1, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, stream);
+    return fc1 ? launch_tc_impl<2, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, stream)
+               : launch_tc_impl<2, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, stream);
 }
 
 }  // namespace nvfp4

@@ -15,6 +15,27 @@ struct TcParams {
     int* status;
 };
 
+// Grouped MoE use of the tile kernel: work items of up to 128*subm permuted
+// rows of one expert; X rows are already in permuted (expert-contiguous) order.
+struct TcMoeParams {
+    bool fc1;                 // FC1 (gate/up + SwiGLU -> H) or FC2 (x p -> Yp)
+    int subm;                 // 1 or 2: 128 or 256 rows per work item
+    const uint16_t* X;        // [x_rows, K] BF16, permuted rows
+    int64_t x_rows;
+    const uint8_t* w;         // stacked repacked experts
+    size_t w_stride;
+    int64_t N, K, I;          // weight rows (FC1: 2I), inner dimension, intermediate size
+    const int4* items;
+    const int32_t* n_items;
+    int64_t max_items;
+    const int32_t* perm;
+    const float* wts;
+    uint16_t* H;              // FC1 output [x_rows, I]
+    float* Yp;                // FC2 output [slots, N]
+    int* status;
+};
+nvfp4_status launch_tc_moe(const TcMoeParams& p, cudaStream_t stream);
+
 // Shape rule between the decode kernel and the tile kernel.
 bool use_tc_path(int64_t M);
 size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs);

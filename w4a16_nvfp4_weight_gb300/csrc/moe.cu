@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "gemm_decode.cuh"
+#include "gemm_tc.cuh"
 #include "ptx.cuh"
 #include "stream_mma.cuh"
 
@@ -406,6 +407,31 @@ __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk
     *reinterpret_cast<uint2*>(out + i) = make_uint2(lo, hi);
 }
 
+// Rows of X in permuted (expert-contiguous) order, for the tile path:
+// Xp[r] = X[perm[r] / topk], times the AWQ pre-quant scale when given.
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
+                                   const int32_t* __restrict__ perm, int topk, int64_t n, int64_t H,
+                                   uint16_t* __restrict__ Xp) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (i >= n * H) return;
+    const int64_t r = i / H, k = i % H;
+    const int64_t t = perm[r] / topk;
+    uint4 v = *reinterpret_cast<const uint4*>(X + t * H + k);
+    if (pqs != nullptr) {
+        const uint4 sv4 = *reinterpret_cast<const uint4*>(pqs + k);
+        uint32_t xv[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint16_t lo = awq_mul_bf16((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
+            const uint16_t hi = awq_mul_bf16((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
+            xv[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        v = make_uint4(xv[0], xv[1], xv[2], xv[3]);
+    }
+    *reinterpret_cast<uint4*>(Xp + i) = v;
+}
+
 size_t moe_lin_smem(int MT, bool gated) {
     const int tok = 8 * MT;
     const size_t part = gated ? ((size_t)tok * 64 + 8) * 2 : (size_t)tok * 128 + 8;
@@ -435,16 +461,22 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
 }
 
 struct MoeLayout {
-    size_t idx, wts, offsets, perm, inv, items, n_items, xs, h, yp, total;
-    int tok, mt;
+    size_t idx, wts, offsets, perm, inv, items, n_items, xs, xp, h, yp, total;
+    bool tile;              // tensor-core tile path (many rows per expert) or the streaming path
+    int tok, mt, subm;
     int64_t max_items;
 };
 
 MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq) {
     MoeLayout L{};
     const int64_t n = T * topk;
-    L.mt = (n / std::max(E, 1)) > 8 ? 2 : 1;        // rows per expert on average
-    L.tok = 8 * L.mt;
+    const int64_t per_expert = n / std::max(E, 1);   // routed rows per expert on average
+    // Many rows per expert: tcgen05 tiles of 128 (or 256) routed rows; few rows:
+    // the streaming kernel with 8 or 16 rows per work item.
+    L.tile = per_expert >= 16 && I % 128 == 0;
+    L.subm = per_expert >= 192 ? 2 : 1;
+    L.mt = per_expert > 8 ? 2 : 1;
+    L.tok = L.tile ? 128 * L.subm : 8 * L.mt;
     L.max_items = ceil_div(n, L.tok) + std::min<int64_t>(E, n);
     size_t off = 0;
     auto take = [&](size_t bytes) { const size_t o = off; off += (size_t)round_up((int64_t)bytes, 256); return o; };
@@ -455,7 +487,8 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq)
     L.inv = take(n * 4);
     L.items = take(L.max_items * 16);
     L.n_items = take(4);
-    L.xs = awq ? take(T * H * 2) : 0;
+    L.xs = (awq && !L.tile) ? take(T * H * 2) : 0;
+    L.xp = L.tile ? take(n * H * 2) : 0;
     L.h = take(n * I * 2);
     L.yp = take(n * H * 4);
     L.total = off;
@@ -522,7 +555,7 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
     nvfp4_status st;
 
     const uint16_t* xin = (const uint16_t*)X;
-    if (fc1_pre_quant_scale) {
+    if (fc1_pre_quant_scale && !L.tile) {
         st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H, s);
         if (st != NVFP4_OK) return st;
         xin = (const uint16_t*)(ws + L.xs);
@@ -532,31 +565,49 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
     permute_kernel<<<1, kPermThreads, 0, s>>>(idx, n, E, L.tok, offsets, perm, inv, items, n_items);
     if ((st = check_cuda(cudaGetLastError(), "MoE permute: launch")) != NVFP4_OK) return st;
 
-    // expected work items in flight, for the split-K choice
-    const int64_t est_items = std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
-    MoeLinParams p1{};
-    p1.w = (const uint8_t*)fc1; p1.w_stride = nvfp4_repack_size(2 * I, H);
-    p1.N = 2 * I; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
-    p1.splits = moe_splits((I / 64) * est_items, p1.KB, 4);
-    p1.kbs = (int)ceil_div(p1.KB, p1.splits);
-    p1.splits = (int)ceil_div(p1.KB, p1.kbs);
-    p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
-    p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
-    st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s)
-                   : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s);
-    if (st != NVFP4_OK) return st;
+    if (L.tile) {
+        // gather the routed rows into expert-contiguous order, then two tile GEMMs
+        uint16_t* xp = (uint16_t*)(ws + L.xp);
+        gather_rows_kernel<<<(unsigned)ceil_div(n * H / 8, 256), 256, 0, s>>>(
+            (const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, perm, topk, n, H, xp);
+        if ((st = check_cuda(cudaGetLastError(), "MoE gather: launch")) != NVFP4_OK) return st;
+        TcMoeParams t1{};
+        t1.fc1 = true; t1.subm = L.subm; t1.X = xp; t1.x_rows = n;
+        t1.w = (const uint8_t*)fc1; t1.w_stride = nvfp4_repack_size(2 * I, H);
+        t1.N = 2 * I; t1.K = H; t1.I = I; t1.items = items; t1.n_items = n_items; t1.max_items = L.max_items;
+        t1.perm = perm; t1.wts = wts; t1.H = hbuf; t1.status = status;
+        if ((st = launch_tc_moe(t1, s)) != NVFP4_OK) return st;
+        TcMoeParams t2 = t1;
+        t2.fc1 = false; t2.X = hbuf; t2.w = (const uint8_t*)fc2; t2.w_stride = nvfp4_repack_size(H, I);
+        t2.N = H; t2.K = I; t2.Yp = yp; t2.H = nullptr;
+        if ((st = launch_tc_moe(t2, s)) != NVFP4_OK) return st;
+    } else {
+        // expected work items in flight, for the split-K choice
+        const int64_t est_items = std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
+        MoeLinParams p1{};
+        p1.w = (const uint8_t*)fc1; p1.w_stride = nvfp4_repack_size(2 * I, H);
+        p1.N = 2 * I; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
+        p1.splits = moe_splits((I / 64) * est_items, p1.KB, 4);
+        p1.kbs = (int)ceil_div(p1.KB, p1.splits);
+        p1.splits = (int)ceil_div(p1.KB, p1.kbs);
+        p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
+        p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
+        st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s)
+                       : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s);
+        if (st != NVFP4_OK) return st;
 
-    MoeLinParams p2{};
-    p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
-    p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
-    p2.splits = moe_splits(ceil_div(H, 128) * est_items, p2.KB, 4);
-    p2.kbs = (int)ceil_div(p2.KB, p2.splits);
-    p2.splits = (int)ceil_div(p2.KB, p2.kbs);
-    p2.X = hbuf; p2.perm = perm; p2.topk = topk; p2.items = items; p2.n_items = n_items;
-    p2.I = I; p2.Yp = yp; p2.wts = wts; p2.status = status;
-    st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s)
-                   : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s);
-    if (st != NVFP4_OK) return st;
+        MoeLinParams p2{};
+        p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
+        p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
+        p2.splits = moe_splits(ceil_div(H, 128) * est_items, p2.KB, 4);
+        p2.kbs = (int)ceil_div(p2.KB, p2.splits);
+        p2.splits = (int)ceil_div(p2.KB, p2.kbs);
+        p2.X = hbuf; p2.perm = perm; p2.topk = topk; p2.items = items; p2.n_items = n_items;
+        p2.I = I; p2.Yp = yp; p2.wts = wts; p2.status = status;
+        st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s)
+                       : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s);
+        if (st != NVFP4_OK) return st;
+    }
 
     combine_kernel<<<(unsigned)ceil_div(T * H / 4, 256), 256, 0, s>>>(yp, T, topk, H, (uint16_t*)out);
     return check_cuda(cudaGetLastError(), "MoE combine: launch");
