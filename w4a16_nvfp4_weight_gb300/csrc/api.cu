@@ -84,8 +84,12 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
     const int64_t RG = ceil_div(N, 128);
     const int64_t base = RG * ceil_div(M, TOK);
-    // two resident CTAs per SM: split K until the grid covers them
-    int64_t splits = std::min<int64_t>(std::min<int64_t>(8, KB), std::max<int64_t>(1, ceil_div(2LL * sm_count(), base)));
+    // Split K until about three CTAs per SM are resident (one wave), with at
+    // most 8 CTAs per cluster (larger, non-portable clusters measured slower)
+    // and at least two 64-k blocks per CTA.
+    const int64_t target = 3LL * sm_count();
+    int64_t splits = std::max<int64_t>(1, target / std::max<int64_t>(base, 1));
+    splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / 2)));
     const int64_t kbs = ceil_div(KB, splits);
     splits = ceil_div(KB, kbs);
     pl.splits = (int)splits;
@@ -124,7 +128,7 @@ extern "C" nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stre
 
 extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
-    if (use_tc_path(M)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
+    if (use_tc_path(M, N)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
     return has_pre_quant_scale ? awq_bytes(M, K) : 0;
 }
 
@@ -146,7 +150,7 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, co
     int* status = device_status_ptr();
     if (!status) return fail(NVFP4_ERR_CUDA, "nvfp4_w4a16_gemm: no CUDA device");
     cudaStream_t s = (cudaStream_t)stream;
-    if (use_tc_path(M)) {
+    if (use_tc_path(M, N)) {
         TcParams tp{};
         tp.X = (const uint16_t*)X; tp.pqs = (const uint16_t*)pre_quant_scale;
         tp.rp = (const uint8_t*)repacked; tp.Y = (uint16_t*)Y;

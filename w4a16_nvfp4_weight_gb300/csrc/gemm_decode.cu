@@ -271,8 +271,8 @@ nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* 
 }
 
 size_t decode_smem_bytes(int MT, int /*kbs*/) {
-    // partial slots: splits x ceil(128 * TOK / splits) floats <= 128 * TOK + 7
-    return Smem::ring + kStages * stage_bytes(8 * MT) + ((size_t)kRowsPerCta * MT * 8 + 8) * 4;
+    // partial slots: splits x ceil(128 * TOK / splits) floats <= 128 * TOK + 15 (splits <= 16)
+    return Smem::ring + kStages * stage_bytes(8 * MT) + ((size_t)kRowsPerCta * MT * 8 + 16) * 4;
 }
 
 nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream) {
@@ -281,6 +281,10 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream
     const void* fn = MT == 1 ? (const void*)decode_kernel<1> : (const void*)decode_kernel<2>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
+    if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return check_cuda(e, "decode GEMM: cluster size attribute");
+    }
     const int64_t rgs = ceil_div(p.N, kRowsPerCta);
     const int64_t mchunks = ceil_div(p.M, 8 * MT);
     cudaLaunchConfig_t cfg = {};

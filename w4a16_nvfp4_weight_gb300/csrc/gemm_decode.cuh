@@ -12,7 +12,7 @@ struct DecodeParams {
     int64_t M, N, K;
     int64_t KB;               // 64-k blocks of the padded K
     int kbs;                  // 64-k blocks per split
-    int splits;               // CTAs per cluster along K (<= 8)
+    int splits;               // CTAs per cluster along K (<= 16)
     int* status;              // device status word
 };
 

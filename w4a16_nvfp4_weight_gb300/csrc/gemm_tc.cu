@@ -380,7 +380,11 @@ size_t awq_ws_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 2
 
 }  // namespace
 
-bool use_tc_path(int64_t M) { return M > 16; }
+bool use_tc_path(int64_t M, int64_t N) {
+    if (M <= 16) return false;
+    const int64_t tiles = ceil_div(N, kBN) * (M <= 128 ? ceil_div(M, 128) : ceil_div(M, 256));
+    return tiles >= sm_count() / 2 || M >= 512;
+}
 
 size_t tc_workspace_bytes(int64_t M, int64_t, int64_t K, bool has_pqs) { return has_pqs ? awq_ws_bytes(M, K) : 0; }
 

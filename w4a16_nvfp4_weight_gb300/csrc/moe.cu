@@ -96,65 +96,83 @@ __global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E,
 
 // ----------------------------------------------------------------- permute --
 constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
 
+// Warp w owns the contiguous slot range [w*seg, (w+1)*seg).  Pass 1 counts each
+// warp's slots per expert (warp-private counters, 32 slots at a time with
+// __match_any_sync); a scan over experts and warps gives every (warp, expert)
+// its first position; pass 2 walks the same slots again and places them.
+// Slots of one expert therefore keep their flat order t*k+j: stable.
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
                int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                int4* __restrict__ items, int32_t* __restrict__ n_items) {
-    __shared__ int cnt[kMaxExperts];
-    __shared__ int base[kMaxExperts];
-    __shared__ int item_base[kMaxExperts];
-    __shared__ int wcnt[kPermThreads / 32][kMaxExperts];
+    extern __shared__ int perm_smem[];
+    int* wcnt = perm_smem;                                  // [kPermWarps][E], then positions
+    int* cnt = perm_smem + kPermWarps * E;                  // [E]
+    int* item_base = cnt + E;                               // [E]
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    const int64_t seg = (n + kPermWarps - 1) / kPermWarps;
+    const int64_t s0 = n < (int64_t)w * seg ? n : (int64_t)w * seg;
+    const int64_t s1 = n < s0 + seg ? n : s0 + seg;
+    for (int k = tid; k < kPermWarps * E; k += kPermThreads) wcnt[k] = 0;
     __syncthreads();
-    for (int64_t i = tid; i < n; i += kPermThreads) atomicAdd(&cnt[idx[i]], 1);
+    int* my = wcnt + w * E;
+    for (int64_t c0 = s0; c0 < s1; c0 += 32) {
+        const int64_t i = c0 + lane;
+        const int e = i < s1 ? idx[i] : -1;
+        const uint32_t mask = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && __popc(mask & ((1u << lane) - 1u)) == 0) my[e] += __popc(mask);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per expert: total, then each warp's first position (exclusive scan over warps)
+    for (int e = tid; e < E; e += kPermThreads) {
+        int run = 0;
+        for (int ww = 0; ww < kPermWarps; ++ww) {
+            const int c = wcnt[ww * E + e];
+            wcnt[ww * E + e] = run;
+            run += c;
+        }
+        cnt[e] = run;
+    }
     __syncthreads();
     if (tid == 0) {
         int run = 0, items_run = 0;
         for (int e = 0; e < E; ++e) {
             offsets[e] = run;
-            base[e] = run;
             item_base[e] = items_run;
-            run += cnt[e];
-            items_run += (cnt[e] + tok - 1) / tok;
+            const int c = cnt[e];
+            cnt[e] = run;                                    // now the expert's offset
+            run += c;
+            items_run += (c + tok - 1) / tok;
         }
         offsets[E] = run;
         *n_items = items_run;
     }
     __syncthreads();
     for (int e = tid; e < E; e += kPermThreads) {
-        const int c = cnt[e];
+        const int off = cnt[e], c = offsets[e + 1] - off;
         for (int r = 0, k = 0; r < c; r += tok, ++k)
-            items[item_base[e] + k] = make_int4(e, base[e] + r, min(tok, c - r), 0);
+            items[item_base[e] + k] = make_int4(e, off + r, min(tok, c - r), 0);
     }
-    // Stable placement, 1024 slots at a time: a slot's position is its expert's
-    // running base plus the number of earlier slots with the same expert in
-    // this chunk (earlier warps, then earlier lanes of its own warp).
-    for (int64_t c0 = 0; c0 < n; c0 += kPermThreads) {
-        const int64_t i = c0 + tid;
-        const int e = i < n ? idx[i] : -1;
-        for (int k = tid; k < (kPermThreads / 32) * E; k += kPermThreads) wcnt[k / E][k % E] = 0;
-        __syncthreads();
+    for (int64_t c0 = s0; c0 < s1; c0 += 32) {
+        const int64_t i = c0 + lane;
+        const int e = i < s1 ? idx[i] : -1;
         const uint32_t mask = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(mask & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) wcnt[w][e] = __popc(mask);
-        __syncthreads();
         if (e >= 0) {
-            int pos = base[e] + rank;
-            for (int w2 = 0; w2 < w; ++w2) pos += wcnt[w2][e];
+            const int pos = cnt[e] + my[e] + rank;
             perm[pos] = (int32_t)i;
             inv[i] = pos;
         }
-        __syncthreads();
-        for (int k = tid; k < E; k += kPermThreads) {
-            int s = 0;
-            for (int w2 = 0; w2 < kPermThreads / 32; ++w2) s += wcnt[w2][k];
-            base[k] += s;
-        }
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && rank == 0) my[e] += __popc(mask);
+        __syncwarp();
     }
 }
+
+size_t permute_smem_bytes(int E) { return ((size_t)kPermWarps * E + 2 * E) * sizeof(int); }
 
 // ------------------------------------------------- grouped streaming linear --
 constexpr int kWarps = 8;                      // 8 x 16 = 128 weight rows per CTA
@@ -562,7 +580,12 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
     }
     route_kernel<<<(unsigned)ceil_div(T, 8), 256, 0, s>>>(router_logits, T, E, topk, idx, wts);
     if ((st = check_cuda(cudaGetLastError(), "MoE route: launch")) != NVFP4_OK) return st;
-    permute_kernel<<<1, kPermThreads, 0, s>>>(idx, n, E, L.tok, offsets, perm, inv, items, n_items);
+    {
+        const size_t psmem = permute_smem_bytes(E);
+        cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+        if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
+        permute_kernel<<<1, kPermThreads, psmem, s>>>(idx, n, E, L.tok, offsets, perm, inv, items, n_items);
+    }
     if ((st = check_cuda(cudaGetLastError(), "MoE permute: launch")) != NVFP4_OK) return st;
 
     if (L.tile) {
