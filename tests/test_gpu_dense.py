@@ -142,6 +142,18 @@ def test_gemm_larger_m_small(M, K, N):
     gu.compare(y, ref, f"M={M} K={K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(512, 8192, 512), (516, 4096, 1000), (600, 6144, 384)])
+def test_gemm_tile_split_k(M, K, N):
+    """Few output tiles and a long K: the tile kernel splits K and sums the FP32
+    partials in split order (M and N tails included)."""
+    c = synth.gaussian_case(M, K, N, seed=3000 + M + N, awq=(M == 516))
+    y = _gemm(c)
+    _, ref = gu.oracle_linear(c)
+    gu.compare(y, ref, f"split-K M={M} K={K} N={N}")
+    y2 = _gemm(c)
+    assert np.array_equal(y, y2)          # fixed reduction order
+
+
 def test_dropped_awq_scale_fails_the_bar():
     c = synth.gaussian_case(8, 1024, 512, seed=77, awq=True)
     y_no = _gemm(c, awq=False)

@@ -65,6 +65,8 @@ struct TcKParams {
     const float* wts;         // MoE FC2: routing weights per slot
     int64_t M, N, K, KB;      // dense M; weight rows N (FC1: 2I) and inner K
     int64_t I;                // MoE FC1: intermediate size
+    int kb_per_split;         // dense split-K: 64-k blocks per split (grid z = split)
+    float* partial;           // dense split-K: FP32 partials [splits, M, N], or null
     int* status;
 };
 
@@ -114,7 +116,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
         m_end = p.M;
     }
     const int64_t n0 = (int64_t)blockIdx.x * (MODE == TcMode::kMoeFc1 ? kBN / 2 : kBN);
-    const int nkb = (int)p.KB;
+    // dense split-K: this CTA covers 64-k blocks [kb_first, kb_first + nkb)
+    const int kb_first = kMoe ? 0 : (int)blockIdx.z * p.kb_per_split;
+    const int64_t kb_left = p.KB - kb_first;
+    const int nkb = kMoe ? (int)p.KB : (int)(kb_left < p.kb_per_split ? kb_left : p.kb_per_split);
 
     if (tid == 0) {
         for (int s = 0; s < kS1; ++s) {
@@ -165,7 +170,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                     if (kb >= kS1 && !mbar_wait(&tma_empty[s], ((kb / kS1) - 1) & 1, p.status)) break;
                     mbar_arrive_expect_tx(&tma_full[s], SUBM * kATileBytes + kBRawBytes);
                     for (int mi = 0; mi < SUBM; ++mi)
-                        tma_load_2d(a_ring + ((size_t)s * SUBM + mi) * kATileBytes, &tmap_x, kb * 64,
+                        tma_load_2d(a_ring + ((size_t)s * SUBM + mi) * kATileBytes, &tmap_x, (kb_first + kb) * 64,
                                     (int)(m0 + mi * 128), &tma_full[s]);
                     if constexpr (MODE == TcMode::kMoeFc1) {
                         bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes,
@@ -173,8 +178,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                         bulk_g2s(braw_ring + (size_t)s * kBRawBytes + kBRawBytes / 2,
                                  wtile_up + (size_t)kb * kBRawBytes, kBRawBytes / 2, &tma_full[s]);
                     } else {
-                        bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)kb * kBRawBytes, kBRawBytes,
-                                 &tma_full[s]);
+                        bulk_g2s(braw_ring + (size_t)s * kBRawBytes, wtile + (size_t)(kb_first + kb) * kBRawBytes,
+                                 kBRawBytes, &tma_full[s]);
                     }
                     ++issued;
                 }
@@ -266,6 +271,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                         tmem_ld_wait();
                         if (m >= m_end) continue;
                         const int64_t n = n0 + col;
+                        if (p.partial != nullptr) {
+                            // split-K: FP32 partial rows, summed in split order afterwards
+                            float* prow = p.partial + ((int64_t)blockIdx.z * p.M + m) * p.N;
+                            if (vec_ok && n + 16 <= p.N) {
+                                #pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    *reinterpret_cast<uint4*>(prow + n + 4 * i) =
+                                        make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                            } else {
+                                for (int i = 0; i < 16 && n + i < p.N; ++i) prow[n + i] = __uint_as_float(v[i]);
+                            }
+                            continue;
+                        }
                         uint32_t packed[8];
                         #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -331,6 +349,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     }
 }
 
+// Y = RN_bf16(sum over splits of the FP32 partials), splits in order.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t MN,
+                                     uint16_t* __restrict__ Y) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= MN) return;
+    float4 s = *reinterpret_cast<const float4*>(part + i);
+    for (int k = 1; k < splits; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(part + (int64_t)k * MN + i);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    // Y is only guaranteed 4-byte aligned: two 32-bit stores
+    reinterpret_cast<uint32_t*>(Y + i)[0] = (uint32_t)f32_to_bf16_bits(s.x) | ((uint32_t)f32_to_bf16_bits(s.y) << 16);
+    reinterpret_cast<uint32_t*>(Y + i)[1] = (uint32_t)f32_to_bf16_bits(s.z) | ((uint32_t)f32_to_bf16_bits(s.w) << 16);
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -378,6 +411,38 @@ nvfp4_status launch_tc_impl(const uint16_t* X, int64_t x_rows, const TcKParams& 
 
 size_t awq_ws_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
 
+// Split-K plan of the dense tile GEMM from a simple cost model (measured on
+// GB300): a wave of tile CTAs costs about 0.78 us per 64-k block with two M
+// sub-tiles (0.45 us with one) plus 3 us, and a split adds its FP32 partials'
+// write and read at ~6 TB/s plus a 2 us reduction.  Split (<= 8 ways, >= 12
+// blocks per split) only when the model predicts at least 20% less time.
+struct TcSplit {
+    int splits, kbs;
+};
+
+TcSplit plan_tc_split(int64_t M, int64_t N, int64_t K) {
+    const int64_t KB = round_up(K, kBlockK) / kBlockK;
+    const int64_t tiles = ceil_div(N, kBN) * (M <= 128 ? ceil_div(M, 128) : ceil_div(M, 256));
+    const int64_t sms = sm_count();
+    const double t_blk = M <= 128 ? 0.45 : 0.78;
+    auto cost = [&](int64_t s) {
+        const int64_t kbs = ceil_div(KB, s);
+        double t = (double)ceil_div(tiles * s, sms) * ((double)kbs * t_blk + 3.0);
+        if (s > 1) t += 2.0 * (double)s * (double)M * (double)N * 4.0 / 6.0e6 + 2.0;
+        return t;
+    };
+    TcSplit best{1, (int)KB};
+    if ((M % 4) != 0 || (N % 4) != 0) return best;
+    double best_t = cost(1);
+    const double limit = 0.8 * best_t;
+    for (int s = 2; s <= 8 && KB / s >= 12; ++s) {
+        const double t = cost(s);
+        if (t < limit && t < best_t) { best_t = t; best = TcSplit{s, (int)ceil_div(KB, s)}; }
+    }
+    if (best.splits > 1) best.splits = (int)ceil_div(KB, best.kbs);
+    return best;
+}
+
 }  // namespace
 
 bool use_tc_path(int64_t M, int64_t N) {
@@ -386,7 +451,11 @@ bool use_tc_path(int64_t M, int64_t N) {
     return tiles >= sm_count() / 2 || M >= 512;
 }
 
-size_t tc_workspace_bytes(int64_t M, int64_t, int64_t K, bool has_pqs) { return has_pqs ? awq_ws_bytes(M, K) : 0; }
+size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs) {
+    const TcSplit sp = plan_tc_split(M, N, K);
+    const size_t part = sp.splits > 1 ? (size_t)round_up((int64_t)sp.splits * M * N * 4, 256) : 0;
+    return (has_pqs ? awq_ws_bytes(M, K) : 0) + part;
+}
 
 nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     const uint16_t* X = p.X;
@@ -399,9 +468,20 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     kp.rp = p.rp; kp.Y = p.Y; kp.M = p.M; kp.N = p.N; kp.K = p.K;
     kp.KB = round_up(p.K, kBlockK) / kBlockK;
     kp.status = p.status;
+    const TcSplit sp = plan_tc_split(p.M, p.N, p.K);
+    kp.kb_per_split = sp.kbs;
+    if (sp.splits > 1)
+        kp.partial = reinterpret_cast<float*>((uint8_t*)p.workspace + (p.pqs ? awq_ws_bytes(p.M, p.K) : 0));
     const unsigned gx = (unsigned)ceil_div(p.N, kBN);
-    if (p.M <= 128) return launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128)), stream);
-    return launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256)), stream);
+    nvfp4_status st;
+    if (p.M <= 128)
+        st = launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128), sp.splits), stream);
+    else
+        st = launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256), sp.splits), stream);
+    if (st != NVFP4_OK || sp.splits == 1) return st;
+    const int64_t MN = p.M * p.N;
+    splitk_reduce_kernel<<<(unsigned)ceil_div(MN / 4, 256), 256, 0, stream>>>(kp.partial, sp.splits, MN, p.Y);
+    return check_cuda(cudaGetLastError(), "tile GEMM: split-K reduction launch");
 }
 
 nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
@@ -409,6 +489,7 @@ nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
     kp.rp = m.w; kp.w_stride = m.w_stride; kp.items = m.items; kp.n_items = m.n_items;
     kp.perm = m.perm; kp.wts = m.wts; kp.I = m.I; kp.status = m.status;
     kp.N = m.N; kp.K = m.K; kp.KB = round_up(m.K, kBlockK) / kBlockK;
+    kp.kb_per_split = (int)kp.KB;
     const bool fc1 = m.fc1;
     kp.Y = m.H; kp.Yp = m.Yp;
     const unsigned gx = fc1 ? (unsigned)(m.I / 128) : (unsigned)ceil_div(m.N, kBN);
