@@ -133,6 +133,17 @@ def test_gemm_decode_small(M, K, N):
     gu.compare(y, ref, f"M={M} K={K} N={N}")
 
 
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_gemm_decode_deep_ring_partial_stages(M):
+    """K = 8240 over 8 splits: 17-block slices (long enough for the deep ring)
+    whose last ring stage holds one block, a last split of 10 blocks and a
+    48-element K tail; 64 CTAs, so the grid is spread one per SM."""
+    c = synth.gaussian_case(M, 8240, 1024, seed=4000 + M, awq=(M == 9))
+    y = _gemm(c)
+    _, ref = gu.oracle_linear(c)
+    gu.compare(y, ref, f"M={M} K=8240 N=1024")
+
+
 @pytest.mark.parametrize("M", [17, 100, 128, 300])
 @pytest.mark.parametrize("K,N", [(256, 256), (2064, 1000), (720, 3000)])
 def test_gemm_larger_m_small(M, K, N):

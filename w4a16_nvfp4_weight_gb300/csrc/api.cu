@@ -73,7 +73,7 @@ int sm_count() {
 
 // Split-K plan of the decode kernel for an M x N x K problem.
 struct DecodePlan {
-    int MT, splits, kbs;
+    int MT, ring, splits, kbs;
     bool ok;
 };
 
@@ -84,16 +84,27 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
     const int64_t RG = ceil_div(N, 128);
     const int64_t base = RG * ceil_div(M, TOK);
-    // Split K until about three CTAs per SM are resident (one wave), with at
-    // most 8 CTAs per cluster (larger, non-portable clusters measured slower)
-    // and at least two 64-k blocks per CTA.
-    const int64_t target = 3LL * sm_count();
-    int64_t splits = std::max<int64_t>(1, target / std::max<int64_t>(base, 1));
-    splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / 2)));
-    const int64_t kbs = ceil_div(KB, splits);
-    splits = ceil_div(KB, kbs);
-    pl.splits = (int)splits;
-    pl.kbs = (int)kbs;
+    // Split K until the CTAs fill one wave (as many per SM as shared memory
+    // holds), with at most 8 CTAs per cluster (larger, non-portable clusters
+    // measured slower) and at least two 64-k blocks per CTA.
+    auto split_for = [&](int ring) {
+        const int64_t target = (int64_t)decode_ctas_per_sm(pl.MT, ring) * sm_count();
+        int64_t splits = std::max<int64_t>(1, target / std::max<int64_t>(base, 1));
+        splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / 2)));
+        const int64_t kbs = ceil_div(KB, splits);
+        pl.splits = (int)ceil_div(KB, kbs);
+        pl.kbs = (int)kbs;
+        pl.ring = ring;
+    };
+    // Slices of at most 16 blocks spend much of their time filling the ring
+    // and reducing: those take the shallow ring, which packs more CTAs per SM,
+    // when that buys a finer split.
+    split_for(kRingDeep);
+    if (pl.kbs <= 16) {
+        const DecodePlan deep = pl;
+        split_for(kRingShallow);
+        if (pl.splits <= deep.splits) pl = deep;
+    }
     pl.ok = true;
     return pl;
 }
@@ -174,5 +185,5 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, co
     p.M = M; p.N = N; p.K = K;
     p.KB = round_up(K, kBlockK) / kBlockK;
     p.kbs = pl.kbs; p.splits = pl.splits; p.status = status;
-    return launch_decode(p, pl.MT, s);
+    return launch_decode(p, pl.MT, pl.ring, s);
 }

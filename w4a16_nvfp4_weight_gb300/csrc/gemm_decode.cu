@@ -3,10 +3,9 @@
 //
 // The weight is the only large operand, so every byte of it is read once.  A
 // CTA owns 128 weight rows (8 consumer warps x 16 rows) and one K slice.  A
-// producer warp streams the slice through a 3-stage shared-memory ring with
-// bulk (TMA) copies: per stage three 64-k blocks of weights (3 x 4608
-// contiguous bytes) and the matching activation chunk, one copy per token
-// row.  Per 64-k atom a lane reads 16 code bytes and 2 scale bytes, looks its
+// producer warp streams the slice through a shared-memory ring with bulk
+// (TMA) copies: per stage four 64-k blocks of weights (4 x 4608 contiguous
+// bytes) and the matching activation chunk, one copy per token row.  Per 64-k atom a lane reads 16 code bytes and 2 scale bytes, looks its
 // two group tables up and expands the codes straight into mma.sync A
 // fragments (weights on the M side, tokens on the N side).  Within a
 // 16-element group the MMA's k order is permuted so that one lane consumes one
@@ -26,6 +25,8 @@
 // (Description / Changes table: dequantize the NVFP4 weight each forward step
 // and run a BF16 GEMM); AWQ activation scaling from "[None][fix] Apply the
 // NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL" (Description).
+#include <algorithm>
+
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -42,14 +43,30 @@ namespace {
 constexpr int kWarps = 8;                      // consumer warps: 8 x 16 = 128 weight rows
 constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
 constexpr int kRowsPerCta = kWarps * kAtomRows;
-constexpr int kStages = 3;
-constexpr int kBlocksPerStage = 3;             // 64-k blocks per ring stage
 constexpr uint32_t kBlockBytes = kWarps * kAtomBytes;          // 4608: 128 rows x 64 k, contiguous
-constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
-constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;      // activation row stride in a stage (+16 B)
 
-__host__ __device__ constexpr size_t x_stage_bytes(int tok) { return (size_t)tok * kXRowElems * 2; }
-__host__ __device__ constexpr size_t stage_bytes(int tok) { return kWeightStageBytes + x_stage_bytes(tok); }
+// Ring shape per number of 8-token MMA tiles (MT) and ring kind: stages x
+// 64-k blocks per stage.  Larger stages amortise the per-stage barrier work;
+// with 16 tokens the activation chunks are twice as large, and two stages
+// keep three CTAs resident per SM.  The shallow rings fit four CTAs per SM.
+// The shapes were chosen by timing the alternatives on GB300 over the decode
+// layer shapes.
+template <int MT, int R> struct Ring;
+template <> struct Ring<1, kRingDeep> { static constexpr int kStages = 3, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingDeep> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
+template <> struct Ring<1, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
+
+template <int MT, int R> struct RingGeom {
+    static constexpr int kTok = 8 * MT;
+    static constexpr int kStages = Ring<MT, R>::kStages;
+    static constexpr int kBlocksPerStage = Ring<MT, R>::kBlocksPerStage;
+    static constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
+    static constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;   // activation row stride (+16 B)
+    static constexpr size_t kXStageBytes = (size_t)kTok * kXRowElems * 2;
+    static constexpr size_t kStageBytes = kWeightStageBytes + kXStageBytes;
+    static_assert(kStageBytes % 16 == 0 && (kXRowElems * 2) % 16 == 0, "bulk copies need 16-byte alignment");
+};
 
 struct Smem {
     // offsets in bytes from the dynamic shared memory base
@@ -59,12 +76,17 @@ struct Smem {
     static constexpr size_t ring = lut + kLutBytes;
 };
 
-template <int MT>
+template <int MT, int R>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int TOK = 8 * MT;
-    constexpr size_t kStageBytes = stage_bytes(TOK);
+    using G = RingGeom<MT, R>;
+    constexpr int TOK = G::kTok;
+    constexpr int kStages = G::kStages;
+    constexpr int kBlocksPerStage = G::kBlocksPerStage;
+    constexpr uint32_t kWeightStageBytes = G::kWeightStageBytes;
+    constexpr int kXRowElems = G::kXRowElems;
+    constexpr size_t kStageBytes = G::kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::bars);
     uint64_t* empty = full + kStages;
     uint64_t* lut_bar = empty + kStages;
@@ -104,7 +126,7 @@ decode_kernel(const DecodeParams p) {
     // k tail, as earlier values of the same row, which meet zero weights).
     for (int s = 0; s < kStages; ++s) {
         uint4* xsb = reinterpret_cast<uint4*>(ring + s * kStageBytes + kWeightStageBytes);
-        for (int i = tid; i < (int)(x_stage_bytes(TOK) / 16); i += kThreads) xsb[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < (int)(G::kXStageBytes / 16); i += kThreads) xsb[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async();      // these generic writes before later bulk copies into the same bytes
     __syncthreads();
@@ -181,22 +203,25 @@ decode_kernel(const DecodeParams p) {
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
         const bool work = rows_valid;
+        // This lane's bytes of stage 0; stage s is kStageBytes further on.
+        const uint8_t* const a0 = ring + warp * kAtomBytes;
+        const uint16_t* const x0 = reinterpret_cast<const uint16_t*>(ring + kWeightStageBytes) +
+                                   g * kXRowElems + q * 16;
+        int s = 0;
+        uint32_t phase = 0;
         for (int i = 0; i < nst && ok; ++i) {
-            const int s = i % kStages;
-            if (!mbar_wait(&full[s], (i / kStages) & 1, p.status)) break;
-            const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
-            const uint8_t* st = ring + s * kStageBytes;
+            if (!mbar_wait(&full[s], phase, p.status)) break;
+            const uint8_t* a = a0 + s * kStageBytes;
             uint4 codes[kBlocksPerStage];
             uint32_t sc[kBlocksPerStage];
             #pragma unroll
             for (int b = 0; b < kBlocksPerStage; ++b) {
-                const uint8_t* a = st + b * kBlockBytes + warp * kAtomBytes;
-                codes[b] = *reinterpret_cast<const uint4*>(a + 16 * lane);
-                sc[b] = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
+                codes[b] = *reinterpret_cast<const uint4*>(a + b * kBlockBytes + 16 * lane);
+                sc[b] = *reinterpret_cast<const uint16_t*>(a + b * kBlockBytes + kAtomCodeBytes + 2 * lane);
             }
             if (work) {
-                const uint16_t* xrow = reinterpret_cast<const uint16_t*>(st + kWeightStageBytes) +
-                                       g * kXRowElems + q * 16;
+                const uint16_t* xrow = x0 + s * (kStageBytes / 2);
+                const int nb = nkb - i * kBlocksPerStage;
                 #pragma unroll
                 for (int b = 0; b < kBlocksPerStage; ++b)
                     if (b < nb) atom_mma<MT, kXRowElems>(codes[b], sc[b], lut, xrow + b * kBlockK, acc);
@@ -204,6 +229,7 @@ decode_kernel(const DecodeParams p) {
             fence_proxy_async();           // reads of the stage before the next bulk copy into it
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (++s == kStages) { s = 0; phase ^= 1u; }
         }
 
         // Push each partial to the CTA that reduces it: output e = token * 128 + row
@@ -270,23 +296,52 @@ nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* 
     return check_cuda(cudaGetLastError(), "AWQ activation scaling: launch");
 }
 
-size_t decode_smem_bytes(int MT, int /*kbs*/) {
+template <int MT, int R>
+constexpr size_t smem_bytes_of() {
     // partial slots: splits x ceil(128 * TOK / splits) floats <= 128 * TOK + 15 (splits <= 16)
-    return Smem::ring + kStages * stage_bytes(8 * MT) + ((size_t)kRowsPerCta * MT * 8 + 16) * 4;
+    return Smem::ring + RingGeom<MT, R>::kStages * RingGeom<MT, R>::kStageBytes +
+           ((size_t)kRowsPerCta * MT * 8 + 16) * 4;
 }
 
-nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream) {
+size_t decode_smem_bytes(int MT, int ring) {
+    if (MT == 1) return ring == kRingDeep ? smem_bytes_of<1, kRingDeep>() : smem_bytes_of<1, kRingShallow>();
+    return ring == kRingDeep ? smem_bytes_of<2, kRingDeep>() : smem_bytes_of<2, kRingShallow>();
+}
+
+int decode_ctas_per_sm(int MT, int ring) {
+    // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+    constexpr size_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
+    const size_t per_cta = decode_smem_bytes(MT, ring) + kReservedPerCta;
+    const int n = (int)(kSmemPerSm / per_cta);
+    return n < 1 ? 1 : (n > 7 ? 7 : n);        // 7 x 288 threads fit in 2048
+}
+
+nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStream_t stream) {
     DecodeParams p = p_in;
-    const size_t smem = decode_smem_bytes(MT, p.kbs);
-    const void* fn = MT == 1 ? (const void*)decode_kernel<1> : (const void*)decode_kernel<2>;
+    const int64_t rgs = ceil_div(p.N, kRowsPerCta);
+    const int64_t mchunks = ceil_div(p.M, 8 * MT);
+    size_t smem = decode_smem_bytes(MT, ring);
+    // A grid smaller than a full wave is spread over the SMs: the block
+    // scheduler would otherwise stack CTAs (clusters) on some SMs while others
+    // idle.  Asking for more shared memory caps the CTAs an SM accepts at the
+    // even share.
+    const int64_t ctas = rgs * p.splits * mchunks;
+    const int64_t even = ceil_div(ctas, (int64_t)sm_count());
+    if (even < decode_ctas_per_sm(MT, ring)) {
+        const size_t cap_smem = (size_t)(228 * 1024) / (size_t)even - 1024 - 128;
+        const size_t max_smem = 227 * 1024;
+        smem = std::max(smem, std::min(cap_smem, max_smem));
+    }
+    const void* fn = MT == 1 ? (ring == kRingDeep ? (const void*)decode_kernel<1, kRingDeep>
+                                                  : (const void*)decode_kernel<1, kRingShallow>)
+                             : (ring == kRingDeep ? (const void*)decode_kernel<2, kRingDeep>
+                                                  : (const void*)decode_kernel<2, kRingShallow>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
     if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return check_cuda(e, "decode GEMM: cluster size attribute");
     }
-    const int64_t rgs = ceil_div(p.N, kRowsPerCta);
-    const int64_t mchunks = ceil_div(p.M, 8 * MT);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rgs, (unsigned)p.splits, (unsigned)mchunks);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -301,8 +356,10 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, cudaStream_t stream
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (MT == 1) e = cudaLaunchKernelEx(&cfg, decode_kernel<1>, p);
-    else e = cudaLaunchKernelEx(&cfg, decode_kernel<2>, p);
+    if (MT == 1) e = ring == kRingDeep ? cudaLaunchKernelEx(&cfg, decode_kernel<1, kRingDeep>, p)
+                                       : cudaLaunchKernelEx(&cfg, decode_kernel<1, kRingShallow>, p);
+    else e = ring == kRingDeep ? cudaLaunchKernelEx(&cfg, decode_kernel<2, kRingDeep>, p)
+                               : cudaLaunchKernelEx(&cfg, decode_kernel<2, kRingShallow>, p);
     return check_cuda(e, "decode GEMM: launch");
 }
 

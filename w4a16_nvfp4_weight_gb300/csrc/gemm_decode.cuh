@@ -16,12 +16,20 @@ struct DecodeParams {
     int* status;              // device status word
 };
 
-// Dynamic shared memory of one CTA for MT token tiles of 8 and kbs blocks.
-size_t decode_smem_bytes(int MT, int kbs);
+// Shared-memory ring shapes: the deep ring streams long K slices; the
+// shallow one lets more CTAs share an SM when each CTA's slice is short, so
+// that one CTA's pipeline fill and reduction overlap another's work.
+enum DecodeRing { kRingDeep = 0, kRingShallow = 1 };
+
+// Dynamic shared memory of one CTA for MT token tiles of 8 and the given ring.
+size_t decode_smem_bytes(int MT, int ring);
+
+// CTAs of the decode kernel that fit on one SM at once (shared memory bound).
+int decode_ctas_per_sm(int MT, int ring);
 
 // MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
 // covered by a third grid dimension.
-nvfp4_status launch_decode(const DecodeParams& p, int MT, cudaStream_t stream);
+nvfp4_status launch_decode(const DecodeParams& p, int MT, int ring, cudaStream_t stream);
 
 // Xs = RN_bf16(X * pqs) for an M x K activation (K a multiple of 16).
 nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* Xs, int64_t M, int64_t K,
