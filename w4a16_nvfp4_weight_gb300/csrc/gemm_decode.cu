@@ -43,7 +43,7 @@ namespace {
 constexpr int kWarps = 8;                      // consumer warps: 8 x 16 = 128 weight rows
 constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
 constexpr int kRowsPerCta = kWarps * kAtomRows;
-constexpr uint32_t kBlockBytes = kWarps * kAtomBytes;          // 4608: 128 rows x 64 k, contiguous
+constexpr uint32_t kBlockBytes = kStreamBlockBytes;            // 4608: 128 rows x 64 k, contiguous
 
 // Ring shape per number of 8-token MMA tiles (MT) and ring kind: stages x
 // 64-k blocks per stage.  Larger stages amortise the per-stage barrier work;
@@ -57,16 +57,8 @@ template <> struct Ring<2, kRingDeep> { static constexpr int kStages = 2, kBlock
 template <> struct Ring<1, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
 template <> struct Ring<2, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
 
-template <int MT, int R> struct RingGeom {
-    static constexpr int kTok = 8 * MT;
-    static constexpr int kStages = Ring<MT, R>::kStages;
-    static constexpr int kBlocksPerStage = Ring<MT, R>::kBlocksPerStage;
-    static constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
-    static constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;   // activation row stride (+16 B)
-    static constexpr size_t kXStageBytes = (size_t)kTok * kXRowElems * 2;
-    static constexpr size_t kStageBytes = kWeightStageBytes + kXStageBytes;
-    static_assert(kStageBytes % 16 == 0 && (kXRowElems * 2) % 16 == 0, "bulk copies need 16-byte alignment");
-};
+template <int MT, int R>
+using RingGeom = StreamRing<MT, Ring<MT, R>::kStages, Ring<MT, R>::kBlocksPerStage>;
 
 struct Smem {
     // offsets in bytes from the dynamic shared memory base

@@ -46,11 +46,10 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 16;
 
 // ------------------------------------------------------------------- route --
-__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int topk,
-                             int32_t* __restrict__ idx, float* __restrict__ wts) {
-    const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    if (t >= T) return;
-    const int lane = threadIdx.x & 31;
+// One warp routes token t: top-k of its E logits (ties to the lower expert
+// index), softmax over the selected k.
+__device__ void route_token(const float* __restrict__ logits, int64_t t, int E, int topk,
+                            int32_t* __restrict__ idx, float* __restrict__ wts, int lane) {
     float l[kMaxExperts / 32];
     uint32_t used = 0;
     #pragma unroll
@@ -94,6 +93,17 @@ __global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E,
     }
 }
 
+// Every kernel of the layer is launched with programmatic dependent launch:
+// it lets the next kernel be scheduled early and waits for its predecessor
+// (griddepcontrol.wait) before touching global memory that one may write.
+__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int topk,
+                             int32_t* __restrict__ idx, float* __restrict__ wts) {
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (t < T) route_token(logits, t, E, topk, idx, wts, threadIdx.x & 31);
+}
+
 // ----------------------------------------------------------------- permute --
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
@@ -103,11 +113,9 @@ constexpr int kPermWarps = kPermThreads / 32;
 // __match_any_sync); a scan over experts and warps gives every (warp, expert)
 // its first position; pass 2 walks the same slots again and places them.
 // Slots of one expert therefore keep their flat order t*k+j: stable.
-__global__ void __launch_bounds__(kPermThreads)
-permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
-               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-               int4* __restrict__ items, int32_t* __restrict__ n_items) {
-    extern __shared__ int perm_smem[];
+__device__ void permute_block(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
+                              int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                              int4* __restrict__ items, int32_t* __restrict__ n_items, int* perm_smem) {
     int* wcnt = perm_smem;                                  // [kPermWarps][E], then positions
     int* cnt = perm_smem + kPermWarps * E;                  // [E]
     int* item_base = cnt + E;                               // [E]
@@ -137,18 +145,36 @@ permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
         cnt[e] = run;
     }
     __syncthreads();
-    if (tid == 0) {
-        int run = 0, items_run = 0;
-        for (int e = 0; e < E; ++e) {
+    if (w == 0) {
+        // exclusive scans over experts of the row counts and the work items:
+        // lane l takes the consecutive experts [l * per, (l + 1) * per)
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int rows = 0, its = 0;
+        for (int e = e0; e < e1; ++e) {
+            rows += cnt[e];
+            its += (cnt[e] + tok - 1) / tok;
+        }
+        int rows_incl = rows, its_incl = its;
+        #pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
+            const int m = __shfl_up_sync(0xffffffffu, its_incl, off);
+            if (lane >= off) { rows_incl += r; its_incl += m; }
+        }
+        int run = rows_incl - rows, items_run = its_incl - its;
+        for (int e = e0; e < e1; ++e) {
+            const int c = cnt[e];
             offsets[e] = run;
             item_base[e] = items_run;
-            const int c = cnt[e];
             cnt[e] = run;                                    // now the expert's offset
             run += c;
             items_run += (c + tok - 1) / tok;
         }
-        offsets[E] = run;
-        *n_items = items_run;
+        if (lane == 31) {
+            offsets[E] = rows_incl;
+            *n_items = its_incl;
+        }
     }
     __syncthreads();
     for (int e = tid; e < E; e += kPermThreads) {
@@ -172,20 +198,46 @@ permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
     }
 }
 
+__global__ void __launch_bounds__(kPermThreads)
+permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
+               int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+               int4* __restrict__ items, int32_t* __restrict__ n_items) {
+    extern __shared__ int perm_smem[];
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    permute_block(idx, n, E, tok, offsets, perm, inv, items, n_items, perm_smem);
+}
+
+// Few tokens: one CTA routes every token (a warp per token) and then permutes,
+// saving a launch.  The block barrier orders the routing writes before the
+// permutation reads them.
+constexpr int64_t kFusedRouteMaxT = 64;
+
+__global__ void __launch_bounds__(kPermThreads)
+route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int topk, int tok,
+                     int32_t* __restrict__ idx, float* __restrict__ wts,
+                     int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                     int4* __restrict__ items, int32_t* __restrict__ n_items) {
+    extern __shared__ int perm_smem[];
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    for (int64_t t = threadIdx.x / 32; t < T; t += kPermWarps)
+        route_token(logits, t, E, topk, idx, wts, threadIdx.x & 31);
+    __syncthreads();
+    permute_block(idx, T * topk, E, tok, offsets, perm, inv, items, n_items, perm_smem);
+}
+
 size_t permute_smem_bytes(int E) { return ((size_t)kPermWarps * E + 2 * E) * sizeof(int); }
 
 // ------------------------------------------------- grouped streaming linear --
 constexpr int kWarps = 8;                      // 8 x 16 = 128 weight rows per CTA
 constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
-constexpr int kStages = 3;
-constexpr int kBlocksPerStage = 3;
-constexpr uint32_t kBlockBytes = kWarps * kAtomBytes;          // 4608 per 64-k block
-constexpr uint32_t kWeightStageBytes = kBlocksPerStage * kBlockBytes;
-constexpr int kXRowElems = kBlocksPerStage * kBlockK + 8;
+constexpr uint32_t kBlockBytes = kStreamBlockBytes;            // 4608 per 64-k block
 
-__host__ __device__ constexpr size_t moe_stage_bytes(int tok) {
-    return kWeightStageBytes + (size_t)tok * kXRowElems * 2;
-}
+// Ring per number of 8-row MMA tiles, as for the dense decode kernel.
+template <int MT> struct MoeRing;
+template <> struct MoeRing<1> { using G = StreamRing<1, 3, 4>; };
+template <> struct MoeRing<2> { using G = StreamRing<2, 2, 4>; };
 constexpr size_t kRingOffset = 128;
 
 struct MoeLinParams {
@@ -211,8 +263,13 @@ template <int MT, bool GATED>
 __global__ void __launch_bounds__(kThreads)
 moe_linear_kernel(const MoeLinParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int TOK = 8 * MT;
-    constexpr size_t kStageBytes = moe_stage_bytes(TOK);
+    using G = typename MoeRing<MT>::G;
+    constexpr int TOK = G::kTok;
+    constexpr int kStages = G::kStages;
+    constexpr int kBlocksPerStage = G::kBlocksPerStage;
+    constexpr uint32_t kWeightStageBytes = G::kWeightStageBytes;
+    constexpr int kXRowElems = G::kXRowElems;
+    constexpr size_t kStageBytes = G::kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStages;
     uint64_t* lut_bar = empty + kStages;
@@ -226,6 +283,8 @@ moe_linear_kernel(const MoeLinParams p) {
     const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
     const int split = blockIdx.y;
     const int item_id = blockIdx.z;
+    pdl_launch_dependents();
+    pdl_wait_previous();                       // items and activations come from earlier kernels
     if (item_id >= *p.n_items) return;         // the same for every CTA of the cluster
     const int4 item = p.items[item_id];
     const int e = item.x, r0 = item.y, nrows = item.z;
@@ -319,21 +378,24 @@ moe_linear_kernel(const MoeLinParams p) {
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
         const bool rows_valid = GATED || row_a + warp * kAtomRows < p.N;
+        const uint8_t* const a0 = ring + warp * kAtomBytes;
+        const uint16_t* const x0 = reinterpret_cast<const uint16_t*>(ring + kWeightStageBytes) +
+                                   g * kXRowElems + q * 16;
+        int s = 0;
+        uint32_t phase = 0;
         for (int i = 0; i < nst && ok; ++i) {
-            const int s = i % kStages;
-            if (!mbar_wait(&full[s], (i / kStages) & 1, p.status)) break;
-            const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
-            const uint8_t* st = ring + s * kStageBytes;
+            if (!mbar_wait(&full[s], phase, p.status)) break;
+            const uint8_t* a = a0 + s * kStageBytes;
             uint4 codes[kBlocksPerStage];
             uint32_t sc[kBlocksPerStage];
             #pragma unroll
             for (int b = 0; b < kBlocksPerStage; ++b) {
-                const uint8_t* a = st + b * kBlockBytes + warp * kAtomBytes;
-                codes[b] = *reinterpret_cast<const uint4*>(a + 16 * lane);
-                sc[b] = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
+                codes[b] = *reinterpret_cast<const uint4*>(a + b * kBlockBytes + 16 * lane);
+                sc[b] = *reinterpret_cast<const uint16_t*>(a + b * kBlockBytes + kAtomCodeBytes + 2 * lane);
             }
             if (rows_valid) {
-                const uint16_t* xr = reinterpret_cast<const uint16_t*>(st + kWeightStageBytes) + g * kXRowElems + q * 16;
+                const uint16_t* xr = x0 + s * (kStageBytes / 2);
+                const int nb = nkb - i * kBlocksPerStage;
                 #pragma unroll
                 for (int b = 0; b < kBlocksPerStage; ++b)
                     if (b < nb) atom_mma<MT, kXRowElems>(codes[b], sc[b], lut, xr + b * kBlockK, acc);
@@ -341,6 +403,7 @@ moe_linear_kernel(const MoeLinParams p) {
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (++s == kStages) { s = 0; phase ^= 1u; }
         }
         // push partials to the reducing CTA
         const int c = lane & 3;
@@ -412,6 +475,8 @@ moe_linear_kernel(const MoeLinParams p) {
 // ----------------------------------------------------------------- combine --
 __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk, int64_t H,
                                uint16_t* __restrict__ out) {
+    pdl_wait_previous();
+    pdl_launch_dependents();
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (i >= T * H) return;
     const int64_t t = i / H, n = i % H;
@@ -430,6 +495,8 @@ __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
                                    const int32_t* __restrict__ perm, int topk, int64_t n, int64_t H,
                                    uint16_t* __restrict__ Xp) {
+    pdl_wait_previous();
+    pdl_launch_dependents();
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= n * H) return;
     const int64_t r = i / H, k = i % H;
@@ -450,10 +517,29 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_
     *reinterpret_cast<uint4*>(Xp + i) = v;
 }
 
+// Launch with programmatic dependent launch enabled (see route_kernel).
+template <typename... Params, typename... Args>
+nvfp4_status launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            const char* what, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return check_cuda(cudaLaunchKernelEx(&cfg, kernel, args...), what);
+}
+
 size_t moe_lin_smem(int MT, bool gated) {
     const int tok = 8 * MT;
     const size_t part = gated ? ((size_t)tok * 64 + 8) * 2 : (size_t)tok * 128 + 8;
-    return kRingOffset + kLutBytes + kStages * moe_stage_bytes(tok) + part * 4;
+    const size_t ring = MT == 1 ? MoeRing<1>::G::kStages * MoeRing<1>::G::kStageBytes
+                                : MoeRing<2>::G::kStages * MoeRing<2>::G::kStageBytes;
+    return kRingOffset + kLutBytes + ring + part * 4;
 }
 
 template <int MT, bool GATED>
@@ -467,13 +553,15 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)p.splits;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED>, p);
     return check_cuda(e, GATED ? "MoE FC1: launch" : "MoE FC2: launch");
 }
@@ -578,22 +666,34 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
         if (st != NVFP4_OK) return st;
         xin = (const uint16_t*)(ws + L.xs);
     }
-    route_kernel<<<(unsigned)ceil_div(T, 8), 256, 0, s>>>(router_logits, T, E, topk, idx, wts);
-    if ((st = check_cuda(cudaGetLastError(), "MoE route: launch")) != NVFP4_OK) return st;
     {
         const size_t psmem = permute_smem_bytes(E);
-        cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
-        if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
-        permute_kernel<<<1, kPermThreads, psmem, s>>>(idx, n, E, L.tok, offsets, perm, inv, items, n_items);
+        if (T <= kFusedRouteMaxT) {
+            cudaError_t ce = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)psmem);
+            if ((st = check_cuda(ce, "MoE route+permute: shared memory attribute")) != NVFP4_OK) return st;
+            st = launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE route+permute: launch",
+                                router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items);
+            if (st != NVFP4_OK) return st;
+        } else {
+            st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
+                                router_logits, T, E, topk, idx, wts);
+            if (st != NVFP4_OK) return st;
+            cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+            if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
+            st = launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
+                                (const int32_t*)idx, n, E, L.tok, offsets, perm, inv, items, n_items);
+            if (st != NVFP4_OK) return st;
+        }
     }
-    if ((st = check_cuda(cudaGetLastError(), "MoE permute: launch")) != NVFP4_OK) return st;
 
     if (L.tile) {
         // gather the routed rows into expert-contiguous order, then two tile GEMMs
         uint16_t* xp = (uint16_t*)(ws + L.xp);
-        gather_rows_kernel<<<(unsigned)ceil_div(n * H / 8, 256), 256, 0, s>>>(
-            (const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, perm, topk, n, H, xp);
-        if ((st = check_cuda(cudaGetLastError(), "MoE gather: launch")) != NVFP4_OK) return st;
+        st = launch_chained(gather_rows_kernel, dim3((unsigned)ceil_div(n * H / 8, 256)), dim3(256), 0, s,
+                            "MoE gather: launch", (const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale,
+                            (const int32_t*)perm, topk, n, H, xp);
+        if (st != NVFP4_OK) return st;
         TcMoeParams t1{};
         t1.fc1 = true; t1.subm = L.subm; t1.X = xp; t1.x_rows = n;
         t1.w = (const uint8_t*)fc1; t1.w_stride = nvfp4_repack_size(2 * I, H);
@@ -632,8 +732,8 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
         if (st != NVFP4_OK) return st;
     }
 
-    combine_kernel<<<(unsigned)ceil_div(T * H / 4, 256), 256, 0, s>>>(yp, T, topk, H, (uint16_t*)out);
-    return check_cuda(cudaGetLastError(), "MoE combine: launch");
+    return launch_chained(combine_kernel, dim3((unsigned)ceil_div(T * H / 4, 256)), dim3(256), 0, s,
+                          "MoE combine: launch", (const float*)yp, T, topk, H, (uint16_t*)out);
 }
 
 // ------------------------------------------------- allocation-free variant --

@@ -7,6 +7,23 @@
 
 namespace nvfp4 {
 
+// Shared-memory ring of the streaming kernels: kStages stages, each holding
+// kBlocksPerStage 64-k blocks of 128 weight rows (4608 contiguous bytes each)
+// followed by the activation chunk of 8*MT token rows (row stride padded by
+// 16 bytes so that the rows fall on different banks).
+constexpr uint32_t kStreamBlockBytes = 8 * kAtomBytes;
+
+template <int MT, int S, int B> struct StreamRing {
+    static constexpr int kTok = 8 * MT;
+    static constexpr int kStages = S;
+    static constexpr int kBlocksPerStage = B;
+    static constexpr uint32_t kWeightStageBytes = B * kStreamBlockBytes;
+    static constexpr int kXRowElems = B * kBlockK + 8;
+    static constexpr size_t kXStageBytes = (size_t)kTok * kXRowElems * 2;
+    static constexpr size_t kStageBytes = kWeightStageBytes + kXStageBytes;
+    static_assert(kStageBytes % 16 == 0 && (kXRowElems * 2) % 16 == 0, "bulk copies need 16-byte alignment");
+};
+
 __device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
