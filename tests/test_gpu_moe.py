@@ -58,9 +58,9 @@ def _small_case(T, E, topk, H, I, seed, awq=False):
     return synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=awq)
 
 
-# (64,16,4,256,128), (300,8,2,256,256), (100,4,3,384,128) and (1024,4,2,128,128) route
-# >= 16 rows per expert and take the tensor-core tile path (128- and 256-row items);
-# the others take the streaming path.
+# (300,8,2,256,256), (100,4,3,384,128) and (1024,4,2,128,128) route >= 32 rows per
+# expert and take the tensor-core tile path (128- and 256-row items); the others take
+# the streaming path ((64,16,4,256,128): 16 rows per expert, some experts in two items).
 @pytest.mark.parametrize("T,E,topk,H,I", [(3, 4, 2, 64, 64), (64, 16, 4, 256, 128), (37, 8, 3, 192, 320),
                                           (5, 1, 1, 128, 64), (200, 32, 8, 128, 64), (300, 8, 2, 256, 256),
                                           (100, 4, 3, 384, 128), (1024, 4, 2, 128, 128)])

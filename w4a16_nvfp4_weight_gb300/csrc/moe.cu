@@ -577,9 +577,12 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq)
     MoeLayout L{};
     const int64_t n = T * topk;
     const int64_t per_expert = n / std::max(E, 1);   // routed rows per expert on average
-    // Many rows per expert: tcgen05 tiles of 128 (or 256) routed rows; few rows:
-    // the streaming kernel with 8 or 16 rows per work item.
-    L.tile = per_expert >= 16 && I % 128 == 0;
+    // Many rows per expert: tcgen05 tiles of 128 (or 256) routed rows; fewer:
+    // the streaming kernel with 8 or 16 rows per work item.  At 16 to 31 rows
+    // per expert the streaming kernel, which expands weights on far more warps
+    // than the tile kernel has, measured faster despite reading an expert
+    // twice when its rows need two items.
+    L.tile = per_expert >= 32 && I % 128 == 0;
     L.subm = per_expert >= 192 ? 2 : 1;
     L.mt = per_expert > 8 ? 2 : 1;
     L.tok = L.tile ? 128 * L.subm : 8 * L.mt;
