@@ -315,21 +315,22 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStrea
     size_t smem = decode_smem_bytes(MT, ring);
     // A grid smaller than a full wave is spread over the SMs: the block
     // scheduler would otherwise stack CTAs (clusters) on some SMs while others
-    // idle.  Asking for more shared memory caps the CTAs an SM accepts at the
-    // even share.
+    // idle.  A smaller shared-memory carve-out caps the CTAs an SM accepts at
+    // the even share.  (Asking for more dynamic shared memory per CTA did the
+    // same, but such launches failed under the profiler.)
     const int64_t ctas = rgs * p.splits * mchunks;
     const int64_t even = ceil_div(ctas, (int64_t)sm_count());
-    if (even < decode_ctas_per_sm(MT, ring)) {
-        const size_t cap_smem = (size_t)(228 * 1024) / (size_t)even - 1024 - 128;
-        const size_t max_smem = 227 * 1024;
-        smem = std::max(smem, std::min(cap_smem, max_smem));
-    }
+    int carve = 100;
+    if (even < decode_ctas_per_sm(MT, ring))
+        carve = (int)ceil_div((int64_t)even * (int64_t)(smem + 1024) * 100, (int64_t)(228 * 1024));
     const void* fn = MT == 1 ? (ring == kRingDeep ? (const void*)decode_kernel<1, kRingDeep>
                                                   : (const void*)decode_kernel<1, kRingShallow>)
                              : (ring == kRingDeep ? (const void*)decode_kernel<2, kRingDeep>
                                                   : (const void*)decode_kernel<2, kRingShallow>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+    if (e != cudaSuccess) return check_cuda(e, "decode GEMM: carveout attribute");
     if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return check_cuda(e, "decode GEMM: cluster size attribute");
