@@ -315,22 +315,23 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStrea
     size_t smem = decode_smem_bytes(MT, ring);
     // A grid smaller than a full wave is spread over the SMs: the block
     // scheduler would otherwise stack CTAs (clusters) on some SMs while others
-    // idle.  A smaller shared-memory carve-out caps the CTAs an SM accepts at
-    // the even share.  (Asking for more dynamic shared memory per CTA did the
-    // same, but such launches failed under the profiler.)
+    // idle.  Asking for more dynamic shared memory than the ring needs caps the
+    // CTAs an SM accepts at the even share.  The request stays 8 KB under the
+    // cap: at the exact cap the launches failed under the profiler.  (A smaller
+    // shared-memory carve-out spreads as well, but switching the carve-out
+    // between consecutive kernels cost more than the spreading gained.)
     const int64_t ctas = rgs * p.splits * mchunks;
     const int64_t even = ceil_div(ctas, (int64_t)sm_count());
-    int carve = 100;
-    if (even < decode_ctas_per_sm(MT, ring))
-        carve = (int)ceil_div((int64_t)even * (int64_t)(smem + 1024) * 100, (int64_t)(228 * 1024));
+    if (even < decode_ctas_per_sm(MT, ring)) {
+        const size_t cap_smem = (size_t)(228 * 1024) / (size_t)even - 1024 - 8192;
+        smem = std::max(smem, cap_smem);
+    }
     const void* fn = MT == 1 ? (ring == kRingDeep ? (const void*)decode_kernel<1, kRingDeep>
                                                   : (const void*)decode_kernel<1, kRingShallow>)
                              : (ring == kRingDeep ? (const void*)decode_kernel<2, kRingDeep>
                                                   : (const void*)decode_kernel<2, kRingShallow>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
-    if (e != cudaSuccess) return check_cuda(e, "decode GEMM: carveout attribute");
     if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return check_cuda(e, "decode GEMM: cluster size attribute");
