@@ -19,6 +19,12 @@ out:
 3. Y[m, n] = sum_k x'[m, k] * W[n, k] in float64 (every product of two BF16
    values is exact in float64); the reported output is RN_bf16(Y).
 
+W4A16 covers FP16 activations as well as BF16 ("[TRTLLM-12720][feat] Support
+nvfp4 w4a16 on sm120", Summary: "BF16/FP16 activations").  With ``act="f16"``
+every BF16 rounding above is an FP16 rounding instead: the weight is
+dequantized to the activation type (W = RN_f16 of the same exact product, so
+one rounding still), x' = RN_f16(x * s), and the output is RN_f16(Y).
+
 Packed layout of the inputs (the checkpoint form): ``packed`` uint8 [N, K/2],
 row-major, the LOW nibble holding the even k; ``scales`` uint8 float8_e4m3fn
 codes [N, K/16], row-major.  K must be a multiple of 16 (the group size).
@@ -31,7 +37,7 @@ case, dequant(quant(x)) idempotence, AWQ identity and dropped-scale controls).
 
 import numpy as np
 
-from .formats import bf16_bits, bf16_to_float, e2m1_value, e4m3_value, global_multiplier
+from .formats import act_bits, act_nan_bits, act_to_float, e2m1_value, e4m3_value, global_multiplier
 
 GROUP = 16
 
@@ -56,11 +62,11 @@ def dequant_values(packed, scales, g, K):
         return e2m1_value(codes) * s_per_k * g64
 
 
-def dequant(packed, scales, global_scale, global_is_divisor, K):
-    """BF16 bit patterns (uint16 [N, K]) of the dequantized weight."""
+def dequant(packed, scales, global_scale, global_is_divisor, K, act="bf16"):
+    """Bit patterns (uint16 [N, K]) of the weight dequantized to ``act``."""
     g = global_multiplier(global_scale, global_is_divisor)
     v = dequant_values(packed, scales, g, K)
-    bits = bf16_bits(v)
+    bits = act_bits(v, act)
     # A NaN weight (only from a NaN scale code) carries the sign of the product
     # of the code's and the scale's signs, like the finite weights do.
     nan = np.isnan(v)
@@ -68,26 +74,28 @@ def dequant(packed, scales, global_scale, global_is_divisor, K):
         codes = unpack_codes(packed, K)
         sc = np.repeat(np.asarray(scales, dtype=np.uint8).astype(np.int64), GROUP, axis=1)
         sgn = ((codes >> 3) ^ (sc >> 7) ^ int(np.signbit(g))) & 1
-        bits = np.where(nan, (0x7FC0 | (sgn << 15)).astype(np.uint16), bits)
+        bits = np.where(nan, (act_nan_bits(act) | (sgn << 15)).astype(np.uint16), bits)
     return bits
 
 
-def awq_scale_activation(x_bits, pqs_bits):
-    """x' = RN_bf16(x * pre_quant_scale), broadcast over rows (uint16 in/out)."""
-    x = bf16_to_float(x_bits)
-    s = bf16_to_float(np.asarray(pqs_bits).reshape(1, -1))
-    return bf16_bits(x * s)
+def awq_scale_activation(x_bits, pqs_bits, act="bf16"):
+    """x' = RN(x * pre_quant_scale) in the activation type, broadcast over rows
+    (uint16 in/out)."""
+    x = act_to_float(x_bits, act)
+    s = act_to_float(np.asarray(pqs_bits).reshape(1, -1), act)
+    return act_bits(x * s, act)
 
 
-def gemm(x_bits, w_bits):
-    """Y = X . W^T in float64 from BF16 operands X [M, K], W [N, K]."""
-    x = bf16_to_float(x_bits)
-    w = bf16_to_float(w_bits)
+def gemm(x_bits, w_bits, act="bf16"):
+    """Y = X . W^T in float64 from 16-bit operands X [M, K], W [N, K]."""
+    x = act_to_float(x_bits, act)
+    w = act_to_float(w_bits, act)
     return x @ w.T
 
 
-def linear(x_bits, packed, scales, global_scale, global_is_divisor, pqs_bits=None, rows=None):
-    """Full W4A16 linear.  Returns (Y_float64 [M, N'], Y_bf16_bits [M, N']).
+def linear(x_bits, packed, scales, global_scale, global_is_divisor, pqs_bits=None, rows=None, act="bf16"):
+    """Full W4A16 linear.  Returns (Y_float64 [M, N'], Y_bits [M, N']) with the
+    output rounded to the activation type ``act`` ("bf16" or "f16").
 
     ``rows`` optionally restricts the output to a subset of the N output
     features (the oracle then dequantizes only those weight rows), for
@@ -99,7 +107,7 @@ def linear(x_bits, packed, scales, global_scale, global_is_divisor, pqs_bits=Non
     if rows is not None:
         p = p[rows]
         s = s[rows]
-    w = dequant(p, s, global_scale, global_is_divisor, K)
-    x = x_bits if pqs_bits is None else awq_scale_activation(x_bits, pqs_bits)
-    y = gemm(x, w)
-    return y, bf16_bits(y)
+    w = dequant(p, s, global_scale, global_is_divisor, K, act)
+    x = x_bits if pqs_bits is None else awq_scale_activation(x_bits, pqs_bits, act)
+    y = gemm(x, w, act)
+    return y, act_bits(y, act)

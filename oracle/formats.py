@@ -10,11 +10,13 @@
 * the FP32 per-tensor global scale, which compressed-tensors checkpoints store
   as a divisor (1/scale) and which must be inverted before use (SGLang PR
   40022, "Note the global-scale inversion").
-* BF16 round-to-nearest-even of an exact float64 value.
+* BF16 round-to-nearest-even of an exact float64 value, and the same for
+  FP16 (IEEE binary16), the other 16-bit activation type of W4A16 ("BF16/FP16
+  activations": "[TRTLLM-12720][feat] Support nvfp4 w4a16 on sm120", Summary).
 
 Parity: pinned by tests/test_oracle_formats.py (hand-listed codebook row,
 closed-form E2M1 from its exponent/mantissa fields, all 256 E4M3 codes against
-torch.float8_e4m3fn, BF16 rounding against torch's float32->bfloat16 cast and
+torch.float8_e4m3fn, BF16 and FP16 rounding against torch's float32 casts and
 against exact rational rounding).
 """
 
@@ -107,3 +109,63 @@ def bf16_to_float(bits):
     """Exact float64 value of BF16 bit patterns (uint16)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+_F16_MIN_NORMAL = 2.0 ** -14
+
+
+def f16_bits(values):
+    """Round exact float64 values to FP16 (IEEE binary16; nearest, ties to even).
+
+    Returns the 16-bit patterns as uint16.  FP16 has 11 significant bits,
+    exponent bias 15 and subnormals down to 2**-24; values whose rounded
+    magnitude reaches 2**16 become infinity (the largest finite value is
+    65504).  NaN becomes the quiet pattern 0x7E00 with the value's sign bit;
+    -0.0 keeps its sign.  One rounding of the float64 value, done as for BF16:
+    scale so that one unit in the last FP16 place is 1.0, rint, scale back.
+    """
+    v = np.asarray(values, dtype=np.float64)
+    sign = np.signbit(v).astype(np.uint32) << 15
+    a = np.abs(v)
+    finite = np.isfinite(a)
+    a_f = np.where(finite, a, 0.0)
+    _, e = np.frexp(a_f)                       # a = m * 2**e, m in [0.5, 1)
+    quantum_exp = np.where(a_f >= _F16_MIN_NORMAL, e - 11, -24)
+    r = np.rint(np.ldexp(a_f, -quantum_exp))  # integer significand, RNE
+    rounded = np.ldexp(r, quantum_exp)        # exact float64, FP16-representable
+    overflow = rounded >= 2.0 ** 16
+    h = np.where(overflow, 0.0, rounded).astype(np.float16)   # exact: representable
+    bits = h.view(np.uint16).astype(np.uint32)
+    bits = np.where(overflow | np.isinf(a), 0x7C00, bits)
+    bits = np.where(np.isnan(a), 0x7E00, bits)
+    return (bits | sign).astype(np.uint16)
+
+
+def f16_to_float(bits):
+    """Exact float64 value of FP16 bit patterns (uint16)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+ACTIVATION_TYPES = ("bf16", "f16")
+
+
+def act_bits(values, act):
+    """Round to the activation type: ``act`` is "bf16" or "f16"."""
+    if act == "bf16":
+        return bf16_bits(values)
+    if act == "f16":
+        return f16_bits(values)
+    raise ValueError(f"unknown activation type {act!r}")
+
+
+def act_to_float(bits, act):
+    if act == "bf16":
+        return bf16_to_float(bits)
+    if act == "f16":
+        return f16_to_float(bits)
+    raise ValueError(f"unknown activation type {act!r}")
+
+
+def act_nan_bits(act):
+    """The quiet-NaN pattern (sign bit clear) the rounding functions produce."""
+    return 0x7FC0 if act == "bf16" else 0x7E00

@@ -25,6 +25,10 @@ Readings taken where the pages are silent:
   perm = the flat routing slots t*k + j sorted stably by expert (so by
   expert, then token, then slot), inv[perm[i]] = i.
 
+With FP16 activations (``act="f16"``; W4A16 covers them: "[TRTLLM-12720]
+[feat] Support nvfp4 w4a16 on sm120", Summary) the expert weights, h and the
+output are rounded to FP16 instead of BF16.
+
 Parity: pinned by tests/test_oracle_moe.py (hand-built logits with a known
 top-k and ties, sum(p) == 1, permutation invariants, E=1/top-1 reduction to the
 dense oracle, and a pure-Python loop implementation on a tiny layer).
@@ -33,7 +37,7 @@ dense oracle, and a pure-Python loop implementation on a tiny layer).
 import numpy as np
 
 from .dense import awq_scale_activation, dequant
-from .formats import bf16_bits, bf16_to_float
+from .formats import act_bits, act_to_float
 
 
 def route(logits, topk):
@@ -74,19 +78,20 @@ def silu(v):
     return v / (1.0 + np.exp(-v))
 
 
-def expert_weights(fc, K):
-    """Dequantized BF16 weight values (float64) of one expert matrix.
+def expert_weights(fc, K, act="bf16"):
+    """Dequantized weight values (float64) of one expert matrix, rounded to the
+    activation type.
 
     ``fc`` = (packed, scales, global_scale, global_is_divisor).
     """
     packed, scales, gs, is_div = fc
-    return bf16_to_float(dequant(packed, scales, gs, is_div, K))
+    return act_to_float(dequant(packed, scales, gs, is_div, K, act), act)
 
 
-def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None):
+def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="bf16"):
     """The whole layer.
 
-    x_bits  uint16 [T, H] BF16 activations
+    x_bits  uint16 [T, H] activations (BF16, or FP16 with act="f16")
     logits  float32 [T, E] router logits
     fc1     list of E tuples (packed [2I, H/2], scales [2I, H/16], global, is_divisor)
     fc2     list of E tuples (packed [H, I/2], scales [H, I/16], global, is_divisor)
@@ -113,25 +118,25 @@ def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None):
         return res
     xs = x_bits[tokens]
     if pqs_bits is not None:
-        xs = awq_scale_activation(xs, pqs_bits)
-    x = bf16_to_float(xs)
+        xs = awq_scale_activation(xs, pqs_bits, act)
+    x = act_to_float(xs, act)
     I = np.asarray(fc1[0][0]).shape[0] // 2
     y = np.zeros((tokens.size, topk, H))
     h_all = np.zeros((tokens.size, topk, I), dtype=np.uint16)
     sel = idx[tokens]                                   # [T', topk]
     for e in np.unique(sel):
         rows, slots = np.nonzero(sel == e)
-        w1 = expert_weights(fc1[e], H)                  # [2I, H]
-        w2 = expert_weights(fc2[e], I)                  # [H, I]
+        w1 = expert_weights(fc1[e], H, act)             # [2I, H]
+        w2 = expert_weights(fc2[e], I, act)             # [H, I]
         gu = x[rows] @ w1.T                             # [r, 2I]
         gate, up = gu[:, :I], gu[:, I:]
-        h = bf16_bits(silu(gate) * up)                  # [r, I]
+        h = act_bits(silu(gate) * up, act)              # [r, I]
         h_all[rows, slots] = h
-        y[rows, slots] = bf16_to_float(h) @ w2.T        # [r, H]
+        y[rows, slots] = act_to_float(h, act) @ w2.T    # [r, H]
     out = np.zeros((tokens.size, H))
     for j in range(topk):                                # slot order
         out = out + p[tokens, j][:, None] * y[:, j]
     res["out"] = out
-    res["out_bits"] = bf16_bits(out)
+    res["out_bits"] = act_bits(out, act)
     res["h_bits"] = h_all
     return res

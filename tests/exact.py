@@ -88,3 +88,40 @@ def bf16_exact(bits):
     else:
         mag = (1 + Fraction(f, 128)) * Fraction(2) ** (e - 127)
     return -mag if s else mag
+
+
+def f16_round_exact(v, negative_zero=False):
+    """Round a Fraction to FP16 (IEEE binary16, nearest, ties to even); returns
+    the 16-bit pattern.  1 sign bit, 5 exponent bits (bias 15), 10 fraction bits."""
+    if v == 0:
+        return 0x8000 if negative_zero else 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = max(_floor_log2(a), -14)
+    quantum = Fraction(2) ** (e - 10)
+    q = a / quantum
+    m = q.numerator // q.denominator
+    rem = q - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and (m & 1)):
+        m += 1
+    if m == 2048:
+        m = 1024
+        e += 1
+    if m < 1024:                                  # subnormal (only when e == -14)
+        return sign | m
+    exp_field = e + 15
+    if exp_field >= 31:
+        return sign | 0x7C00
+    return sign | (exp_field << 10) | (m - 1024)
+
+
+def f16_exact(bits):
+    """Exact value of a finite FP16 pattern."""
+    s = (bits >> 15) & 1
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    if e == 0:
+        mag = Fraction(f, 1024) * Fraction(2) ** -14
+    else:
+        mag = (1 + Fraction(f, 1024)) * Fraction(2) ** (e - 15)
+    return -mag if s else mag

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 from oracle import dense, formats
-from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f32_exact
+from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f16_exact, f16_round_exact, f32_exact
 from w4a16_nvfp4_weight_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -41,11 +41,12 @@ def _pack(codes):
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
 
 
-def _exact_dequant(code, scale_code, g):
+def _exact_dequant(code, scale_code, g, act="bf16"):
     s = e4m3_exact(scale_code)
     v = e2m1_exact(code) * s * f32_exact(g)
     neg_zero = v == 0 and (((code >> 3) ^ (scale_code >> 7)) & 1) == 1
-    return bf16_round_exact(v, negative_zero=neg_zero)
+    rnd = bf16_round_exact if act == "bf16" else f16_round_exact
+    return rnd(v, negative_zero=neg_zero)
 
 
 def test_worked_row_with_unit_scales():
@@ -204,3 +205,59 @@ def test_linear_row_sampling_matches_full():
     rows = np.array([0, 5, 95, 17])
     ys, ysb = dense.linear(c.x_bits, c.packed, c.scales, c.divisor, True, rows=rows)
     assert np.array_equal(ys, y[:, rows]) and np.array_equal(ysb, yb[:, rows])
+
+
+# ------------------------------------------------- FP16 activations ---
+@pytest.mark.parametrize("divisor", [448.0, 3.0, 24366.764, 0.37, 1.0e-3, 1.0e6])
+def test_dequant_f16_exact_over_all_codes_and_scales(divisor):
+    """FP16 dequant of every (code, scale) pair against exact rational rounding,
+    including products that overflow FP16 (1e-3) or fall in its subnormals (1e6)."""
+    codes = np.tile(np.arange(16, dtype=np.uint8), (256, 1))
+    scales = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    w = dense.dequant(_pack(codes), scales, divisor, True, 16, act="f16")
+    g = formats.global_multiplier(divisor, True)
+    for s in range(256):
+        for c in range(16):
+            got = int(w[s, c])
+            if e4m3_exact(s) is None:
+                assert got & 0x7FFF == 0x7E00
+                assert (got >> 15) == (((c >> 3) ^ (s >> 7)) & 1)
+            else:
+                assert got == _exact_dequant(c, s, g, "f16"), (hex(s), c)
+
+
+def test_f16_dequant_is_not_the_bf16_one():
+    """Control: the two activation types give different weights for a generic global."""
+    codes = np.tile(np.arange(16, dtype=np.uint8), (64, 1))
+    scales = np.arange(0x20, 0x60, dtype=np.uint8).reshape(64, 1)
+    wb = formats.bf16_to_float(dense.dequant(_pack(codes), scales, 24366.764, True, 16))
+    wh = formats.f16_to_float(dense.dequant(_pack(codes), scales, 24366.764, True, 16, act="f16"))
+    assert not np.array_equal(wb, wh)
+
+
+def test_gemm_f16_brute_force_4x16x16():
+    c = synth.uniform_codes_case(M=4, K=16, N=16, seed=98)
+    x = synth.normal_act(synth.rng(5), (4, 16), "f16")
+    y, yb = dense.linear(x, c.packed, c.scales, c.divisor, True, act="f16")
+    g = formats.global_multiplier(c.divisor, True)
+    codes = dense.unpack_codes(c.packed, 16)
+    for m in range(4):
+        for n in range(16):
+            acc = Fraction(0)
+            for k in range(16):
+                wb = _exact_dequant(int(codes[n, k]), int(c.scales[n, k // 16]), g, "f16")
+                acc += f16_exact(int(x[m, k])) * f16_exact(wb)
+            assert abs(Fraction(float(y[m, n])) - acc) <= abs(acc) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 140)
+            assert int(yb[m, n]) == f16_round_exact(acc)
+
+
+def test_awq_f16_single_rounding_and_dropped_scale_control():
+    c = synth.gaussian_case(8, 256, 64, seed=33, awq=True, act="f16")
+    xs = dense.awq_scale_activation(c.x_bits[:2, :32], c.pqs_bits[:32], act="f16")
+    for m in range(2):
+        for k in range(32):
+            want = f16_round_exact(f16_exact(int(c.x_bits[m, k])) * f16_exact(int(c.pqs_bits[k])))
+            assert int(xs[m, k]) == want
+    y0, _ = dense.linear(c.x_bits, c.packed, c.scales, c.divisor, True, act="f16")
+    ya, _ = dense.linear(c.x_bits, c.packed, c.scales, c.divisor, True, pqs_bits=c.pqs_bits, act="f16")
+    assert np.linalg.norm(y0 - ya) / np.linalg.norm(ya) > 0.2

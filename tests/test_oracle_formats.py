@@ -16,7 +16,7 @@ import pytest
 import torch
 
 from oracle import formats
-from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact
+from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f16_exact, f16_round_exact
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -166,3 +166,69 @@ def test_plant_wrong_tie_rule_is_caught(monkeypatch):
     monkeypatch.setattr(formats, "bf16_bits", bad)
     with pytest.raises(AssertionError):
         test_bf16_rounding_is_single_rounding()
+
+
+# ---------------------------------------------------------------- FP16 ---
+def test_f16_rounding_matches_torch_on_float32():
+    r = np.random.default_rng(17)
+    n = 200000
+    mant = r.integers(0, 2 ** 23, size=n)
+    exps = r.integers(-30, 18, size=n)            # subnormal range, normal range, overflow
+    sgn = np.where(r.integers(0, 2, size=n) == 1, -1.0, 1.0)
+    f = (sgn * np.ldexp(1.0 + mant / 2.0 ** 23, exps)).astype(np.float32)
+    edges = np.array([65504.0, 65519.99, 65520.0, 65536.0, 2.0 ** -24, 2.0 ** -25, 1.5 * 2.0 ** -25,
+                      2.0 ** -14 - 2.0 ** -26, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -0.0, 0.0,
+                      3.0e38, -65520.0], dtype=np.float32)
+    f = np.concatenate([f, edges])
+    ours = formats.f16_bits(f.astype(np.float64))
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_f16_rounding_is_single_rounding():
+    # 1 + 2^-11 + 2^-40 lies above the FP16 tie between 1 and 1 + 2^-10; rounding it to
+    # float32 first lands exactly on the tie, which then goes to the even neighbour 1.0.
+    v = 1.0 + 2.0 ** -11 + 2.0 ** -40
+    assert int(formats.f16_bits(v)) == 0x3C01
+    assert int(formats.f16_bits(np.float32(v))) == 0x3C00       # the double-rounded result
+    for x in (1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -(1.0 + 2.0 ** -11) - 2.0 ** -45,
+              2.0 ** -20 * 1.5, 2.0 ** -24 / 2, 2.0 ** -24 * 0.75, 65504.0, 65519.999, 65520.0,
+              -0.0, 0.0, 2.0 ** -14 * (1 - 2.0 ** -12)):
+        want = f16_round_exact(Fraction(x), negative_zero=math.copysign(1, x) < 0)
+        assert int(formats.f16_bits(x)) == want, (x, hex(want))
+
+
+def test_f16_rounding_against_exact_rationals_random():
+    r = np.random.default_rng(13)
+    mant = r.integers(1, 2 ** 52, size=3000)
+    exps = r.integers(-30, 18, size=3000)
+    vals = np.ldexp(1.0 + mant / 2.0 ** 52, exps)
+    ours = formats.f16_bits(vals)
+    for v, b in zip(vals, ours):
+        assert int(b) == f16_round_exact(Fraction(float(v)))
+
+
+def test_f16_specials_and_roundtrip():
+    assert int(formats.f16_bits(np.nan)) & 0x7FFF == 0x7E00
+    assert int(formats.f16_bits(-np.inf)) == 0xFC00
+    assert int(formats.f16_bits(np.inf)) == 0x7C00
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = formats.f16_to_float(allbits)
+    finite = np.isfinite(vals)
+    assert np.array_equal(formats.f16_bits(vals[finite]), allbits[finite])
+    for b in (0x0001, 0x03FF, 0x0400, 0x3C00, 0x7BFF, 0x8400, 0xC0C0):
+        assert Fraction(float(formats.f16_to_float(np.uint16(b)))) == f16_exact(b)
+
+
+def test_plant_f16_wrong_tie_rule_is_caught(monkeypatch):
+    """Ties away from zero instead of to even must fail the FP16 rounding pins."""
+    def bad(values):
+        v = np.asarray(values, dtype=np.float64)
+        a = np.abs(v)
+        _, e = np.frexp(a)
+        q = np.where(a >= 2.0 ** -14, e - 11, -24)
+        r = np.floor(np.ldexp(a, -q) + 0.5)
+        return (np.ldexp(r, q) * np.sign(v)).astype(np.float16).view(np.uint16)
+    monkeypatch.setattr(formats, "f16_bits", bad)
+    with pytest.raises(AssertionError):
+        test_f16_rounding_is_single_rounding()

@@ -14,7 +14,7 @@ import pytest
 from scipy.special import expit
 
 from oracle import dense, formats, moe
-from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f32_exact
+from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f16_exact, f16_round_exact, f32_exact
 from w4a16_nvfp4_weight_gb300 import synth
 
 
@@ -70,16 +70,20 @@ def test_silu_against_logistic():
     assert moe.silu(0.0) == 0.0
 
 
-def _tiny_layer(T=3, E=4, topk=2, H=32, I=16, seed=5, awq=False):
+def _tiny_layer(T=3, E=4, topk=2, H=32, I=16, seed=5, awq=False, act="bf16"):
     r = synth.rng(seed)
     fc1, fc2 = [], []
     for _ in range(E):
         fc1.append(synth.quantize(synth.normal_weight(r, 2 * I, H)))
         fc2.append(synth.quantize(synth.normal_weight(r, H, I)))
-    return synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=awq)
+    return synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=awq, act=act)
 
 
-def _loop_dequant(packed, scales, divisor, K):
+_ROUND = {"bf16": bf16_round_exact, "f16": f16_round_exact}
+_VALUE = {"bf16": bf16_exact, "f16": f16_exact}
+
+
+def _loop_dequant(packed, scales, divisor, K, act="bf16"):
     g = f32_exact(np.float32(1.0) / np.float32(divisor))
     N = packed.shape[0]
     out = []
@@ -89,18 +93,19 @@ def _loop_dequant(packed, scales, divisor, K):
             byte = int(packed[n, k // 2])
             code = (byte & 0xF) if k % 2 == 0 else (byte >> 4)
             v = e2m1_exact(code) * e4m3_exact(int(scales[n, k // 16])) * g
-            row.append(float(bf16_exact(bf16_round_exact(v))))
+            row.append(float(_VALUE[act](_ROUND[act](v))))
         out.append(row)
     return out
 
 
-def test_tiny_layer_against_python_loops():
-    c = _tiny_layer()
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_tiny_layer_against_python_loops(act):
+    c = _tiny_layer(act=act)
     res = moe.moe_layer(c.x_bits, c.logits, [(p, s, d, True) for p, s, d in c.fc1],
-                        [(p, s, d, True) for p, s, d in c.fc2], c.topk)
+                        [(p, s, d, True) for p, s, d in c.fc2], c.topk, act=act)
     T, E, k, H, I = c.T, c.E, c.topk, c.H, c.I
-    w1 = [_loop_dequant(p, s, d, H) for p, s, d in c.fc1]
-    w2 = [_loop_dequant(p, s, d, I) for p, s, d in c.fc2]
+    w1 = [_loop_dequant(p, s, d, H, act) for p, s, d in c.fc1]
+    w2 = [_loop_dequant(p, s, d, I, act) for p, s, d in c.fc2]
     for t in range(T):
         logits = [float(v) for v in c.logits[t]]
         order = sorted(range(E), key=lambda e: (-logits[e], e))[:k]
@@ -108,12 +113,12 @@ def test_tiny_layer_against_python_loops():
         z = sum(math.exp(logits[e] - logits[order[0]]) for e in order)
         pw = [math.exp(logits[e] - logits[order[0]]) / z for e in order]
         assert np.allclose(res["p"][t], pw, rtol=1e-14)
-        x = [float(bf16_exact(int(b))) for b in c.x_bits[t]]
+        x = [float(_VALUE[act](int(b))) for b in c.x_bits[t]]
         acc = [0.0] * H
         for j, e in enumerate(order):
             gate = [math.fsum(x[i] * w1[e][n][i] for i in range(H)) for n in range(I)]
             up = [math.fsum(x[i] * w1[e][I + n][i] for i in range(H)) for n in range(I)]
-            h = [float(bf16_exact(int(formats.bf16_bits(gate[n] / (1 + math.exp(-gate[n])) * up[n]))))
+            h = [float(_VALUE[act](int(formats.act_bits(gate[n] / (1 + math.exp(-gate[n])) * up[n], act))))
                  for n in range(I)]
             for o in range(H):
                 y = math.fsum(h[n] * w2[e][o][n] for n in range(I))
@@ -121,34 +126,39 @@ def test_tiny_layer_against_python_loops():
         ref = np.array(acc)
         got = res["out"][t]
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
-        assert np.array_equal(res["out_bits"][t], formats.bf16_bits(ref))
+        assert np.array_equal(res["out_bits"][t], formats.act_bits(ref, act))
 
 
-def test_single_expert_top1_reduces_to_dense():
-    c = _tiny_layer(T=5, E=1, topk=1, H=64, I=32, seed=9)
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_single_expert_top1_reduces_to_dense(act):
+    _single_expert_check(act)
+
+
+def _single_expert_check(act):
+    c = _tiny_layer(T=5, E=1, topk=1, H=64, I=32, seed=9, act=act)
     fc1 = [(p, s, d, True) for p, s, d in c.fc1]
     fc2 = [(p, s, d, True) for p, s, d in c.fc2]
-    res = moe.moe_layer(c.x_bits, c.logits, fc1, fc2, 1)
+    res = moe.moe_layer(c.x_bits, c.logits, fc1, fc2, 1, act=act)
     assert np.all(res["p"] == 1.0)
-    gu, _ = dense.linear(c.x_bits, *fc1[0])
-    h = formats.bf16_bits(moe.silu(gu[:, :32]) * gu[:, 32:])
-    y, yb = dense.linear(h, *fc2[0])
+    gu, _ = dense.linear(c.x_bits, *fc1[0], act=act)
+    h = formats.act_bits(moe.silu(gu[:, :32]) * gu[:, 32:], act)
+    y, yb = dense.linear(h, *fc2[0], act=act)
     assert np.array_equal(res["out"], y) and np.array_equal(res["out_bits"], yb)
 
 
 def test_planted_gate_up_swap_is_caught(monkeypatch):
     orig = moe.moe_layer
 
-    def swapped(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None):
+    def swapped(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="bf16"):
         flipped = []
         for p, s, g, d in fc1:
             half = p.shape[0] // 2
             flipped.append((np.concatenate([p[half:], p[:half]]),
                             np.concatenate([s[half:], s[:half]]), g, d))
-        return orig(x_bits, logits, flipped, fc2, topk, pqs_bits, tokens)
+        return orig(x_bits, logits, flipped, fc2, topk, pqs_bits, tokens, act)
     monkeypatch.setattr(moe, "moe_layer", swapped)
     with pytest.raises(AssertionError):
-        test_single_expert_top1_reduces_to_dense()
+        _single_expert_check("bf16")
 
 
 def test_token_subset_and_awq():

@@ -1,7 +1,7 @@
 """Seeded synthetic inputs shaped like the dense, LM-head and MoE workloads.
 
-This module only *makes inputs*: random numbers, the BF16 cast of activations
-(torch's float32->bfloat16 cast) and the weight quantizer that turns an
+This module only *makes inputs*: random numbers, the BF16 or FP16 cast of
+activations (torch's float32->bfloat16 / float16 casts) and the weight quantizer that turns an
 FP32 matrix into NVFP4 checkpoint tensors (packed E2M1 codes, E4M3 group
 scales, an FP32 global divisor).  It contains no decoding, dequantization,
 GEMM or routing arithmetic; both the CUDA library's tests and the CPU oracle
@@ -43,11 +43,26 @@ def bf16_bits_of(x_f32):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def f16_bits_of(x_f32):
+    """FP16 bit patterns (uint16) of float32 values, via torch's RNE cast."""
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def act_bits_of(x_f32, act):
+    """16-bit activation patterns: act = "bf16" or "f16"."""
+    return bf16_bits_of(x_f32) if act == "bf16" else f16_bits_of(x_f32)
+
+
 def normal_bf16(r, shape, std=1.0):
+    return normal_act(r, shape, "bf16", std)
+
+
+def normal_act(r, shape, act, std=1.0):
     x = r.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x = x * np.float32(std)
-    return bf16_bits_of(x)
+    return act_bits_of(x, act)
 
 
 def _e4m3_codes(v_f32):
@@ -129,19 +144,20 @@ def uniform_codes_case(M=4, K=256, N=256, seed=None):
     return DenseCase(M, K, N, x, packed, scales, np.float32(448.0))
 
 
-def awq_scale_bits(r, K):
-    """Per-channel AWQ pre-quant scale, log-uniform in [1/e, e], as BF16."""
-    return bf16_bits_of(np.exp(r.uniform(-1.0, 1.0, size=K)).astype(np.float32))
+def awq_scale_bits(r, K, act="bf16"):
+    """Per-channel AWQ pre-quant scale, log-uniform in [1/e, e], as BF16 (or FP16)."""
+    return act_bits_of(np.exp(r.uniform(-1.0, 1.0, size=K)).astype(np.float32), act)
 
 
-def gaussian_case(M, K, N, seed, awq=False):
-    """A linear whose weight is quantized from N(0, 0.02); X ~ N(0, 1)."""
+def gaussian_case(M, K, N, seed, awq=False, act="bf16"):
+    """A linear whose weight is quantized from N(0, 0.02); X ~ N(0, 1) in the
+    activation type ``act`` ("bf16" or "f16")."""
     r = rng(seed)
     w = normal_weight(r, N, K)
     packed, scales, d = quantize(w)
     del w
-    x = normal_bf16(r, (M, K))
-    pqs = awq_scale_bits(r, K) if awq else None
+    x = normal_act(r, (M, K), act)
+    pqs = awq_scale_bits(r, K, act) if awq else None
     return DenseCase(M, K, N, x, packed, scales, d, pqs)
 
 
@@ -171,11 +187,12 @@ def moe_weights(E, H, I, seed):
     return fc1, fc2
 
 
-def moe_case(T, seed, E=128, topk=8, H=2048, I=768, weights=None, awq=False):
-    """MoE layer inputs: logits ~ N(0,1) FP32, X ~ N(0,1) BF16, experts from N(0,0.02)."""
+def moe_case(T, seed, E=128, topk=8, H=2048, I=768, weights=None, awq=False, act="bf16"):
+    """MoE layer inputs: logits ~ N(0,1) FP32, X ~ N(0,1) BF16 (or FP16), experts
+    from N(0,0.02)."""
     fc1, fc2 = weights if weights is not None else moe_weights(E, H, I, seed + 500)
     r = rng(seed)
     logits = r.standard_normal(size=(T, E), dtype=np.float32)
-    x = normal_bf16(r, (T, H))
-    pqs = awq_scale_bits(r, H) if awq else None
+    x = normal_act(r, (T, H), act)
+    pqs = awq_scale_bits(r, H, act) if awq else None
     return MoECase(T, E, topk, H, I, x, logits, fc1, fc2, pqs)
