@@ -9,7 +9,10 @@ algorithmic bytes moved per second (weights at 0.5625 B/element plus BF16
 activations in and out), with TFLOP/s beside it.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
-                    [--workload decode|prefill|lmhead|moe|tails]
+                    [--workload decode|prefill|lmhead|moe|tails] [--dtype bf16|f16]
+
+--dtype f16 runs the same workload with FP16 activations (FP16 weights operand
+and output) through the *_f16 entry points.
 
 Under torchrun each rank runs its own replica (the path has no data exchange);
 rank 0 prints one JSON line with the max-over-ranks time.
@@ -151,8 +154,16 @@ def traffic_ratio(kind):
 
 
 # ------------------------------------------------------------------ inputs --
+# Activation type of the run (--dtype): "bf16" (default) or "f16".
+ACT = "bf16"
+
+
+def act_torch():
+    return torch.bfloat16 if ACT == "bf16" else torch.float16
+
+
 def bits_tensor(bits, device):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(act_torch()).to(device)
 
 
 def build_decode_workload(nv, synth, device):
@@ -169,9 +180,9 @@ def build_decode_workload(nv, synth, device):
         for (K, N) in DECODE_SHAPES:
             w0 = base[(K, N)][0]
             w = nv.NVFP4Weight(w0.buf.clone(), N, K)       # a copy per GEMM: no L2 reuse in a step
-            x_bits = synth.normal_bf16(r, (M, K))
+            x_bits = synth.normal_act(r, (M, K), ACT)
             launches.append(dict(M=M, K=K, N=N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits,
-                                 pqs=None, y=torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+                                 pqs=None, y=torch.empty((M, N), dtype=act_torch(), device=device)))
     return launches, base
 
 
@@ -185,12 +196,12 @@ def build_dense_workload(nv, synth, device, shapes, wl_index, awq=False):
                           float(d), N, K)
             base[(K, N)] = (w, packed, scales, d)
         w = base[(K, N)][0]
-        x_bits = synth.normal_bf16(r, (M, K))
-        pqs_bits = synth.awq_scale_bits(r, K) if awq else None
+        x_bits = synth.normal_act(r, (M, K), ACT)
+        pqs_bits = synth.awq_scale_bits(r, K, ACT) if awq else None
         launches.append(dict(M=M, K=K, N=N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits,
                              pqs_bits=pqs_bits,
                              pqs=bits_tensor(pqs_bits, device) if awq else None,
-                             y=torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+                             y=torch.empty((M, N), dtype=act_torch(), device=device)))
     return launches, base
 
 
@@ -295,7 +306,7 @@ def run_ours(args, rank, world, device):
         "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": ACT,
         "data": "synthetic (seeded; NVFP4 weights quantized from N(0,0.02), X~N(0,1))",
         "config": dict(config, parallelism=f"replicas{world}" if world > 1 else "single GPU",
                        l2="inputs larger than L2: each GEMM of a step reads its own weight copy "
@@ -346,7 +357,7 @@ def run_moe(args, rank, world, device, nv, synth):
         x = bits_tensor(c.x_bits, device)
         lg = torch.from_numpy(np.ascontiguousarray(c.logits)).to(device)
         ws = torch.empty(nv.moe_workspace_size(T, MOE_E, MOE_TOPK, MOE_H, MOE_I), dtype=torch.uint8, device=device)
-        out = torch.empty((T, MOE_H), dtype=torch.bfloat16, device=device)
+        out = torch.empty((T, MOE_H), dtype=act_torch(), device=device)
         offs = torch.empty(MOE_E + 1, dtype=torch.int32, device=device)
         calls.append(dict(T=T, x=x, lg=lg, ws=ws, out=out, offs=offs))
 
@@ -354,7 +365,8 @@ def run_moe(args, rank, world, device, nv, synth):
         # routing tables come back through offsets_out so the bench can count active experts
         h = nv._lib.load()
         w1, w2 = wcopies[w % len(wcopies)]
-        nv._lib.check(h.nvfp4_w4a16_moe_grouped(
+        fn = h.nvfp4_w4a16_moe_grouped_f16 if ACT == "f16" else h.nvfp4_w4a16_moe_grouped
+        nv._lib.check(fn(
             nv._ptr(C["x"]), nv._ptr(C["lg"]), nv._ptr(w1), nv._ptr(w2), None, C["T"], MOE_E, MOE_TOPK,
             MOE_H, MOE_I, nv._ptr(C["out"]), None, None, None, nv._ptr(C["offs"]), nv._ptr(C["ws"]),
             C["ws"].numel(), nv._stream()))
@@ -418,7 +430,7 @@ def run_moe(args, rank, world, device, nv, synth):
         "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded)",
+        "dtype": ACT, "data": "synthetic (seeded)",
         "config": {"workload": "MoE layer E=128 top-8 H=2048 I=768 at T{1,16,256,4096}",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: the 128 experts hold 340 MB of weights, and four copies of "
@@ -477,7 +489,7 @@ def run_e2e(nv, launches, stream, args, bw_unit):
     """Same step through the public API with pinned host activations in and
     host outputs back, copies inside the timed region."""
     hx = [L["x"].cpu().pin_memory() for L in launches]
-    hy = [torch.empty(L["y"].shape, dtype=torch.bfloat16).pin_memory() for L in launches]
+    hy = [torch.empty(L["y"].shape, dtype=act_torch()).pin_memory() for L in launches]
     dx = [torch.empty_like(L["x"]) for L in launches]
     steps = max(3, min(args.steps, 200))
 
@@ -526,13 +538,13 @@ def cpu_baseline(seconds_target=15.0, reps=None, base=None, rows_per_gemm=256):
         rows = np.sort(r.choice(N, size=rows_per_gemm, replace=False))
         sub_p, sub_s = packed[rows], scales[rows]
         for M in DECODE_M:
-            cases.append((M, K, sub_p, sub_s, d, synth.normal_bf16(r, (M, K))))
+            cases.append((M, K, sub_p, sub_s, d, synth.normal_act(r, (M, K), ACT)))
     t0 = time.perf_counter()
     n_sweeps = 0
     b = 0
     while True:
         for (M, K, p, s, d, x) in cases:
-            dense.linear(x, p, s, d, True)
+            dense.linear(x, p, s, d, True, act=ACT)
             b += algo_bytes(M, rows_per_gemm, K)
         n_sweeps += 1
         el = time.perf_counter() - t0
@@ -581,8 +593,8 @@ def profile_case(args):
     packed, scales, d = synth.weight_only(K, N, synth.seed_for(9, 0))
     w = nv.repack(torch.from_numpy(packed).cuda(), torch.from_numpy(scales).cuda(), float(d), N, K)
     r = synth.rng(7)
-    x = bits_tensor(synth.normal_bf16(r, (M, K)), "cuda")
-    pqs = bits_tensor(synth.awq_scale_bits(r, K), "cuda") if args.awq else None
+    x = bits_tensor(synth.normal_act(r, (M, K), ACT), "cuda")
+    pqs = bits_tensor(synth.awq_scale_bits(r, K, ACT), "cuda") if args.awq else None
     for _ in range(6):
         y = nv.gemm(x, w, pre_quant_scale=pqs)
     torch.cuda.synchronize()
@@ -612,10 +624,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails", "moe"])
     ap.add_argument("--awq", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="activation type: BF16 (default) or FP16 activations, weights and output")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, metavar="M,K,N",
                     help="run one GEMM shape 3 times after 3 warm-ups (for ncu captures); no timing")
     args = ap.parse_args()
+    global ACT
+    ACT = args.dtype
     if args.profile:
         profile_case(args)
         return

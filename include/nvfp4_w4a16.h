@@ -3,11 +3,13 @@
  *
  * The method: weights are NVFP4 -- 4-bit E2M1 codes (sign bit + magnitudes
  * {0, 0.5, 1, 1.5, 2, 3, 4, 6}), one float8_e4m3fn scale per 16 consecutive K
- * elements, one FP32 global scale per tensor -- and activations stay BF16; the
- * activation is never quantized.  Every forward step computes
- *     W[n,k] = RN_bf16( e2m1(code[n,k]) * e4m3(scale[n,k/16]) * g )
- *     Y[m,n] = RN_bf16( sum_k x'[m,k] * W[n,k] )       (FP32 accumulation)
- * with x' = x, or x' = RN_bf16(x * pre_quant_scale) for AWQ checkpoints.
+ * elements, one FP32 global scale per tensor -- and activations stay 16-bit
+ * (BF16, or FP16 through the *_f16 entry points); the activation is never
+ * quantized.  Every forward step computes, with RN the round-to-nearest-even
+ * conversion to the activation type,
+ *     W[n,k] = RN( e2m1(code[n,k]) * e4m3(scale[n,k/16]) * g )
+ *     Y[m,n] = RN( sum_k x'[m,k] * W[n,k] )            (FP32 accumulation)
+ * with x' = x, or x' = RN(x * pre_quant_scale) for AWQ checkpoints.
  * Sources: "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper"
  * (TensorRT-LLM PR 14775), Description and Changes table (on-the-fly NVFP4
  * dequant: E2M1 codebook lookup, per-block FP8 scale, per-tensor scale;
@@ -16,15 +18,17 @@
  * stored as a divisor that must be inverted); "[None][fix] Apply the NVFP4_AWQ
  * pre-quant scale in MegaMoE CuteDSL" (TensorRT-LLM PR 20823), Description
  * (x * pre_quant_scale in BF16 before the GEMM, shape [1, hidden]; a zero-token
- * chunk launches no kernel; an already-quantized activation is refused).
+ * chunk launches no kernel; an already-quantized activation is refused);
+ * "[TRTLLM-12720][feat] Support nvfp4 w4a16 on sm120" (TensorRT-LLM PR 16511),
+ * Summary (W4A16 = FP4 weights with BF16 or FP16 activations).
  *
  * Conventions for every entry point
  *  - All tensor pointers are DEVICE pointers on the current CUDA device unless
  *    stated otherwise; all calls are asynchronous on `stream` (a cudaStream_t;
  *    NULL = the legacy default stream).  The library never allocates, frees or
  *    synchronizes (except nvfp4_device_status, which synchronizes `stream`).
- *  - The caller owns every buffer.  BF16 tensors are passed as raw 16-bit
- *    patterns (uint16_t / void*), row-major, densely packed.
+ *  - The caller owns every buffer.  BF16 and FP16 tensors are passed as raw
+ *    16-bit patterns (uint16_t / void*), row-major, densely packed.
  *  - Arguments are validated before anything is launched; a failed check
  *    returns a non-OK status, launches nothing and sets a message readable
  *    with nvfp4_last_error() (thread-local).
@@ -99,10 +103,12 @@ size_t nvfp4_repack_size(int64_t N, int64_t K);
  *  [0, 256)      header: u32 magic 0x34504E56, u32 version, i64 N, i64 K,
  *                i64 Np (N rounded up to 256), i64 Kp (K rounded up to 64),
  *                f32 g, f32 global_scale, u32 global_is_divisor.
- *  [256, 4352)   magnitude table: 256 entries of 16 bytes, entry s = the BF16
- *                values RN_bf16(mag_j * e4m3(s) * g) of the 8 E2M1 magnitudes
- *                j = 0..7, stored as 8 low bytes then 8 high bytes.
- *  [4352, ...)   atoms of 16 rows x 64 k (576 bytes each), ordered by
+ *  [256, 4352)   BF16 magnitude table: 256 entries of 16 bytes, entry s = the
+ *                BF16 values RN_bf16(mag_j * e4m3(s) * g) of the 8 E2M1
+ *                magnitudes j = 0..7, stored as 8 low bytes then 8 high bytes.
+ *  [4352, 8448)  FP16 magnitude table: the same with RN_f16 (IEEE binary16;
+ *                products beyond 65504 round to infinity).
+ *  [8448, ...)   atoms of 16 rows x 64 k (576 bytes each), ordered by
  *                256-row tile, then 64-k block, then 16-row block.  In an atom,
  *                lane L = 4r + q (r < 8, q < 4) owns 16 code bytes at 16L
  *                (rows r and r+8 of the block, k group q, 8 bytes each) and 2
@@ -128,6 +134,10 @@ nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
  */
 nvfp4_status nvfp4_dequant(const void* repacked, int64_t N, int64_t K,
                            uint16_t* out_bf16, void* stream);
+
+/* The same with FP16 output: the operand of the *_f16 GEMM entry points. */
+nvfp4_status nvfp4_dequant_f16(const void* repacked, int64_t N, int64_t K,
+                               uint16_t* out_f16, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Dense W4A16 GEMM                                                          */
@@ -158,6 +168,16 @@ size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_q
 nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
                               int64_t M, int64_t N, int64_t K, void* Y,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FP16 activations: the same call with X, pre_quant_scale and Y in FP16, the
+ * weight dequantized to FP16 and every RN an FP16 rounding (results beyond
+ * 65504 in magnitude become infinities).  Same kernels, FP16 tensor-core
+ * MMAs, same workspace size.
+ */
+nvfp4_status nvfp4_w4a16_gemm_f16(const void* X, const void* repacked, const void* pre_quant_scale,
+                                  int64_t M, int64_t N, int64_t K, void* Y,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Grouped top-k MoE layer (FC1 gate/up + SwiGLU, FC2, weighted combine)     */
@@ -196,6 +216,18 @@ nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
                                      void* out, int32_t* topk_idx_out, float* topk_weight_out,
                                      int32_t* perm_out, int32_t* offsets_out,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FP16 activations: X, fc1_pre_quant_scale and out in FP16; the expert weights,
+ * h and out rounded to FP16.  Routing is unchanged (FP32 logits).
+ */
+nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* router_logits,
+                                         const void* fc1, const void* fc2,
+                                         const void* fc1_pre_quant_scale,
+                                         int64_t T, int E, int topk, int64_t H, int64_t I,
+                                         void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                         int32_t* perm_out, int32_t* offsets_out,
+                                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Allocation-free variant of nvfp4_w4a16_moe_grouped (no counterpart in the

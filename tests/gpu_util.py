@@ -15,8 +15,14 @@ MAX_ABS = 2e-2
 
 
 def bits_to_bf16_tensor(bits, device="cuda"):
+    return bits_to_tensor(bits, "bf16", device)
+
+
+def bits_to_tensor(bits, act, device="cuda"):
+    """16-bit patterns -> a CUDA tensor of the activation type ("bf16" or "f16")."""
     a = np.ascontiguousarray(bits, dtype=np.uint16)
-    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    dt = torch.bfloat16 if act == "bf16" else torch.float16
+    return torch.from_numpy(a.view(np.int16)).view(dt).to(device)
 
 
 def tensor_to_bits(t):
@@ -32,10 +38,10 @@ def repack_case(case, device="cuda"):
                      case.N, case.K, global_is_divisor=True)
 
 
-def compare(y_gpu_bits, y_ref_bits, what=""):
+def compare(y_gpu_bits, y_ref_bits, what="", act="bf16"):
     """Assert the parity bar; returns (rel_fro, max_abs_rel)."""
-    g = formats.bf16_to_float(y_gpu_bits)
-    r = formats.bf16_to_float(y_ref_bits)
+    g = formats.act_to_float(y_gpu_bits, act)
+    r = formats.act_to_float(y_ref_bits, act)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
     assert np.all(np.isfinite(r)), f"{what}: non-finite oracle output"
     denom = np.linalg.norm(r)
@@ -52,7 +58,7 @@ def check_device_status():
     assert st == 0, f"device status word {st}"
 
 
-def oracle_linear(case, rows=None, awq=True):
+def oracle_linear(case, rows=None, awq=True, act="bf16"):
     pqs = case.pqs_bits if awq else None
     return dense.linear(case.x_bits, case.packed, case.scales, case.divisor, True,
-                        pqs_bits=pqs, rows=rows)
+                        pqs_bits=pqs, rows=rows, act=act)

@@ -26,7 +26,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("nvfp4_repack", "nvfp4_dequant", "nvfp4_w4a16_gemm", "nvfp4_w4a16_moe_grouped",
-              "nvfp4_repack_size", "nvfp4_last_error", "nvfp4_device_status"):
+              "nvfp4_repack_size", "nvfp4_last_error", "nvfp4_device_status",
+              "nvfp4_dequant_f16", "nvfp4_w4a16_gemm_f16", "nvfp4_w4a16_moe_grouped_f16"):
         assert n in names
 
 
@@ -34,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in sorted(_declared_functions()):
         assert hasattr(lib, n), f"{n} declared but not exported"
     assert set(_lib.SIGNATURES) == _declared_functions()
-    assert lib.nvfp4_abi_version() == 1
+    assert lib.nvfp4_abi_version() == 2
 
 
 def test_repack_size():
@@ -42,10 +43,10 @@ def test_repack_size():
     assert lib.nvfp4_repack_size(0, 64) == 0
     assert lib.nvfp4_repack_size(4, 24) == 0                 # K % 16 != 0
     assert lib.nvfp4_repack_size(-1, 64) == 0
-    # one 256-row tile, one 64-k block: header + table + 16 atoms
-    assert lib.nvfp4_repack_size(1, 16) == 4352 + 16 * 576
-    assert lib.nvfp4_repack_size(256, 64) == 4352 + 16 * 576
-    assert lib.nvfp4_repack_size(257, 80) == 4352 + 2 * 2 * 16 * 576
+    # one 256-row tile, one 64-k block: header + two magnitude tables + 16 atoms
+    assert lib.nvfp4_repack_size(1, 16) == 8448 + 16 * 576
+    assert lib.nvfp4_repack_size(256, 64) == 8448 + 16 * 576
+    assert lib.nvfp4_repack_size(257, 80) == 8448 + 2 * 2 * 16 * 576
     assert lib.nvfp4_repack_size(1000, 2064) % 256 == 0
 
 

@@ -35,7 +35,7 @@ def _unrepack(buf, N, K):
     sign_pos = [7, 15, 23, 31, 3, 11, 19, 27]
     codes = np.zeros((Np, Kp), dtype=np.uint8)
     scales = np.zeros((Np, Kp // 16), dtype=np.uint8)
-    atoms = b[4352:4352 + (Np // 16) * KB * 576].reshape(Np // 256, KB, 16, 576)
+    atoms = b[8448:8448 + (Np // 16) * KB * 576].reshape(Np // 256, KB, 16, 576)
     for lane in range(32):
         r, q = lane // 4, lane % 4
         words = atoms[:, :, :, 16 * lane:16 * lane + 16].copy().view(np.uint32)  # [nt,KB,16,4]

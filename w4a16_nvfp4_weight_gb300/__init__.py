@@ -8,6 +8,11 @@ in the library's CUDA kernels; there is no Python or CPU fallback.
     w = repack(packed_u8, scales_u8, divisor, N, K, global_is_divisor=True)
     y = gemm(x_bf16, w)                       # [M, K] -> [M, N]
     y = gemm(x_bf16, w, pre_quant_scale=s)    # AWQ checkpoints
+    y = gemm(x_fp16, w)                       # FP16 activations: FP16 weights and output
+
+The activation dtype (torch.bfloat16 or torch.float16) selects the entry
+point (nvfp4_w4a16_gemm or nvfp4_w4a16_gemm_f16, and likewise for the MoE
+layer and the dequant).
 """
 
 import ctypes
@@ -28,6 +33,15 @@ def _stream():
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+_ACT_DTYPES = (torch.bfloat16, torch.float16)
+
+
+def _act_dtype(x, name):
+    if not isinstance(x, torch.Tensor) or x.dtype not in _ACT_DTYPES:
+        raise Nvfp4Error(1, f"{name} must be a torch.bfloat16 or torch.float16 CUDA tensor")
+    return x.dtype
 
 
 def _require_cuda(t, name, dtype=None):
@@ -72,12 +86,17 @@ def repack(packed, scales, global_scale, N, K, global_is_divisor=True, out=None)
     return NVFP4Weight(out, N, K)
 
 
-def dequant(w, out=None):
-    """BF16 [N, K] weight exactly as the GEMM kernels see it."""
+def dequant(w, out=None, dtype=torch.bfloat16):
+    """[N, K] weight exactly as the GEMM kernels see it, in ``dtype`` (the
+    activation type: torch.bfloat16 or torch.float16)."""
     h = _lib.load()
+    if dtype not in _ACT_DTYPES:
+        raise Nvfp4Error(1, "dtype must be torch.bfloat16 or torch.float16")
     if out is None:
-        out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.buf.device)
-    _lib.check(h.nvfp4_dequant(_ptr(w.buf), w.N, w.K, _ptr(out), _stream()))
+        out = torch.empty((w.N, w.K), dtype=dtype, device=w.buf.device)
+    _require_cuda(out, "out", dtype)
+    fn = h.nvfp4_dequant_f16 if dtype == torch.float16 else h.nvfp4_dequant
+    _lib.check(fn(_ptr(w.buf), w.N, w.K, _ptr(out), _stream()))
     return out
 
 
@@ -86,24 +105,28 @@ def gemm_workspace_size(M, N, K, has_pre_quant_scale=False):
 
 
 def gemm(x, w, pre_quant_scale=None, out=None, workspace=None):
-    """Y[M, N] = X'[M, K] . W^T (BF16), X' = X or RN_bf16(X * pre_quant_scale)."""
+    """Y[M, N] = X'[M, K] . W^T in the activation type of x (BF16 or FP16),
+    X' = X or RN(X * pre_quant_scale)."""
     h = _lib.load()
-    _require_cuda(x, "x", torch.bfloat16)
+    dt = _act_dtype(x, "x")
+    _require_cuda(x, "x", dt)
     if x.dim() != 2 or x.shape[1] != w.K:
         raise Nvfp4Error(2, f"x must be [M, {w.K}], got {tuple(x.shape)}")
     if pre_quant_scale is not None:
-        _require_cuda(pre_quant_scale, "pre_quant_scale", torch.bfloat16)
+        _require_cuda(pre_quant_scale, "pre_quant_scale", dt)
         if pre_quant_scale.numel() != w.K:
             raise Nvfp4Error(2, f"pre_quant_scale must have {w.K} elements")
     M = x.shape[0]
     if out is None:
-        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((M, w.N), dtype=dt, device=x.device)
+    _require_cuda(out, "out", dt)
     need = gemm_workspace_size(M, w.N, w.K, pre_quant_scale is not None)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    _lib.check(h.nvfp4_w4a16_gemm(_ptr(x), _ptr(w.buf), _ptr(pre_quant_scale), M, w.N, w.K,
-                                  _ptr(out), _ptr(workspace), ws_bytes, _stream()))
+    fn = h.nvfp4_w4a16_gemm_f16 if dt == torch.float16 else h.nvfp4_w4a16_gemm
+    _lib.check(fn(_ptr(x), _ptr(w.buf), _ptr(pre_quant_scale), M, w.N, w.K,
+                  _ptr(out), _ptr(workspace), ws_bytes, _stream()))
     return out
 
 
@@ -114,14 +137,19 @@ def moe_workspace_size(T, E, topk, H, I):
 def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, out=None,
                 return_routing=False, workspace=None):
     """Top-k MoE layer.  ``fc1``/``fc2``: uint8 device buffers holding E repacked
-    expert weights back to back ([2I, H] and [H, I] each)."""
+    expert weights back to back ([2I, H] and [H, I] each).  x is BF16 or FP16;
+    out and fc1_pre_quant_scale have its type."""
     h = _lib.load()
-    _require_cuda(x, "x", torch.bfloat16)
+    dt = _act_dtype(x, "x")
+    _require_cuda(x, "x", dt)
     _require_cuda(router_logits, "router_logits", torch.float32)
+    if fc1_pre_quant_scale is not None:
+        _require_cuda(fc1_pre_quant_scale, "fc1_pre_quant_scale", dt)
     T, H = x.shape
     E = router_logits.shape[1]
     if out is None:
-        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((T, H), dtype=dt, device=x.device)
+    _require_cuda(out, "out", dt)
     dev = x.device
     idx = wts = perm = offs = None
     if return_routing:
@@ -133,7 +161,8 @@ def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, o
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    _lib.check(h.nvfp4_w4a16_moe_grouped(
+    fn = h.nvfp4_w4a16_moe_grouped_f16 if dt == torch.float16 else h.nvfp4_w4a16_moe_grouped
+    _lib.check(fn(
         _ptr(x), _ptr(router_logits), _ptr(fc1), _ptr(fc2), _ptr(fc1_pre_quant_scale),
         T, E, topk, H, I, _ptr(out), _ptr(idx), _ptr(wts), _ptr(perm), _ptr(offs),
         _ptr(workspace), ws_bytes, _stream()))

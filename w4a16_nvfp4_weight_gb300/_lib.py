@@ -23,11 +23,15 @@ SIGNATURES = {
     "nvfp4_repack_size": (c_size, [c_i64, c_i64]),
     "nvfp4_repack": (c_int, [c_vp, c_vp, c_float, c_int, c_i64, c_i64, c_vp, c_size, c_vp]),
     "nvfp4_dequant": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
+    "nvfp4_dequant_f16": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
     "nvfp4_w4a16_gemm_workspace": (c_size, [c_i64, c_i64, c_i64, c_int]),
     "nvfp4_w4a16_gemm": (c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
+    "nvfp4_w4a16_gemm_f16": (c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_moe_workspace": (c_size, [c_i64, c_int, c_int, c_i64, c_i64]),
     "nvfp4_w4a16_moe_grouped": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
                                         c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "nvfp4_w4a16_moe_grouped_f16": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
+                                            c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_moe_noalloc_scratch_bytes": (c_size, []),
     "nvfp4_w4a16_moe_grouped_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
                                                 c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),

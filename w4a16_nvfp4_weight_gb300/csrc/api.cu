@@ -116,7 +116,7 @@ size_t awq_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256)
 
 using namespace nvfp4;
 
-extern "C" int nvfp4_abi_version(void) { return 1; }
+extern "C" int nvfp4_abi_version(void) { return 2; }
 
 extern "C" const char* nvfp4_last_error(void) { return g_msg; }
 
@@ -143,39 +143,41 @@ extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, in
     return has_pre_quant_scale ? awq_bytes(M, K) : 0;
 }
 
-extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
-                                         int64_t M, int64_t N, int64_t K, void* Y,
-                                         void* workspace, size_t workspace_bytes, void* stream) {
-    if (M < 0 || N < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_w4a16_gemm: negative size M=%lld N=%lld", (long long)M, (long long)N);
-    if (K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_gemm: K=%lld must be a positive multiple of 16", (long long)K);
+namespace {
+
+nvfp4_status gemm_impl(const void* X, const void* repacked, const void* pre_quant_scale, int64_t M, int64_t N,
+                       int64_t K, void* Y, void* workspace, size_t workspace_bytes, bool f16, void* stream) {
+    const char* fn = f16 ? "nvfp4_w4a16_gemm_f16" : "nvfp4_w4a16_gemm";
+    if (M < 0 || N < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
+    if (K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld must be a positive multiple of 16", fn, (long long)K);
     if (M == 0 || N == 0) return NVFP4_OK;          // nothing to compute, nothing launched
-    if (!X || !repacked || !Y) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_w4a16_gemm: null pointer (X=%p W=%p Y=%p)", X, repacked, Y);
-    if (!aligned(X, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: X must be 16-byte aligned");
-    if (!aligned(repacked, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: repacked weight must be 256-byte aligned");
-    if (!aligned(Y, 4)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: Y must be 4-byte aligned");
-    if (pre_quant_scale && !aligned(pre_quant_scale, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: pre_quant_scale must be 16-byte aligned");
+    if (!X || !repacked || !Y) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer (X=%p W=%p Y=%p)", fn, X, repacked, Y);
+    if (!aligned(X, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: X must be 16-byte aligned", fn);
+    if (!aligned(repacked, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: repacked weight must be 256-byte aligned", fn);
+    if (!aligned(Y, 4)) return fail(NVFP4_ERR_ALIGNMENT, "%s: Y must be 4-byte aligned", fn);
+    if (pre_quant_scale && !aligned(pre_quant_scale, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: pre_quant_scale must be 16-byte aligned", fn);
     const size_t need = nvfp4_w4a16_gemm_workspace(M, N, K, pre_quant_scale != nullptr);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr))
-        return fail(NVFP4_ERR_WORKSPACE, "nvfp4_w4a16_gemm: workspace %zu bytes, needs %zu", workspace_bytes, need);
-    if (need > 0 && !aligned(workspace, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_w4a16_gemm: workspace must be 256-byte aligned");
+        return fail(NVFP4_ERR_WORKSPACE, "%s: workspace %zu bytes, needs %zu", fn, workspace_bytes, need);
+    if (need > 0 && !aligned(workspace, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: workspace must be 256-byte aligned", fn);
     int* status = device_status_ptr();
-    if (!status) return fail(NVFP4_ERR_CUDA, "nvfp4_w4a16_gemm: no CUDA device");
+    if (!status) return fail(NVFP4_ERR_CUDA, "%s: no CUDA device", fn);
     cudaStream_t s = (cudaStream_t)stream;
     if (use_tc_path(M, N)) {
         TcParams tp{};
         tp.X = (const uint16_t*)X; tp.pqs = (const uint16_t*)pre_quant_scale;
         tp.rp = (const uint8_t*)repacked; tp.Y = (uint16_t*)Y;
-        tp.M = M; tp.N = N; tp.K = K; tp.status = status;
+        tp.M = M; tp.N = N; tp.K = K; tp.status = status; tp.f16 = f16;
         tp.workspace = workspace; tp.workspace_bytes = workspace_bytes;
         return launch_tc(tp, s);
     }
     const DecodePlan pl = plan_decode(M, N, K);
-    if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_w4a16_gemm: K=%lld too large for the decode kernel", (long long)K);
+    if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld too large for the decode kernel", fn, (long long)K);
     const uint16_t* xin = (const uint16_t*)X;
     if (pre_quant_scale) {
-        // x' = RN_bf16(x * pre_quant_scale) into the workspace, then the GEMM reads x'
+        // x' = RN(x * pre_quant_scale) into the workspace, then the GEMM reads x'
         nvfp4_status st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)pre_quant_scale,
-                                           (uint16_t*)workspace, M, K, s);
+                                           (uint16_t*)workspace, M, K, f16, s);
         if (st != NVFP4_OK) return st;
         xin = (const uint16_t*)workspace;
     }
@@ -185,5 +187,19 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, co
     p.M = M; p.N = N; p.K = K;
     p.KB = round_up(K, kBlockK) / kBlockK;
     p.kbs = pl.kbs; p.splits = pl.splits; p.status = status;
-    return launch_decode(p, pl.MT, pl.ring, s);
+    return launch_decode(p, pl.MT, pl.ring, f16, s);
+}
+
+}  // namespace
+
+extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
+                                         int64_t M, int64_t N, int64_t K, void* Y,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+    return gemm_impl(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, false, stream);
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_gemm_f16(const void* X, const void* repacked, const void* pre_quant_scale,
+                                             int64_t M, int64_t N, int64_t K, void* Y,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+    return gemm_impl(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, true, stream);
 }

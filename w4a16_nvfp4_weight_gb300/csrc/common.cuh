@@ -16,7 +16,7 @@ namespace nvfp4 {
 
 // ---------------------------------------------------------------- layout ---
 constexpr uint32_t kMagic = 0x34504E56u;   // "VNP4"
-constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersion = 2;            // 2: BF16 and FP16 magnitude tables
 constexpr int kGroup = 16;                  // K elements per E4M3 scale
 constexpr int kTileRows = 256;              // rows per tile (N padding)
 constexpr int kBlockK = 64;                 // k per atom (K padding)
@@ -26,8 +26,14 @@ constexpr int kAtomCodeBytes = 512;         // 16 rows x 64 k x 4 bits
 constexpr int kAtomScaleBytes = 64;         // 16 rows x 4 groups
 constexpr int kAtomBytes = kAtomCodeBytes + kAtomScaleBytes;   // 576
 constexpr size_t kHeaderBytes = 256;
-constexpr size_t kLutBytes = 256 * 16;
-constexpr size_t kTilesOffset = kHeaderBytes + kLutBytes;      // 4352
+constexpr size_t kLutBytes = 256 * 16;                          // one magnitude table
+constexpr size_t kLutBf16Offset = kHeaderBytes;                 // table for BF16 activations
+constexpr size_t kLutF16Offset = kHeaderBytes + kLutBytes;      // table for FP16 activations
+constexpr size_t kTilesOffset = kHeaderBytes + 2 * kLutBytes;   // 8448
+
+// Byte offset of the magnitude table for the activation type (FP16 or BF16).
+template <bool F16>
+__host__ __device__ constexpr size_t lut_offset() { return F16 ? kLutF16Offset : kLutBf16Offset; }
 
 struct Header {
     uint32_t magic;
@@ -49,9 +55,10 @@ __host__ __device__ inline size_t atom_offset(int64_t nt, int64_t kb, int64_t rb
 }
 
 // ----------------------------------------------------- register expansion ---
-// One magnitude-table entry: BF16 of the 8 E2M1 magnitudes times one E4M3
-// scale times g, split into low bytes (l0: m0..m3, l1: m4..m7) and high
-// bytes (h0, h1), so that one byte permute per byte plane looks up 4 codes.
+// One magnitude-table entry: the 8 E2M1 magnitudes times one E4M3 scale times
+// g, rounded to the 16-bit activation type (BF16 or FP16; both keep the sign
+// in bit 15), split into low bytes (l0: m0..m3, l1: m4..m7) and high bytes
+// (h0, h1), so that one byte permute per byte plane looks up 4 codes.
 struct Lut {
     uint32_t l0, l1, h0, h1;
 };
@@ -114,6 +121,35 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
     uint16_t out;
     asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(out) : "f"(v));
     return out;
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float v) {
+    uint16_t out;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(out) : "f"(v));
+    return out;
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    float out;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(out) : "h"(h));
+    return out;
+}
+
+// FP16 (bits) of x * s, both FP16: 11 x 11 significant bits are exact in FP32
+// (FP16 subnormals are FP32 normals), so one RN conversion rounds once.
+__device__ __forceinline__ uint16_t awq_mul_f16(uint16_t x, uint16_t s) {
+    return f32_to_f16_bits(__fmul_rn(f16_bits_to_f32(x), f16_bits_to_f32(s)));
+}
+
+// Round an FP32 result to the activation type.
+template <bool F16>
+__device__ __forceinline__ uint16_t f32_to_act_bits(float v) {
+    return F16 ? f32_to_f16_bits(v) : f32_to_bf16_bits(v);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint16_t awq_mul(uint16_t x, uint16_t s) {
+    return F16 ? awq_mul_f16(x, s) : awq_mul_bf16(x, s);
 }
 
 // ---------------------------------------------------------- host helpers ---

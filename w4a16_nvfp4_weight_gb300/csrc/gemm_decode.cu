@@ -68,7 +68,7 @@ struct Smem {
     static constexpr size_t ring = lut + kLutBytes;
 };
 
-template <int MT, int R>
+template <int MT, int R, bool F16>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -146,7 +146,7 @@ decode_kernel(const DecodeParams p) {
                 // copies go out before the programmatic-launch wait, every
                 // activation copy after it.
                 mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
-                bulk_g2s(lut, p.rp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                bulk_g2s(lut, p.rp + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
                 auto stage_blocks = [&](int i) { return min(kBlocksPerStage, nkb - i * kBlocksPerStage); };
                 auto stage_xk = [&](int i) {
                     const int64_t kx_left = p.K - (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
@@ -216,7 +216,7 @@ decode_kernel(const DecodeParams p) {
                 const int nb = nkb - i * kBlocksPerStage;
                 #pragma unroll
                 for (int b = 0; b < kBlocksPerStage; ++b)
-                    if (b < nb) atom_mma<MT, kXRowElems>(codes[b], sc[b], lut, xrow + b * kBlockK, acc);
+                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], lut, xrow + b * kBlockK, acc);
             }
             fence_proxy_async();           // reads of the stage before the next bulk copy into it
             __syncwarp();
@@ -254,12 +254,13 @@ decode_kernel(const DecodeParams p) {
             const int t = e / kRowsPerCta, row = e % kRowsPerCta;      // consecutive e -> consecutive n
             const int64_t n = (int64_t)rg * kRowsPerCta + row;
             const int64_t m = m0 + t;
-            if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_bf16_bits(sum);
+            if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_act_bits<F16>(sum);
         }
     }
 }
 
-// x' = RN_bf16(x * pre_quant_scale), one thread per 8 elements.
+// x' = RN(x * pre_quant_scale) in the activation type, one thread per 8 elements.
+template <bool F16>
 __global__ void awq_scale_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
                                  uint16_t* __restrict__ Xs, int64_t M, int64_t K) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
@@ -272,8 +273,8 @@ __global__ void awq_scale_kernel(const uint16_t* __restrict__ X, const uint16_t*
     uint32_t o[4];
     #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const uint16_t lo = awq_mul_bf16((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
-        const uint16_t hi = awq_mul_bf16((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
+        const uint16_t lo = awq_mul<F16>((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
+        const uint16_t hi = awq_mul<F16>((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
         o[e] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
     *reinterpret_cast<uint4*>(Xs + i) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -282,9 +283,10 @@ __global__ void awq_scale_kernel(const uint16_t* __restrict__ X, const uint16_t*
 }  // namespace
 
 nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* Xs, int64_t M, int64_t K,
-                              cudaStream_t stream) {
+                              bool f16, cudaStream_t stream) {
     const int64_t n8 = M * K / 8;
-    awq_scale_kernel<<<(unsigned)ceil_div(n8, 256), 256, 0, stream>>>(X, pqs, Xs, M, K);
+    if (f16) awq_scale_kernel<true><<<(unsigned)ceil_div(n8, 256), 256, 0, stream>>>(X, pqs, Xs, M, K);
+    else awq_scale_kernel<false><<<(unsigned)ceil_div(n8, 256), 256, 0, stream>>>(X, pqs, Xs, M, K);
     return check_cuda(cudaGetLastError(), "AWQ activation scaling: launch");
 }
 
@@ -308,7 +310,12 @@ int decode_ctas_per_sm(int MT, int ring) {
     return n < 1 ? 1 : (n > 7 ? 7 : n);        // 7 x 288 threads fit in 2048
 }
 
-nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStream_t stream) {
+template <int MT, int R>
+const void* decode_fn(bool f16) {
+    return f16 ? (const void*)decode_kernel<MT, R, true> : (const void*)decode_kernel<MT, R, false>;
+}
+
+nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, bool f16, cudaStream_t stream) {
     DecodeParams p = p_in;
     const int64_t rgs = ceil_div(p.N, kRowsPerCta);
     const int64_t mchunks = ceil_div(p.M, 8 * MT);
@@ -326,10 +333,8 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStrea
         const size_t cap_smem = (size_t)(228 * 1024) / (size_t)even - 1024 - 8192;
         smem = std::max(smem, cap_smem);
     }
-    const void* fn = MT == 1 ? (ring == kRingDeep ? (const void*)decode_kernel<1, kRingDeep>
-                                                  : (const void*)decode_kernel<1, kRingShallow>)
-                             : (ring == kRingDeep ? (const void*)decode_kernel<2, kRingDeep>
-                                                  : (const void*)decode_kernel<2, kRingShallow>);
+    const void* fn = MT == 1 ? (ring == kRingDeep ? decode_fn<1, kRingDeep>(f16) : decode_fn<1, kRingShallow>(f16))
+                             : (ring == kRingDeep ? decode_fn<2, kRingDeep>(f16) : decode_fn<2, kRingShallow>(f16));
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
     if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
@@ -350,10 +355,8 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, cudaStrea
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (MT == 1) e = ring == kRingDeep ? cudaLaunchKernelEx(&cfg, decode_kernel<1, kRingDeep>, p)
-                                       : cudaLaunchKernelEx(&cfg, decode_kernel<1, kRingShallow>, p);
-    else e = ring == kRingDeep ? cudaLaunchKernelEx(&cfg, decode_kernel<2, kRingDeep>, p)
-                               : cudaLaunchKernelEx(&cfg, decode_kernel<2, kRingShallow>, p);
+    void* args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
     return check_cuda(e, "decode GEMM: launch");
 }
 

@@ -5,10 +5,10 @@
 namespace nvfp4 {
 
 struct DecodeParams {
-    const uint16_t* X;        // BF16 [M, K]
+    const uint16_t* X;        // BF16 or FP16 [M, K]
     const uint16_t* pqs;      // unused by the kernel: AWQ scaling runs first (launch_awq_scale)
     const uint8_t* rp;        // repacked weight
-    uint16_t* Y;              // BF16 [M, N]
+    uint16_t* Y;              // BF16 or FP16 [M, N]
     int64_t M, N, K;
     int64_t KB;               // 64-k blocks of the padded K
     int kbs;                  // 64-k blocks per split
@@ -29,10 +29,12 @@ int decode_ctas_per_sm(int MT, int ring);
 
 // MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
 // covered by a third grid dimension.
-nvfp4_status launch_decode(const DecodeParams& p, int MT, int ring, cudaStream_t stream);
+// f16: FP16 activations and output (else BF16).
+nvfp4_status launch_decode(const DecodeParams& p, int MT, int ring, bool f16, cudaStream_t stream);
 
-// Xs = RN_bf16(X * pqs) for an M x K activation (K a multiple of 16).
+// Xs = RN(X * pqs) in the activation type (FP16 when f16, else BF16) for an
+// M x K activation (K a multiple of 16).
 nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* Xs, int64_t M, int64_t K,
-                              cudaStream_t stream);
+                              bool f16, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int c) {
 
 __device__ __forceinline__ float silu_tc(float v) { return v / (1.0f + expf(-v)); }
 
-template <int SUBM, TcMode MODE>
+template <int SUBM, TcMode MODE, bool F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -142,7 +142,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t idesc = umma_idesc_bf16(128, kBN);
+    constexpr uint32_t idesc = umma_idesc(128, kBN, F16);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -155,7 +155,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 mbar_arrive(lut_bar);
             } else {
                 mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
-                bulk_g2s(lut, wbase + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                bulk_g2s(lut, wbase + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
                 // FC1: 128 gate rows j0.. and the 128 matching up rows I + j0.. (two
                 // half tiles); otherwise one 256-row tile
                 auto half_tile = [&](int64_t row0) {
@@ -206,7 +206,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 for (int mi = 0; mi < SUBM; ++mi)
                     #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(tmem + mi * kBN, sw128_kmajor_desc(a_base + mi * kATileBytes + kk * 32),
+                        umma_f16kind_ss(tmem + mi * kBN, sw128_kmajor_desc(a_base + mi * kATileBytes + kk * 32),
                                      sw128_kmajor_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
                 umma_commit(&tma_empty[s1]);
                 umma_commit(&deq_empty[s2]);
@@ -287,8 +287,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                         uint32_t packed[8];
                         #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            packed[i] = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i])) |
-                                        ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[2 * i + 1])) << 16);
+                            packed[i] = (uint32_t)f32_to_act_bits<F16>(__uint_as_float(v[2 * i])) |
+                                        ((uint32_t)f32_to_act_bits<F16>(__uint_as_float(v[2 * i + 1])) << 16);
                         uint16_t* yrow = p.Y + m * p.N;
                         if (vec_ok && n + 16 <= p.N) {
                             *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -313,7 +313,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                         for (int i = 0; i < 8; ++i) {
                             const float h0 = silu_tc(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
                             const float h1 = silu_tc(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                            packed[i] = (uint32_t)f32_to_bf16_bits(h0) | ((uint32_t)f32_to_bf16_bits(h1) << 16);
+                            packed[i] = (uint32_t)f32_to_act_bits<F16>(h0) | ((uint32_t)f32_to_act_bits<F16>(h1) << 16);
                         }
                         uint16_t* hrow = p.Y + m * p.I + n0 + col;      // I and n0 are multiples of 64
                         *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -349,7 +349,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     }
 }
 
-// Y = RN_bf16(sum over splits of the FP32 partials), splits in order.
+// Y = RN(sum over splits of the FP32 partials) in the activation type, splits in order.
+template <bool F16>
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t MN,
                                      uint16_t* __restrict__ Y) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -360,8 +361,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
         s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
     // Y is only guaranteed 4-byte aligned: two 32-bit stores
-    reinterpret_cast<uint32_t*>(Y + i)[0] = (uint32_t)f32_to_bf16_bits(s.x) | ((uint32_t)f32_to_bf16_bits(s.y) << 16);
-    reinterpret_cast<uint32_t*>(Y + i)[1] = (uint32_t)f32_to_bf16_bits(s.z) | ((uint32_t)f32_to_bf16_bits(s.w) << 16);
+    reinterpret_cast<uint32_t*>(Y + i)[0] = (uint32_t)f32_to_act_bits<F16>(s.x) | ((uint32_t)f32_to_act_bits<F16>(s.y) << 16);
+    reinterpret_cast<uint32_t*>(Y + i)[1] = (uint32_t)f32_to_act_bits<F16>(s.z) | ((uint32_t)f32_to_act_bits<F16>(s.w) << 16);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -382,31 +383,38 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-nvfp4_status encode_rows_map(CUtensorMap* tmap, const uint16_t* X, int64_t rows, int64_t K) {
+nvfp4_status encode_rows_map(CUtensorMap* tmap, const uint16_t* X, int64_t rows, int64_t K, bool f16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(NVFP4_ERR_CUDA, "tile GEMM: cuTensorMapEncodeTiled unavailable");
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {64, 128};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult cr = enc(tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+    CUresult cr = enc(tmap, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "tile GEMM: tensor map encode failed (%d)", (int)cr);
     return NVFP4_OK;
 }
 
-template <int SUBM, TcMode MODE>
-nvfp4_status launch_tc_impl(const uint16_t* X, int64_t x_rows, const TcKParams& kp, dim3 grid, cudaStream_t stream) {
+template <int SUBM, TcMode MODE, bool F16>
+nvfp4_status launch_tc_typed(const uint16_t* X, int64_t x_rows, const TcKParams& kp, dim3 grid, cudaStream_t stream) {
     CUtensorMap tmap;
-    nvfp4_status st = encode_rows_map(&tmap, X, x_rows, kp.K);
+    nvfp4_status st = encode_rows_map(&tmap, X, x_rows, kp.K, F16);
     if (st != NVFP4_OK) return st;
     const size_t smem = TcSmem<SUBM>::total + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SUBM, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SUBM, MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "tile GEMM: shared memory attribute");
-    tc_gemm_kernel<SUBM, MODE><<<grid, kTcThreads, smem, stream>>>(tmap, kp);
+    tc_gemm_kernel<SUBM, MODE, F16><<<grid, kTcThreads, smem, stream>>>(tmap, kp);
     return check_cuda(cudaGetLastError(), "tile GEMM: launch");
+}
+
+template <int SUBM, TcMode MODE>
+nvfp4_status launch_tc_impl(const uint16_t* X, int64_t x_rows, const TcKParams& kp, dim3 grid, bool f16,
+                            cudaStream_t stream) {
+    return f16 ? launch_tc_typed<SUBM, MODE, true>(X, x_rows, kp, grid, stream)
+               : launch_tc_typed<SUBM, MODE, false>(X, x_rows, kp, grid, stream);
 }
 
 size_t awq_ws_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
@@ -460,7 +468,7 @@ size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs) {
 nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     const uint16_t* X = p.X;
     if (p.pqs) {
-        nvfp4_status st = launch_awq_scale(p.X, p.pqs, (uint16_t*)p.workspace, p.M, p.K, stream);
+        nvfp4_status st = launch_awq_scale(p.X, p.pqs, (uint16_t*)p.workspace, p.M, p.K, p.f16, stream);
         if (st != NVFP4_OK) return st;
         X = (const uint16_t*)p.workspace;
     }
@@ -475,12 +483,16 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     const unsigned gx = (unsigned)ceil_div(p.N, kBN);
     nvfp4_status st;
     if (p.M <= 128)
-        st = launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128), sp.splits), stream);
+        st = launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128), sp.splits), p.f16,
+                                               stream);
     else
-        st = launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256), sp.splits), stream);
+        st = launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256), sp.splits), p.f16,
+                                               stream);
     if (st != NVFP4_OK || sp.splits == 1) return st;
     const int64_t MN = p.M * p.N;
-    splitk_reduce_kernel<<<(unsigned)ceil_div(MN / 4, 256), 256, 0, stream>>>(kp.partial, sp.splits, MN, p.Y);
+    const unsigned rgrid = (unsigned)ceil_div(MN / 4, 256);
+    if (p.f16) splitk_reduce_kernel<true><<<rgrid, 256, 0, stream>>>(kp.partial, sp.splits, MN, p.Y);
+    else splitk_reduce_kernel<false><<<rgrid, 256, 0, stream>>>(kp.partial, sp.splits, MN, p.Y);
     return check_cuda(cudaGetLastError(), "tile GEMM: split-K reduction launch");
 }
 
@@ -495,10 +507,10 @@ nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
     const unsigned gx = fc1 ? (unsigned)(m.I / 128) : (unsigned)ceil_div(m.N, kBN);
     const dim3 grid(gx, (unsigned)m.max_items);
     if (m.subm == 1)
-        return fc1 ? launch_tc_impl<1, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, stream)
-                   : launch_tc_impl<1, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, stream);
-    return fc1 ? launch_tc_impl<2, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, stream)
-               : launch_tc_impl<2, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, stream);
+        return fc1 ? launch_tc_impl<1, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
+                   : launch_tc_impl<1, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
+    return fc1 ? launch_tc_impl<2, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
+               : launch_tc_impl<2, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
 }
 
 }  // namespace nvfp4

@@ -5,10 +5,11 @@
 namespace nvfp4 {
 
 struct TcParams {
-    const uint16_t* X;        // BF16 [M, K]
-    const uint16_t* pqs;      // BF16 [K] or nullptr
+    const uint16_t* X;        // BF16 or FP16 [M, K]
+    const uint16_t* pqs;      // [K] or nullptr, same type as X
     const uint8_t* rp;        // repacked weight
-    uint16_t* Y;              // BF16 [M, N]
+    uint16_t* Y;              // [M, N], same type as X
+    bool f16;                 // FP16 activations and output (else BF16)
     int64_t M, N, K;
     void* workspace;
     size_t workspace_bytes;
@@ -19,8 +20,9 @@ struct TcParams {
 // rows of one expert; X rows are already in permuted (expert-contiguous) order.
 struct TcMoeParams {
     bool fc1;                 // FC1 (gate/up + SwiGLU -> H) or FC2 (x p -> Yp)
+    bool f16;                 // FP16 activations (else BF16)
     int subm;                 // 1 or 2: 128 or 256 rows per work item
-    const uint16_t* X;        // [x_rows, K] BF16, permuted rows
+    const uint16_t* X;        // [x_rows, K] BF16 or FP16, permuted rows
     int64_t x_rows;
     const uint8_t* w;         // stacked repacked experts
     size_t w_stride;

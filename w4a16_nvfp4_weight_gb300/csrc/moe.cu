@@ -259,7 +259,7 @@ struct MoeLinParams {
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
-template <int MT, bool GATED>
+template <int MT, bool GATED, bool F16>
 __global__ void __launch_bounds__(kThreads)
 moe_linear_kernel(const MoeLinParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -334,7 +334,7 @@ moe_linear_kernel(const MoeLinParams p) {
                 mbar_arrive(lut_bar);
             } else {
                 mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
-                bulk_g2s(lut, wexp + kHeaderBytes, (uint32_t)kLutBytes, lut_bar);
+                bulk_g2s(lut, wexp + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
                 // activation row of each of this item's routed rows
                 const uint16_t* xrow[TOK];
                 for (int t = 0; t < nrows; ++t) {
@@ -398,7 +398,7 @@ moe_linear_kernel(const MoeLinParams p) {
                 const int nb = nkb - i * kBlocksPerStage;
                 #pragma unroll
                 for (int b = 0; b < kBlocksPerStage; ++b)
-                    if (b < nb) atom_mma<MT, kXRowElems>(codes[b], sc[b], lut, xr + b * kBlockK, acc);
+                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], lut, xr + b * kBlockK, acc);
             }
             fence_proxy_async();
             __syncwarp();
@@ -452,7 +452,7 @@ moe_linear_kernel(const MoeLinParams p) {
                 }
                 const int t = ei / 64, jj = ei % 64;
                 if (t < nrows)
-                    p.H[(int64_t)(r0 + t) * p.I + (int64_t)cgi * 64 + jj] = f32_to_bf16_bits(silu_f(gsum) * usum);
+                    p.H[(int64_t)(r0 + t) * p.I + (int64_t)cgi * 64 + jj] = f32_to_act_bits<F16>(silu_f(gsum) * usum);
             }
         } else {
             const int total = TOK * 128;
@@ -473,6 +473,7 @@ moe_linear_kernel(const MoeLinParams p) {
 }
 
 // ----------------------------------------------------------------- combine --
+template <bool F16>
 __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk, int64_t H,
                                uint16_t* __restrict__ out) {
     pdl_wait_previous();
@@ -485,13 +486,14 @@ __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk
         const float4 v = *reinterpret_cast<const float4*>(Yp + (t * topk + j) * H + n);
         s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
-    const uint32_t lo = (uint32_t)f32_to_bf16_bits(s.x) | ((uint32_t)f32_to_bf16_bits(s.y) << 16);
-    const uint32_t hi = (uint32_t)f32_to_bf16_bits(s.z) | ((uint32_t)f32_to_bf16_bits(s.w) << 16);
+    const uint32_t lo = (uint32_t)f32_to_act_bits<F16>(s.x) | ((uint32_t)f32_to_act_bits<F16>(s.y) << 16);
+    const uint32_t hi = (uint32_t)f32_to_act_bits<F16>(s.z) | ((uint32_t)f32_to_act_bits<F16>(s.w) << 16);
     *reinterpret_cast<uint2*>(out + i) = make_uint2(lo, hi);
 }
 
 // Rows of X in permuted (expert-contiguous) order, for the tile path:
 // Xp[r] = X[perm[r] / topk], times the AWQ pre-quant scale when given.
+template <bool F16>
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
                                    const int32_t* __restrict__ perm, int topk, int64_t n, int64_t H,
                                    uint16_t* __restrict__ Xp) {
@@ -508,8 +510,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_
         const uint32_t sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
         #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const uint16_t lo = awq_mul_bf16((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
-            const uint16_t hi = awq_mul_bf16((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
+            const uint16_t lo = awq_mul<F16>((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
+            const uint16_t hi = awq_mul<F16>((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
             xv[e] = (uint32_t)lo | ((uint32_t)hi << 16);
         }
         v = make_uint4(xv[0], xv[1], xv[2], xv[3]);
@@ -542,10 +544,10 @@ size_t moe_lin_smem(int MT, bool gated) {
     return kRingOffset + kLutBytes + ring + part * 4;
 }
 
-template <int MT, bool GATED>
-nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_items, cudaStream_t s) {
+template <int MT, bool GATED, bool F16>
+nvfp4_status launch_moe_linear_typed(const MoeLinParams& p, unsigned gx, unsigned max_items, cudaStream_t s) {
     const size_t smem = moe_lin_smem(MT, GATED);
-    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED>,
+    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "MoE linear: shared memory attribute");
     cudaLaunchConfig_t cfg = {};
@@ -562,8 +564,14 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED>, p);
+    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED, F16>, p);
     return check_cuda(e, GATED ? "MoE FC1: launch" : "MoE FC2: launch");
+}
+
+template <int MT, bool GATED>
+nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_items, bool f16, cudaStream_t s) {
+    return f16 ? launch_moe_linear_typed<MT, GATED, true>(p, gx, max_items, s)
+               : launch_moe_linear_typed<MT, GATED, false>(p, gx, max_items, s);
 }
 
 struct MoeLayout {
@@ -621,14 +629,14 @@ extern "C" size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t 
     return moe_layout(T, E, topk, H, I, true).total;
 }
 
-extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
-                                                const void* fc1, const void* fc2,
-                                                const void* fc1_pre_quant_scale,
-                                                int64_t T, int E, int topk, int64_t H, int64_t I,
-                                                void* out, int32_t* topk_idx_out, float* topk_weight_out,
-                                                int32_t* perm_out, int32_t* offsets_out,
-                                                void* workspace, size_t workspace_bytes, void* stream) {
-    const char* fn = "nvfp4_w4a16_moe_grouped";
+namespace nvfp4 {
+namespace {
+
+nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1, const void* fc2,
+                      const void* fc1_pre_quant_scale, int64_t T, int E, int topk, int64_t H, int64_t I,
+                      void* out, int32_t* topk_idx_out, float* topk_weight_out, int32_t* perm_out,
+                      int32_t* offsets_out, void* workspace, size_t workspace_bytes, bool f16, void* stream) {
+    const char* fn = f16 ? "nvfp4_w4a16_moe_grouped_f16" : "nvfp4_w4a16_moe_grouped";
     if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
     if (E < 1 || E > kMaxExperts) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: E=%d outside [1, %d]", fn, E, kMaxExperts);
     if (topk < 1 || topk > kMaxTopk || topk > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: topk=%d outside [1, min(E, %d)]", fn, topk, kMaxTopk);
@@ -665,7 +673,8 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
 
     const uint16_t* xin = (const uint16_t*)X;
     if (fc1_pre_quant_scale && !L.tile) {
-        st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H, s);
+        st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H,
+                              f16, s);
         if (st != NVFP4_OK) return st;
         xin = (const uint16_t*)(ws + L.xs);
     }
@@ -693,12 +702,13 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
     if (L.tile) {
         // gather the routed rows into expert-contiguous order, then two tile GEMMs
         uint16_t* xp = (uint16_t*)(ws + L.xp);
-        st = launch_chained(gather_rows_kernel, dim3((unsigned)ceil_div(n * H / 8, 256)), dim3(256), 0, s,
+        st = launch_chained(f16 ? gather_rows_kernel<true> : gather_rows_kernel<false>,
+                            dim3((unsigned)ceil_div(n * H / 8, 256)), dim3(256), 0, s,
                             "MoE gather: launch", (const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale,
                             (const int32_t*)perm, topk, n, H, xp);
         if (st != NVFP4_OK) return st;
         TcMoeParams t1{};
-        t1.fc1 = true; t1.subm = L.subm; t1.X = xp; t1.x_rows = n;
+        t1.fc1 = true; t1.f16 = f16; t1.subm = L.subm; t1.X = xp; t1.x_rows = n;
         t1.w = (const uint8_t*)fc1; t1.w_stride = nvfp4_repack_size(2 * I, H);
         t1.N = 2 * I; t1.K = H; t1.I = I; t1.items = items; t1.n_items = n_items; t1.max_items = L.max_items;
         t1.perm = perm; t1.wts = wts; t1.H = hbuf; t1.status = status;
@@ -718,8 +728,8 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
         p1.splits = (int)ceil_div(p1.KB, p1.kbs);
         p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
         p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
-        st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s)
-                       : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, s);
+        st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, f16, s)
+                       : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
 
         MoeLinParams p2{};
@@ -730,13 +740,39 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
         p2.splits = (int)ceil_div(p2.KB, p2.kbs);
         p2.X = hbuf; p2.perm = perm; p2.topk = topk; p2.items = items; p2.n_items = n_items;
         p2.I = I; p2.Yp = yp; p2.wts = wts; p2.status = status;
-        st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s)
-                       : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, s);
+        st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s)
+                       : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
     }
 
-    return launch_chained(combine_kernel, dim3((unsigned)ceil_div(T * H / 4, 256)), dim3(256), 0, s,
+    return launch_chained(f16 ? combine_kernel<true> : combine_kernel<false>,
+                          dim3((unsigned)ceil_div(T * H / 4, 256)), dim3(256), 0, s,
                           "MoE combine: launch", (const float*)yp, T, topk, H, (uint16_t*)out);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* router_logits,
+                                                const void* fc1, const void* fc2,
+                                                const void* fc1_pre_quant_scale,
+                                                int64_t T, int E, int topk, int64_t H, int64_t I,
+                                                void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                                int32_t* perm_out, int32_t* offsets_out,
+                                                void* workspace, size_t workspace_bytes, void* stream) {
+    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out, topk_idx_out,
+                    topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, false, stream);
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* router_logits,
+                                                    const void* fc1, const void* fc2,
+                                                    const void* fc1_pre_quant_scale,
+                                                    int64_t T, int E, int topk, int64_t H, int64_t I,
+                                                    void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                                    int32_t* perm_out, int32_t* offsets_out,
+                                                    void* workspace, size_t workspace_bytes, void* stream) {
+    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out, topk_idx_out,
+                    topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, true, stream);
 }
 
 // ------------------------------------------------- allocation-free variant --

@@ -49,27 +49,56 @@ __device__ uint16_t bf16_from_double(double v) {
     return sign | (uint16_t)(e << 7) | (uint16_t)((r >> 45) & 0x7F);
 }
 
-// Magnitude table: entry s holds RN_bf16(mag_j * e4m3(s) * g) for the eight
-// E2M1 magnitudes j.  The product is exact in double (<= 30 significant bits),
-// so each entry is rounded exactly once.
+// Round a double to FP16 (IEEE binary16), nearest-even, on the bit pattern:
+// keep the top 10 of the 52 fraction bits (round at bit 42) for normal
+// results, use the fixed 2^-24 grid for FP16 subnormals, overflow to infinity.
+__device__ uint16_t f16_from_double(double v) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(v);
+    const uint16_t sign = (uint16_t)((b >> 48) & 0x8000);
+    const unsigned long long a = b & 0x7FFFFFFFFFFFFFFFull;
+    if (a > 0x7FF0000000000000ull) return sign | 0x7E00;   // NaN
+    if (a == 0x7FF0000000000000ull) return sign | 0x7C00;  // inf
+    const double x = __longlong_as_double((long long)a);
+    if (x < 0x1p-14) {
+        const double q = rint(x * 0x1p24);                   // exact scaling, RNE
+        return sign | (uint16_t)q;                           // 1024 -> min normal
+    }
+    const unsigned long long lsb = (a >> 42) & 1ull;
+    unsigned long long r = a + 0x1FFFFFFFFFFull + lsb;       // + (2^41 - 1) + lsb
+    r &= ~((1ull << 42) - 1ull);
+    const int e = (int)(r >> 52) - 1023 + 15;
+    if (e >= 31) return sign | 0x7C00;
+    return sign | (uint16_t)(e << 10) | (uint16_t)((r >> 42) & 0x3FF);
+}
+
+// Magnitude tables: entry s holds RN(mag_j * e4m3(s) * g) for the eight E2M1
+// magnitudes j, once rounded to BF16 and once to FP16 (the two activation
+// types).  The product is exact in double (<= 30 significant bits), so each
+// entry is rounded exactly once.
 __global__ void lut_kernel(uint8_t* out, float g, int64_t N, int64_t K, int64_t Np, int64_t Kp,
                            float global_scale, uint32_t is_div) {
     const int s = threadIdx.x;          // 256 threads
     const double mags[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
     const double sv = e4m3_to_double((uint32_t)s);
-    uint8_t lo[8], hi[8];
+    // sign of a NaN weight = sign(scale) xor sign(g) (code sign applied later)
+    const uint16_t nan_sign = (uint16_t)((((uint32_t)s >> 7) ^ (__float_as_uint(g) >> 31)) << 15);
+    uint8_t lo[2][8], hi[2][8];
     for (int j = 0; j < 8; ++j) {
         const double v = mags[j] * sv * (double)g;
-        uint16_t bits = bf16_from_double(v);
+        uint16_t bits[2] = {bf16_from_double(v), f16_from_double(v)};
         if (isnan(v)) {
-            // sign of a NaN weight = sign(scale) xor sign(g) (code sign applied later)
-            bits = (uint16_t)(0x7FC0 | ((((uint32_t)s >> 7) ^ (__float_as_uint(g) >> 31)) << 15));
+            bits[0] = (uint16_t)(0x7FC0 | nan_sign);
+            bits[1] = (uint16_t)(0x7E00 | nan_sign);
         }
-        lo[j] = (uint8_t)(bits & 0xFF);
-        hi[j] = (uint8_t)(bits >> 8);
+        for (int t = 0; t < 2; ++t) {
+            lo[t][j] = (uint8_t)(bits[t] & 0xFF);
+            hi[t][j] = (uint8_t)(bits[t] >> 8);
+        }
     }
-    uint8_t* e = out + kHeaderBytes + (size_t)s * 16;
-    for (int j = 0; j < 8; ++j) { e[j] = lo[j]; e[8 + j] = hi[j]; }
+    for (int t = 0; t < 2; ++t) {
+        uint8_t* e = out + (t ? kLutF16Offset : kLutBf16Offset) + (size_t)s * 16;
+        for (int j = 0; j < 8; ++j) { e[j] = lo[t][j]; e[8 + j] = hi[t][j]; }
+    }
     if (s == 0) {
         Header h{};
         h.magic = kMagic; h.version = kVersion;
@@ -124,8 +153,9 @@ __global__ void tiles_kernel(const uint8_t* __restrict__ packed, const uint8_t* 
 }
 
 // Standalone dequant: one warp per atom, each lane expands its 32 elements
-// through the magnitude table (the same expansion the GEMM kernels use) and
-// stores the valid ones.
+// through the magnitude table of the activation type (the same expansion the
+// GEMM kernels use) and stores the valid ones.
+template <bool F16>
 __global__ void dequant_kernel(const uint8_t* __restrict__ rp, uint16_t* __restrict__ out,
                                int64_t N, int64_t K, int64_t KB, int64_t total_atoms, int* status) {
     __shared__ uint4 lut[256];
@@ -135,7 +165,7 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ rp, uint16_t* __restr
         return;
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x)
-        lut[i] = reinterpret_cast<const uint4*>(rp + kHeaderBytes)[i];
+        lut[i] = reinterpret_cast<const uint4*>(rp + lut_offset<F16>())[i];
     __syncthreads();
     const int64_t atom = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (atom >= total_atoms) return;
@@ -203,18 +233,37 @@ extern "C" nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scale
     return check_cuda(cudaGetLastError(), "nvfp4_repack: tile launch");
 }
 
-extern "C" nvfp4_status nvfp4_dequant(const void* repacked, int64_t N, int64_t K,
-                                      uint16_t* out_bf16, void* stream) {
-    if (N <= 0 || K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_dequant: N=%lld K=%lld (K must be a positive multiple of 16)", (long long)N, (long long)K);
-    if (!repacked || !out_bf16) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_dequant: null pointer");
-    if (!aligned(repacked, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_dequant: repacked weight must be 256-byte aligned");
-    if (!aligned(out_bf16, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_dequant: out must be 16-byte aligned");
+namespace nvfp4 {
+namespace {
+
+nvfp4_status dequant_impl(const void* repacked, int64_t N, int64_t K, uint16_t* out, bool f16, void* stream) {
+    const char* fn = f16 ? "nvfp4_dequant_f16" : "nvfp4_dequant";
+    if (N <= 0 || K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: N=%lld K=%lld (K must be a positive multiple of 16)", fn, (long long)N, (long long)K);
+    if (!repacked || !out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(repacked, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: repacked weight must be 256-byte aligned", fn);
+    if (!aligned(out, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: out must be 16-byte aligned", fn);
     const int64_t Np = round_up(N, kTileRows), KB = round_up(K, kBlockK) / kBlockK;
     const int64_t atoms = (Np / kAtomRows) * KB;
     int* status = device_status_ptr();
-    if (!status) return fail(NVFP4_ERR_CUDA, "nvfp4_dequant: no CUDA device");
+    if (!status) return fail(NVFP4_ERR_CUDA, "%s: no CUDA device", fn);
     const int warps = 8;
-    dequant_kernel<<<(unsigned)ceil_div(atoms, warps), warps * 32, 0, (cudaStream_t)stream>>>(
-        (const uint8_t*)repacked, out_bf16, N, K, KB, atoms, status);
-    return check_cuda(cudaGetLastError(), "nvfp4_dequant: launch");
+    const unsigned grid = (unsigned)ceil_div(atoms, warps);
+    if (f16)
+        dequant_kernel<true><<<grid, warps * 32, 0, (cudaStream_t)stream>>>((const uint8_t*)repacked, out, N, K, KB, atoms, status);
+    else
+        dequant_kernel<false><<<grid, warps * 32, 0, (cudaStream_t)stream>>>((const uint8_t*)repacked, out, N, K, KB, atoms, status);
+    return check_cuda(cudaGetLastError(), f16 ? "nvfp4_dequant_f16: launch" : "nvfp4_dequant: launch");
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_dequant(const void* repacked, int64_t N, int64_t K,
+                                      uint16_t* out_bf16, void* stream) {
+    return dequant_impl(repacked, N, K, out_bf16, false, stream);
+}
+
+extern "C" nvfp4_status nvfp4_dequant_f16(const void* repacked, int64_t N, int64_t K,
+                                          uint16_t* out_f16, void* stream) {
+    return dequant_impl(repacked, N, K, out_f16, true, stream);
 }

@@ -24,12 +24,23 @@ template <int MT, int S, int B> struct StreamRing {
     static_assert(kStageBytes % 16 == 0 && (kXRowElems * 2) % 16 == 0, "bulk copies need 16-byte alignment");
 };
 
-__device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// D += A * B on 16-bit operands of the activation type (BF16, or FP16 when
+// F16), FP32 accumulators.
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    if constexpr (F16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
 }
 
 // One atom: a lane holds 16 code bytes (rows g and g+8 of the atom, group q)
@@ -37,7 +48,7 @@ __device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], 
 // activation chunk (row stride XS elements, 16-byte aligned).  Within the
 // group the MMA's k order is permuted -- MMA j consumes k = 4j..4j+3 of every
 // lane's group -- and the activation fragments use the same permutation.
-template <int MT, int XS>
+template <int MT, int XS, bool F16>
 __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const uint4* lut,
                                          const uint16_t* xrow, float acc[MT][4]) {
     const Lut t0 = lut_from_uint4(lut[sc2 & 0xFF]);
@@ -55,10 +66,10 @@ __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const 
         const uint32_t a1[4] = {ra[2], rb[2], ra[3], rb[3]};
         const uint32_t a2[4] = {ra[4], rb[4], ra[5], rb[5]};
         const uint32_t a3[4] = {ra[6], rb[6], ra[7], rb[7]};
-        mma_bf16_16816(acc[mt], a0, b01.x, b01.y);
-        mma_bf16_16816(acc[mt], a1, b01.z, b01.w);
-        mma_bf16_16816(acc[mt], a2, b23.x, b23.y);
-        mma_bf16_16816(acc[mt], a3, b23.z, b23.w);
+        mma_16816<F16>(acc[mt], a0, b01.x, b01.y);
+        mma_16816<F16>(acc[mt], a1, b01.z, b01.w);
+        mma_16816<F16>(acc[mt], a2, b23.x, b23.y);
+        mma_16816<F16>(acc[mt], a3, b23.z, b23.w);
     }
 }
 

@@ -57,18 +57,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16: BF16 A and B, FP32 accumulator, both
-// K-major, M x N tile.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+// Instruction descriptor of kind::f16: A and B both BF16 (or both FP16 when
+// f16), FP32 accumulator, both K-major, M x N tile.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool f16) {
     return (1u << 4)                      // D format: F32
-         | (1u << 7)                      // A format: BF16
-         | (1u << 10)                     // B format: BF16
+         | ((f16 ? 0u : 1u) << 7)         // A format: F16 = 0, BF16 = 1
+         | ((f16 ? 0u : 1u) << 10)        // B format: F16 = 0, BF16 = 1
          | ((uint32_t)(N >> 3) << 17)     // N >> 3
          | ((uint32_t)(M >> 4) << 24);    // M >> 4
 }
 
-// D(tmem) (+)= A(smem) * B(smem)^T, issued by one thread.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+// D(tmem) (+)= A(smem) * B(smem)^T with 16-bit operands, issued by one thread.
+__device__ __forceinline__ void umma_f16kind_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                              uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
