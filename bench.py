@@ -9,7 +9,7 @@ algorithmic bytes moved per second (weights at 0.5625 B/element plus BF16
 activations in and out), with TFLOP/s beside it.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
-                    [--workload decode|prefill|lmhead|moe|tails] [--dtype bf16|f16]
+                    [--workload decode|prefill|lmhead|moe|mlp|tails] [--dtype bf16|f16]
 
 --dtype f16 runs the same workload with FP16 activations (FP16 weights operand
 and output) through the *_f16 entry points.
@@ -232,6 +232,8 @@ def run_ours(args, rank, world, device):
         config = {"workload": "odd shapes M{1,8,256} x (K,N){(2064,1000),(720,3000)}", "gemms_per_step": len(launches)}
     elif wl == "moe":
         return run_moe(args, rank, world, device, nv, synth)
+    elif wl == "mlp":
+        return run_mlp(args, rank, world, device, nv, synth)
     else:
         raise SystemExit(f"unknown workload {wl}")
 
@@ -485,6 +487,107 @@ def kernel_timing(nv, launches, base, stream, device, reps=30):
     return dict(seconds=total_s, bytes=total_b, flops=total_f, per_shape_us=per)
 
 
+MLP_H, MLP_I = 4096, 14336
+MLP_T = (1, 16, 512, 2048)
+
+
+def run_mlp(args, rank, world, device, nv, synth):
+    """The dense gated MLP (H=4096, I=14336: FC1 [28672 x 4096], FC2 [4096 x 14336])
+    at T = 1, 16, 512, 2048 tokens, one call each per step."""
+    r = synth.rng(synth.seed_for(6, 0))
+    fc1 = synth.quantize(synth.normal_weight(r, 2 * MLP_I, MLP_H))
+    fc2 = synth.quantize(synth.normal_weight(r, MLP_H, MLP_I))
+
+    def rep(w, N, K):
+        p, sc, d = w
+        return nv.repack(torch.from_numpy(p).to(device), torch.from_numpy(sc).to(device), float(d), N, K)
+
+    w1, w2 = rep(fc1, 2 * MLP_I, MLP_H), rep(fc2, MLP_H, MLP_I)
+    # four weight copies (4 x 99 MB), rotated between steps and repeated calls
+    wcopies = [(w1, w2)] + [(nv.NVFP4Weight(w1.buf.clone(), w1.N, w1.K), nv.NVFP4Weight(w2.buf.clone(), w2.N, w2.K))
+                            for _ in range(3)]
+    calls = []
+    for T in MLP_T:
+        x = bits_tensor(synth.normal_act(synth.rng(synth.seed_for(6, T)), (T, MLP_H), ACT), device)
+        ws = torch.empty(nv.mlp_workspace_size(T, MLP_H, MLP_I), dtype=torch.uint8, device=device)
+        out = torch.empty((T, MLP_H), dtype=act_torch(), device=device)
+        calls.append(dict(T=T, x=x, ws=ws, out=out))
+
+    def call(C, w=0):
+        a, b = wcopies[w % len(wcopies)]
+        nv.mlp(C["x"], a, b, out=C["out"], workspace=C["ws"])
+
+    stream = torch.cuda.Stream(device)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for C in calls:
+            call(C)
+        torch.cuda.synchronize()
+        assert nv.device_status() == 0
+        for w in range(len(wcopies)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for C in calls:
+                    call(C, w)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    wbytes = weight_bytes(2 * MLP_I, MLP_H) + weight_bytes(MLP_H, MLP_I)
+    for C in calls:
+        T = C["T"]
+        C["bytes"] = wbytes + 2 * 2 * T * MLP_H
+        C["flops"] = flops(T, 2 * MLP_I, MLP_H) + flops(T, MLP_H, MLP_I)
+    bytes_step = sum(C["bytes"] for C in calls)
+    flops_step = sum(C["flops"] for C in calls)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+    assert nv.device_status() == 0
+    per = {}
+    for C in calls:
+        with torch.cuda.stream(stream):
+            gg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gg, stream=stream):
+                for i in range(12):
+                    call(C, i)
+            gg.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gg.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 12
+        per[f"T={C['T']}"] = {"us": round(us, 2), "GB/s": round(C["bytes"] / us / 1e3, 1),
+                              "TFLOP/s": round(C["flops"] / us / 1e6, 2)}
+    pk = peaks()
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    return {
+        "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ACT, "data": "synthetic (seeded)",
+        "config": {"workload": "dense gated MLP H=4096 I=14336 at T{1,16,512,2048}",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: four copies of the 99 MB weight pair rotated between steps "
+                         "and between the repeated calls of the per-call timing"},
+        "tflops": round(world * flops_step / (ms_step * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(value / pk["hbm"], 4), "traffic": None, "peak_source": pk["source"],
+                     "note": "whole layer per step; T=512 and 2048 are tensor-bound, see per_call"},
+        "per_call": per,
+    }
+
+
 def run_e2e(nv, launches, stream, args, bw_unit):
     """Same step through the public API with pinned host activations in and
     host outputs back, copies inside the timed region."""
@@ -622,7 +725,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails", "moe"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails", "moe", "mlp"])
     ap.add_argument("--awq", action="store_true")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="activation type: BF16 (default) or FP16 activations, weights and output")
@@ -651,7 +754,7 @@ def main():
         return
     device = torch.device("cuda", local)
     res = run_ours(args, rank, world, device)
-    base = res.pop("_base")
+    base = res.pop("_base", None)
     if rank == 0:
         if not args.no_cpu_baseline and args.workload == "decode":
             res["cpu_baseline"] = cpu_baseline(base=base)

@@ -229,6 +229,36 @@ nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* router_logi
                                          int32_t* perm_out, int32_t* offsets_out,
                                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Dense gated MLP (FC1 gate/up + SwiGLU, FC2)                               */
+/* ------------------------------------------------------------------------ */
+
+size_t nvfp4_w4a16_mlp_workspace(int64_t T, int64_t H, int64_t I);
+
+/*
+ * out[t] = RN( FC2( RN( silu(g) * u ) ) ), [g; u] = FC1(x'_t): the MoE layer's
+ * expert computation on one dense weight pair, for every token (the SwiGLU of
+ * gated experts: SGLang PR 40022, review thread on is_gated; the fused gate/up
+ * FC1 "w3_w1" of "[TRTLLM-12288][feat] Support Nemotron-H nvfp4 ckpt on Hopper",
+ * Changes table).  RN rounds to BF16 (or FP16 for the _f16 entry point).
+ *  X                  device [T, H], 16-byte aligned.
+ *  fc1                device, repacked [2I, H]: rows [0, I) gate, [I, 2I) up.
+ *  fc2                device, repacked [H, I].
+ *  fc1_pre_quant_scale device [H] or NULL (AWQ scale on FC1's input).
+ *  out                device [T, H], 16-byte aligned.
+ *  workspace          >= nvfp4_w4a16_mlp_workspace(T, H, I) bytes, 256-byte
+ *                     aligned; holds h [T, I] and the scaled activation.
+ * H and I positive multiples of 64; T == 0 returns NVFP4_OK and launches nothing.
+ * FC1 runs the MoE FC1 kernels (SwiGLU fused into the epilogue, h never in
+ * FP32 memory), FC2 the dense GEMM.
+ */
+nvfp4_status nvfp4_w4a16_mlp(const void* X, const void* fc1, const void* fc2,
+                             const void* fc1_pre_quant_scale, int64_t T, int64_t H, int64_t I,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream);
+nvfp4_status nvfp4_w4a16_mlp_f16(const void* X, const void* fc1, const void* fc2,
+                                 const void* fc1_pre_quant_scale, int64_t T, int64_t H, int64_t I,
+                                 void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Allocation-free variant of nvfp4_w4a16_moe_grouped (no counterpart in the
  * source pages: it exists for callers that cannot allocate device memory, such

@@ -140,3 +140,24 @@ def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="b
     res["out_bits"] = act_bits(out, act)
     res["h_bits"] = h_all
     return res
+
+
+def mlp(x_bits, fc1, fc2, pqs_bits=None, act="bf16"):
+    """Dense gated MLP: the expert computation of ``moe_layer`` on one weight
+    pair, for every token (SwiGLU of gated experts: SGLang PR 40022, review
+    thread on ``is_gated``; fused gate/up FC1: "[TRTLLM-12288][feat] Support
+    Nemotron-H nvfp4 ckpt on Hopper", Changes table).
+
+    fc1 = (packed [2I, H/2], scales [2I, H/16], global, is_divisor), rows
+    [0, I) gate and [I, 2I) up; fc2 = (packed [H, I/2], scales [H, I/16],
+    global, is_divisor).  Returns (out float64 [T, H], out_bits, h_bits).
+    """
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    T, H = x_bits.shape
+    I = np.asarray(fc1[0]).shape[0] // 2
+    xs = x_bits if pqs_bits is None else awq_scale_activation(x_bits, pqs_bits, act)
+    x = act_to_float(xs, act)
+    gu = x @ expert_weights(fc1, H, act).T                # [T, 2I], exact float64
+    h = act_bits(silu(gu[:, :I]) * gu[:, I:], act)
+    out = act_to_float(h, act) @ expert_weights(fc2, I, act).T
+    return out, act_bits(out, act), h

@@ -182,3 +182,55 @@ def test_zero_tokens():
                         [(p, s, d, True) for p, s, d in c.fc2], 2)
     assert res["out"].shape == (0, c.H) and res["perm"].size == 0
     assert res["offsets"].tolist() == [0] * (c.E + 1)
+
+
+# ------------------------------------------------------------ dense MLP ---
+def _mlp_case(T=2, H=32, I=16, seed=41, act="bf16", awq=False):
+    r = synth.rng(seed)
+    fc1 = synth.quantize(synth.normal_weight(r, 2 * I, H))
+    fc2 = synth.quantize(synth.normal_weight(r, H, I))
+    x = synth.normal_act(r, (T, H), act)
+    pqs = synth.awq_scale_bits(r, H, act) if awq else None
+    return x, fc1, fc2, pqs
+
+
+@pytest.mark.parametrize("act,awq", [("bf16", False), ("f16", False), ("bf16", True)])
+def test_mlp_against_python_loops(act, awq):
+    """Every product and sum by hand: exact-rational weights, math.fsum dot
+    products, the SwiGLU and both roundings done element by element."""
+    T, H, I = 2, 32, 16
+    x_bits, fc1, fc2, pqs = _mlp_case(act=act, awq=awq)
+    out, out_bits, h_bits = moe.mlp(x_bits, (*fc1, True), (*fc2, True), pqs_bits=pqs, act=act)
+    w1 = _loop_dequant(*fc1, H, act)
+    w2 = _loop_dequant(*fc2, I, act)
+    for t in range(T):
+        xv = [_VALUE[act](int(b)) for b in x_bits[t]]
+        if awq:
+            xv = [_VALUE[act](_ROUND[act](v * _VALUE[act](int(s)))) for v, s in zip(xv, pqs)]
+        x = [float(v) for v in xv]
+        gate = [math.fsum(x[i] * w1[n][i] for i in range(H)) for n in range(I)]
+        up = [math.fsum(x[i] * w1[I + n][i] for i in range(H)) for n in range(I)]
+        h = [int(formats.act_bits(gate[n] / (1 + math.exp(-gate[n])) * up[n], act)) for n in range(I)]
+        assert h == [int(b) for b in h_bits[t]]
+        hv = [float(_VALUE[act](b)) for b in h]
+        y = [math.fsum(hv[n] * w2[o][n] for n in range(I)) for o in range(H)]
+        assert np.allclose(out[t], y, rtol=1e-12, atol=1e-12 * max(abs(v) for v in y))
+        assert np.array_equal(out_bits[t], formats.act_bits(np.array(y), act))
+
+
+def test_mlp_is_the_single_expert_layer():
+    x_bits, fc1, fc2, _ = _mlp_case(T=5, H=64, I=32, seed=43)
+    out, out_bits, _ = moe.mlp(x_bits, (*fc1, True), (*fc2, True))
+    logits = np.zeros((5, 1), dtype=np.float32)
+    res = moe.moe_layer(x_bits, logits, [(*fc1, True)], [(*fc2, True)], 1)
+    assert np.array_equal(res["out"], out) and np.array_equal(res["out_bits"], out_bits)
+
+
+def test_mlp_planted_gate_up_swap_is_caught():
+    x_bits, fc1, fc2, _ = _mlp_case(T=3, seed=44)
+    p, s, d = fc1
+    half = p.shape[0] // 2
+    swapped = (np.concatenate([p[half:], p[:half]]), np.concatenate([s[half:], s[:half]]), d, True)
+    a, _, _ = moe.mlp(x_bits, (*fc1, True), (*fc2, True))
+    b, _, _ = moe.mlp(x_bits, swapped, (*fc2, True))
+    assert np.linalg.norm(a - b) / np.linalg.norm(a) > 0.1

@@ -23,7 +23,8 @@ from . import _lib
 from ._lib import Nvfp4Error
 
 __all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "dequant", "gemm",
-           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "device_status",
+           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "mlp", "mlp_workspace_size",
+           "device_status",
            "abi_version"]
 
 
@@ -168,6 +169,36 @@ def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, o
         _ptr(workspace), ws_bytes, _stream()))
     if return_routing:
         return out, dict(idx=idx, p=wts, perm=perm, offsets=offs)
+    return out
+
+
+def mlp_workspace_size(T, H, I):
+    return int(_lib.load().nvfp4_w4a16_mlp_workspace(T, H, I))
+
+
+def mlp(x, fc1, fc2, fc1_pre_quant_scale=None, out=None, workspace=None):
+    """Dense gated MLP: out = FC2(RN(silu(g) * u)), [g; u] = FC1(x').
+    ``fc1``: NVFP4Weight [2I, H] (gate rows then up rows), ``fc2``: NVFP4Weight
+    [H, I]; x is BF16 or FP16 [T, H] and out has its type."""
+    h = _lib.load()
+    dt = _act_dtype(x, "x")
+    _require_cuda(x, "x", dt)
+    T, H = x.shape
+    I = fc1.N // 2
+    if fc1.K != H or fc1.N != 2 * I or fc2.N != H or fc2.K != I:
+        raise Nvfp4Error(2, f"fc1 must be [2I, {H}] and fc2 [{H}, I]; got {fc1.N}x{fc1.K} and {fc2.N}x{fc2.K}")
+    if fc1_pre_quant_scale is not None:
+        _require_cuda(fc1_pre_quant_scale, "fc1_pre_quant_scale", dt)
+    if out is None:
+        out = torch.empty((T, H), dtype=dt, device=x.device)
+    _require_cuda(out, "out", dt)
+    need = mlp_workspace_size(T, H, I)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    fn = h.nvfp4_w4a16_mlp_f16 if dt == torch.float16 else h.nvfp4_w4a16_mlp
+    _lib.check(fn(_ptr(x), _ptr(fc1.buf), _ptr(fc2.buf), _ptr(fc1_pre_quant_scale), T, H, I,
+                  _ptr(out), _ptr(workspace), ws_bytes, _stream()))
     return out
 
 

@@ -32,6 +32,9 @@ SIGNATURES = {
                                         c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_moe_grouped_f16": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
                                             c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "nvfp4_w4a16_mlp_workspace": (c_size, [c_i64, c_i64, c_i64]),
+    "nvfp4_w4a16_mlp": (c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
+    "nvfp4_w4a16_mlp_f16": (c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_moe_noalloc_scratch_bytes": (c_size, []),
     "nvfp4_w4a16_moe_grouped_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
                                                 c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),

@@ -143,10 +143,9 @@ extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, in
     return has_pre_quant_scale ? awq_bytes(M, K) : 0;
 }
 
-namespace {
-
-nvfp4_status gemm_impl(const void* X, const void* repacked, const void* pre_quant_scale, int64_t M, int64_t N,
-                       int64_t K, void* Y, void* workspace, size_t workspace_bytes, bool f16, void* stream) {
+nvfp4_status nvfp4::run_dense_gemm(const void* X, const void* repacked, const void* pre_quant_scale, int64_t M,
+                                   int64_t N, int64_t K, void* Y, void* workspace, size_t workspace_bytes, bool f16,
+                                   void* stream) {
     const char* fn = f16 ? "nvfp4_w4a16_gemm_f16" : "nvfp4_w4a16_gemm";
     if (M < 0 || N < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
     if (K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld must be a positive multiple of 16", fn, (long long)K);
@@ -190,16 +189,14 @@ nvfp4_status gemm_impl(const void* X, const void* repacked, const void* pre_quan
     return launch_decode(p, pl.MT, pl.ring, f16, s);
 }
 
-}  // namespace
-
 extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
                                          int64_t M, int64_t N, int64_t K, void* Y,
                                          void* workspace, size_t workspace_bytes, void* stream) {
-    return gemm_impl(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, false, stream);
+    return run_dense_gemm(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, false, stream);
 }
 
 extern "C" nvfp4_status nvfp4_w4a16_gemm_f16(const void* X, const void* repacked, const void* pre_quant_scale,
                                              int64_t M, int64_t N, int64_t K, void* Y,
                                              void* workspace, size_t workspace_bytes, void* stream) {
-    return gemm_impl(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, true, stream);
+    return run_dense_gemm(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, true, stream);
 }

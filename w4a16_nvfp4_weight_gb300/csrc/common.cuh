@@ -166,6 +166,12 @@ int* device_status_ptr();
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// The dense GEMM behind nvfp4_w4a16_gemm / nvfp4_w4a16_gemm_f16 (argument
+// checks, then the decode or the tile kernel), for layers built from it.
+nvfp4_status run_dense_gemm(const void* X, const void* repacked, const void* pre_quant_scale, int64_t M,
+                            int64_t N, int64_t K, void* Y, void* workspace, size_t workspace_bytes, bool f16,
+                            void* stream);
+
 // Kernels record the first error only.
 __device__ __forceinline__ void record_status(int* status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);

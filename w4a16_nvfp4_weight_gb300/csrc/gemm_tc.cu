@@ -59,7 +59,8 @@ struct TcKParams {
     size_t w_stride;          // MoE: bytes between experts
     uint16_t* Y;              // dense: [M, N] BF16; MoE FC1: H [rows, I] BF16
     float* Yp;                // MoE FC2: [slots, N] FP32, scaled by the routing weight
-    const int4* items;        // MoE: (expert, first row, rows, -) work list
+    const int4* items;        // MoE: (expert, first row, rows, -) work list; null with one
+                              //   dense weight: runs of 128*SUBM rows of M
     const int32_t* n_items;
     const int32_t* perm;      // MoE FC2: permuted row -> routing slot
     const float* wts;         // MoE FC2: routing weights per slot
@@ -106,8 +107,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     int64_t m0, m_end;
     const uint8_t* wbase = p.rp;
     if constexpr (kMoe) {
-        if ((int)blockIdx.y >= *p.n_items) return;      // uniform across the CTA
-        const int4 item = p.items[blockIdx.y];
+        int4 item;                                      // uniform across the CTA
+        if (p.items != nullptr) {
+            if ((int)blockIdx.y >= *p.n_items) return;
+            item = p.items[blockIdx.y];
+        } else {
+            // one dense weight (FC1 of a dense MLP): consecutive runs of token rows
+            const int64_t first = (int64_t)blockIdx.y * 128 * SUBM;
+            if (first >= p.M) return;
+            item = make_int4(0, (int)first, (int)(p.M - first < 128 * SUBM ? p.M - first : 128 * SUBM), 0);
+        }
         wbase = p.rp + (size_t)item.x * p.w_stride;
         m0 = item.y;
         m_end = (int64_t)item.y + item.z;
@@ -499,6 +508,7 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
 nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
     TcKParams kp{};
     kp.rp = m.w; kp.w_stride = m.w_stride; kp.items = m.items; kp.n_items = m.n_items;
+    kp.M = m.rows;
     kp.perm = m.perm; kp.wts = m.wts; kp.I = m.I; kp.status = m.status;
     kp.N = m.N; kp.K = m.K; kp.KB = round_up(m.K, kBlockK) / kBlockK;
     kp.kb_per_split = (int)kp.KB;

@@ -27,9 +27,10 @@ struct TcMoeParams {
     const uint8_t* w;         // stacked repacked experts
     size_t w_stride;
     int64_t N, K, I;          // weight rows (FC1: 2I), inner dimension, intermediate size
-    const int4* items;
+    const int4* items;        // null: one dense weight, items are runs of 128*subm rows
     const int32_t* n_items;
     int64_t max_items;
+    int64_t rows;             // dense use: token rows
     const int32_t* perm;
     const float* wts;
     uint16_t* H;              // FC1 output [x_rows, I]

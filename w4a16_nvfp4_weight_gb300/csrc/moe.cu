@@ -248,8 +248,9 @@ struct MoeLinParams {
     const uint16_t* X;         // gated: token activations [T, K]; else: H rows [T*k, K]
     const int32_t* perm;       // [T*k]
     int topk;
-    const int4* items;         // (expert, first permuted row, rows, -)
-    const int32_t* n_items;
+    const int4* items;         // (expert, first permuted row, rows, -); null: one dense
+    const int32_t* n_items;    //   weight and consecutive runs of TOK token rows
+    int64_t rows;              // dense use: token rows
     int64_t I;                 // gated: intermediate size (gate rows [0, I), up rows [I, 2I))
     uint16_t* H;               // gated output [T*k, I]
     float* Yp;                 // ungated output [T*k, N], scaled by the routing weight
@@ -285,8 +286,15 @@ moe_linear_kernel(const MoeLinParams p) {
     const int item_id = blockIdx.z;
     pdl_launch_dependents();
     pdl_wait_previous();                       // items and activations come from earlier kernels
-    if (item_id >= *p.n_items) return;         // the same for every CTA of the cluster
-    const int4 item = p.items[item_id];
+    int4 item;                                 // the same for every CTA of the cluster
+    if (p.items != nullptr) {
+        if (item_id >= *p.n_items) return;
+        item = p.items[item_id];
+    } else {
+        const int64_t first = (int64_t)item_id * TOK;
+        if (first >= p.rows) return;
+        item = make_int4(0, (int)first, (int)min((int64_t)TOK, p.rows - first), 0);
+    }
     const int e = item.x, r0 = item.y, nrows = item.z;
     const uint8_t* wexp = p.w + (size_t)e * p.w_stride;
 
@@ -339,7 +347,7 @@ moe_linear_kernel(const MoeLinParams p) {
                 const uint16_t* xrow[TOK];
                 for (int t = 0; t < nrows; ++t) {
                     const int64_t r = r0 + t;
-                    const int64_t src_row = GATED ? (int64_t)(p.perm[r] / p.topk) : r;
+                    const int64_t src_row = (GATED && p.perm) ? (int64_t)(p.perm[r] / p.topk) : r;
                     xrow[t] = p.X + src_row * p.K;
                 }
                 int issued = 0;
@@ -773,6 +781,110 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* 
                                                     void* workspace, size_t workspace_bytes, void* stream) {
     return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out, topk_idx_out,
                     topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, true, stream);
+}
+
+// ---------------------------------------------------------- dense MLP --
+// The gated MLP of a dense layer: h = RN(silu(g) * u) with [g; u] = FC1(x'),
+// out = RN(FC2(h)).  FC1 runs on the MoE FC1 kernels (SwiGLU fused into their
+// epilogue) with one expert and the token rows as the work items; FC2 is the
+// dense GEMM.
+namespace nvfp4 {
+namespace {
+
+struct MlpLayout {
+    size_t h, xs, gemm, total;
+};
+
+MlpLayout mlp_layout(int64_t T, int64_t H, int64_t I) {
+    MlpLayout L{};
+    L.h = 0;
+    L.xs = (size_t)round_up(T * I * 2, 256);
+    L.gemm = L.xs + (size_t)round_up(T * H * 2, 256);
+    L.total = L.gemm + (size_t)round_up((int64_t)nvfp4_w4a16_gemm_workspace(T, H, I, 0), 256);
+    return L;
+}
+
+// FC1 on the tile kernel when the dense shape rule picks tiles for [T, 2I]
+// and the gate/up halves are whole 128-row tiles; else the streaming kernel.
+bool mlp_fc1_tile(int64_t T, int64_t I) { return I % 128 == 0 && use_tc_path(T, 2 * I); }
+
+nvfp4_status mlp_impl(const void* X, const void* fc1, const void* fc2, const void* fc1_pre_quant_scale, int64_t T,
+                      int64_t H, int64_t I, void* out, void* workspace, size_t workspace_bytes, bool f16,
+                      void* stream) {
+    const char* fn = f16 ? "nvfp4_w4a16_mlp_f16" : "nvfp4_w4a16_mlp";
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
+    if (H <= 0 || I <= 0 || H % 64 != 0 || I % 64 != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: H=%lld and I=%lld must be positive multiples of 64", fn,
+                    (long long)H, (long long)I);
+    if (T == 0) return NVFP4_OK;                  // a zero-token chunk launches no kernel
+    if (!X || !fc1 || !fc2 || !out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(X, 16) || !aligned(out, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: X and out must be 16-byte aligned", fn);
+    if (!aligned(fc1, 256) || !aligned(fc2, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: weights must be 256-byte aligned", fn);
+    if (fc1_pre_quant_scale && !aligned(fc1_pre_quant_scale, 16))
+        return fail(NVFP4_ERR_ALIGNMENT, "%s: fc1_pre_quant_scale must be 16-byte aligned", fn);
+    const MlpLayout L = mlp_layout(T, H, I);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(NVFP4_ERR_WORKSPACE, "%s: workspace %zu bytes, needs %zu", fn, workspace_bytes, L.total);
+    if (!aligned(workspace, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: workspace must be 256-byte aligned", fn);
+    int* status = device_status_ptr();
+    if (!status) return fail(NVFP4_ERR_CUDA, "%s: no CUDA device", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = (uint8_t*)workspace;
+    uint16_t* hbuf = (uint16_t*)(ws + L.h);
+    nvfp4_status st;
+
+    const uint16_t* xin = (const uint16_t*)X;
+    if (fc1_pre_quant_scale) {
+        st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H,
+                              f16, s);
+        if (st != NVFP4_OK) return st;
+        xin = (const uint16_t*)(ws + L.xs);
+    }
+    if (mlp_fc1_tile(T, I)) {
+        TcMoeParams t1{};
+        t1.fc1 = true; t1.f16 = f16; t1.subm = T > 128 ? 2 : 1;
+        t1.X = xin; t1.x_rows = T; t1.w = (const uint8_t*)fc1; t1.w_stride = 0;
+        t1.N = 2 * I; t1.K = H; t1.I = I;
+        t1.items = nullptr; t1.n_items = nullptr; t1.max_items = ceil_div(T, 128 * t1.subm); t1.rows = T;
+        t1.H = hbuf; t1.status = status;
+        if ((st = launch_tc_moe(t1, s)) != NVFP4_OK) return st;
+    } else {
+        const int mt = T > 8 ? 2 : 1;
+        const int64_t items = ceil_div(T, 8 * mt);
+        if (items > 65535) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: T=%lld too large for one call", fn, (long long)T);
+        MoeLinParams p1{};
+        p1.w = (const uint8_t*)fc1; p1.w_stride = 0;
+        p1.N = 2 * I; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
+        p1.splits = moe_splits((I / 64) * items, p1.KB, 4);
+        p1.kbs = (int)ceil_div(p1.KB, p1.splits);
+        p1.splits = (int)ceil_div(p1.KB, p1.kbs);
+        p1.X = xin; p1.perm = nullptr; p1.topk = 1; p1.items = nullptr; p1.n_items = nullptr; p1.rows = T;
+        p1.I = I; p1.H = hbuf; p1.wts = nullptr; p1.status = status;
+        st = mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)items, f16, s)
+                     : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)items, f16, s);
+        if (st != NVFP4_OK) return st;
+    }
+    return run_dense_gemm(hbuf, fc2, nullptr, T, H, I, out, ws + L.gemm, workspace_bytes - L.gemm, f16, stream);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" size_t nvfp4_w4a16_mlp_workspace(int64_t T, int64_t H, int64_t I) {
+    if (T <= 0 || H <= 0 || I <= 0) return 0;
+    return nvfp4::mlp_layout(T, H, I).total;
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_mlp(const void* X, const void* fc1, const void* fc2,
+                                        const void* fc1_pre_quant_scale, int64_t T, int64_t H, int64_t I,
+                                        void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return nvfp4::mlp_impl(X, fc1, fc2, fc1_pre_quant_scale, T, H, I, out, workspace, workspace_bytes, false, stream);
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_mlp_f16(const void* X, const void* fc1, const void* fc2,
+                                            const void* fc1_pre_quant_scale, int64_t T, int64_t H, int64_t I,
+                                            void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return nvfp4::mlp_impl(X, fc1, fc2, fc1_pre_quant_scale, T, H, I, out, workspace, workspace_bytes, true, stream);
 }
 
 // ------------------------------------------------- allocation-free variant --
