@@ -78,6 +78,27 @@ def silu(v):
     return v / (1.0 + np.exp(-v))
 
 
+def relu2(v):
+    """Squared ReLU, max(v, 0)**2: the "relu2" activation of non-gated experts
+    (SGLang PR 40022, review thread: relu2 and silu non-gated experts)."""
+    r = np.maximum(v, 0.0)
+    return r * r
+
+
+ACTIVATIONS = ("swiglu", "relu2", "silu")
+
+
+def finalize_pre_quant_scale(w1_pqs_bits, w3_pqs_bits, act="bf16"):
+    """The layer's FC1 activation scale from per-expert AWQ pre-quant scales:
+    s[k] = max over experts e of max(w3_e[k], w1_e[k]) ("[None][fix] Apply the
+    NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL", Description, step 2: the
+    finalization writes max(w3, w1) into the [1, hidden] FC1 input scale).
+    Inputs uint16 [E, H] bit patterns of the activation type; returns uint16 [H]."""
+    a = act_to_float(np.asarray(w1_pqs_bits, dtype=np.uint16), act)
+    b = act_to_float(np.asarray(w3_pqs_bits, dtype=np.uint16), act)
+    return act_bits(np.maximum(a, b).max(axis=0), act)
+
+
 def expert_weights(fc, K, act="bf16"):
     """Dequantized weight values (float64) of one expert matrix, rounded to the
     activation type.
@@ -88,12 +109,36 @@ def expert_weights(fc, K, act="bf16"):
     return act_to_float(dequant(packed, scales, gs, is_div, K, act), act)
 
 
-def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="bf16"):
+def _fc1_out(x, fc1_e, H, act, activation, fc1_split):
+    """h (bit patterns) of one expert for the rows x (float64), and I."""
+    if activation == "swiglu":
+        if fc1_split:      # gate and up quantized separately, each with its own global
+            w1 = np.concatenate([expert_weights(fc1_e[0], H, act), expert_weights(fc1_e[1], H, act)])
+        else:
+            w1 = expert_weights(fc1_e, H, act)
+        I = w1.shape[0] // 2
+        gu = x @ w1.T
+        return act_bits(silu(gu[:, :I]) * gu[:, I:], act)
+    w1 = expert_weights(fc1_e, H, act)                  # non-gated: [I, H]
+    v = x @ w1.T
+    if activation == "relu2":
+        return act_bits(relu2(v), act)
+    if activation == "silu":
+        return act_bits(silu(v), act)
+    raise ValueError(f"unknown activation {activation!r}")
+
+
+def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="bf16", activation="swiglu",
+              fc1_split=False):
     """The whole layer.
 
     x_bits  uint16 [T, H] activations (BF16, or FP16 with act="f16")
     logits  float32 [T, E] router logits
-    fc1     list of E tuples (packed [2I, H/2], scales [2I, H/16], global, is_divisor)
+    fc1     list of E tuples (packed [2I, H/2], scales [2I, H/16], global, is_divisor);
+            with fc1_split, E pairs (gate tuple [I, H], up tuple [I, H]), each
+            with its own global (per-shard w1/w3 globals, SGLang PR 40022,
+            review thread: per-shard global/input scales); with a non-gated
+            activation ("relu2" or "silu"), E tuples of [I, H]
     fc2     list of E tuples (packed [H, I/2], scales [H, I/16], global, is_divisor)
     tokens  optional subset of token indices whose outputs are computed
             (routing and permutation tables are always computed for all T)
@@ -120,17 +165,17 @@ def moe_layer(x_bits, logits, fc1, fc2, topk, pqs_bits=None, tokens=None, act="b
     if pqs_bits is not None:
         xs = awq_scale_activation(xs, pqs_bits, act)
     x = act_to_float(xs, act)
-    I = np.asarray(fc1[0][0]).shape[0] // 2
+    if activation == "swiglu":
+        I = np.asarray(fc1[0][0][0] if fc1_split else fc1[0][0]).shape[0] // (1 if fc1_split else 2)
+    else:
+        I = np.asarray(fc1[0][0]).shape[0]
     y = np.zeros((tokens.size, topk, H))
     h_all = np.zeros((tokens.size, topk, I), dtype=np.uint16)
     sel = idx[tokens]                                   # [T', topk]
     for e in np.unique(sel):
         rows, slots = np.nonzero(sel == e)
-        w1 = expert_weights(fc1[e], H, act)             # [2I, H]
         w2 = expert_weights(fc2[e], I, act)             # [H, I]
-        gu = x[rows] @ w1.T                             # [r, 2I]
-        gate, up = gu[:, :I], gu[:, I:]
-        h = act_bits(silu(gate) * up, act)              # [r, I]
+        h = _fc1_out(x[rows], fc1[e], H, act, activation, fc1_split)   # [r, I]
         h_all[rows, slots] = h
         y[rows, slots] = act_to_float(h, act) @ w2.T    # [r, H]
     out = np.zeros((tokens.size, H))

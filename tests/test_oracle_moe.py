@@ -234,3 +234,105 @@ def test_mlp_planted_gate_up_swap_is_caught():
     a, _, _ = moe.mlp(x_bits, (*fc1, True), (*fc2, True))
     b, _, _ = moe.mlp(x_bits, swapped, (*fc2, True))
     assert np.linalg.norm(a - b) / np.linalg.norm(a) > 0.1
+
+
+# ------------------------------------------------------------ MoE variants ---
+def test_relu2_against_exact():
+    from fractions import Fraction
+    r = np.random.default_rng(3)
+    v = r.standard_normal(200) * 3
+    got = moe.relu2(v)
+    for a, b in zip(v, got):
+        want = Fraction(float(a)) ** 2 if a > 0 else Fraction(0)
+        assert abs(Fraction(float(b)) - want) <= want * Fraction(1, 2 ** 52)
+    assert moe.relu2(np.array([-0.0, 0.0, -5.0]))[2] == 0.0
+
+
+def _variant_layer(activation, split=False, T=3, E=4, topk=2, H=32, I=16, seed=51, act="bf16"):
+    r = synth.rng(seed)
+    fc1, fc2 = [], []
+    for _ in range(E):
+        if activation == "swiglu" and split:
+            fc1.append((synth.quantize(synth.normal_weight(r, I, H)), synth.quantize(synth.normal_weight(r, I, H))))
+        elif activation == "swiglu":
+            fc1.append(synth.quantize(synth.normal_weight(r, 2 * I, H)))
+        else:
+            fc1.append(synth.quantize(synth.normal_weight(r, I, H)))
+        fc2.append(synth.quantize(synth.normal_weight(r, H, I)))
+    c = synth.moe_case(T, seed, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), act=act)
+    return c, fc1, fc2
+
+
+@pytest.mark.parametrize("activation", ["relu2", "silu"])
+def test_non_gated_layer_against_python_loops(activation):
+    c, fc1, fc2 = _variant_layer(activation)
+    T, E, k, H, I = c.T, c.E, c.topk, c.H, c.I
+    res = moe.moe_layer(c.x_bits, c.logits, [(p, s, d, True) for p, s, d in fc1],
+                        [(p, s, d, True) for p, s, d in fc2], k, activation=activation)
+    w1 = [_loop_dequant(p, s, d, H) for p, s, d in fc1]
+    w2 = [_loop_dequant(p, s, d, I) for p, s, d in fc2]
+    for t in range(T):
+        order = res["idx"][t].tolist()
+        pw = res["p"][t]
+        x = [float(bf16_exact(int(b))) for b in c.x_bits[t]]
+        acc = [0.0] * H
+        for j, e in enumerate(order):
+            v = [math.fsum(x[i] * w1[e][n][i] for i in range(H)) for n in range(I)]
+            a = [max(u, 0.0) ** 2 if activation == "relu2" else u / (1 + math.exp(-u)) for u in v]
+            h = [float(bf16_exact(int(formats.bf16_bits(u)))) for u in a]
+            for o in range(H):
+                acc[o] += pw[j] * math.fsum(h[n] * w2[e][o][n] for n in range(I))
+        ref = np.array(acc)
+        assert np.allclose(res["out"][t], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+        assert np.array_equal(res["out_bits"][t], formats.bf16_bits(ref))
+
+
+def test_split_gate_up_with_equal_globals_is_the_fused_layer():
+    """Gate and up quantized with one shared divisor and stored as two shards give
+    exactly the fused [2I, H] layer."""
+    c, fc1, fc2 = _variant_layer("swiglu", seed=52)
+    I = c.I
+    split = [((p[:I], s[:I], d, True), (p[I:], s[I:], d, True)) for p, s, d in fc1]
+    fused = moe.moe_layer(c.x_bits, c.logits, [(p, s, d, True) for p, s, d in fc1],
+                          [(p, s, d, True) for p, s, d in fc2], c.topk)
+    shards = moe.moe_layer(c.x_bits, c.logits, split, [(p, s, d, True) for p, s, d in fc2], c.topk, fc1_split=True)
+    assert np.array_equal(fused["out_bits"], shards["out_bits"])
+
+
+def test_split_gate_up_own_globals_against_python_loops():
+    c, fc1, fc2 = _variant_layer("swiglu", split=True, seed=53)
+    T, k, H, I = c.T, c.topk, c.H, c.I
+    res = moe.moe_layer(c.x_bits, c.logits, [((gp, gs, gd, True), (up, us, ud, True)) for (gp, gs, gd), (up, us, ud) in fc1],
+                        [(p, s, d, True) for p, s, d in fc2], k, fc1_split=True)
+    assert any(g[2] != u[2] for g, u in fc1)                    # the shards' globals differ
+    for t in range(T):
+        order = res["idx"][t].tolist()
+        x = [float(bf16_exact(int(b))) for b in c.x_bits[t]]
+        acc = [0.0] * H
+        for j, e in enumerate(order):
+            wg = _loop_dequant(*fc1[e][0], H)
+            wu = _loop_dequant(*fc1[e][1], H)
+            w2 = _loop_dequant(*fc2[e], I)
+            gate = [math.fsum(x[i] * wg[n][i] for i in range(H)) for n in range(I)]
+            up = [math.fsum(x[i] * wu[n][i] for i in range(H)) for n in range(I)]
+            h = [float(bf16_exact(int(formats.bf16_bits(gate[n] / (1 + math.exp(-gate[n])) * up[n])))) for n in range(I)]
+            for o in range(H):
+                acc[o] += res["p"][t][j] * math.fsum(h[n] * w2[o][n] for n in range(I))
+        ref = np.array(acc)
+        assert np.array_equal(res["out_bits"][t], formats.bf16_bits(ref))
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_finalize_pre_quant_scale(act):
+    r = synth.rng(61)
+    E, H = 5, 48
+    w1 = np.stack([synth.awq_scale_bits(r, H, act) for _ in range(E)])
+    w3 = np.stack([synth.awq_scale_bits(r, H, act) for _ in range(E)])
+    got = moe.finalize_pre_quant_scale(w1, w3, act)
+    val = _VALUE[act]
+    for k in range(H):
+        best = max([val(int(w1[e, k])) for e in range(E)] + [val(int(w3[e, k])) for e in range(E)])
+        assert val(int(got[k])) == best
+    # one expert: the elementwise max(w3, w1)
+    one = moe.finalize_pre_quant_scale(w1[:1], w3[:1], act)
+    assert all(val(int(one[k])) == max(val(int(w1[0, k])), val(int(w3[0, k]))) for k in range(H))
