@@ -229,6 +229,44 @@ nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* router_logi
                                          int32_t* perm_out, int32_t* offsets_out,
                                          void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * MoE layer variants.  activation: the expert type -- NVFP4_MOE_SWIGLU (gated:
+ * h = RN(silu(g) * u), the default of nvfp4_w4a16_moe_grouped), NVFP4_MOE_RELU2
+ * (non-gated: h = RN(max(v, 0)^2)) or NVFP4_MOE_SILU (non-gated: h =
+ * RN(silu(v))), v = FC1_e(x'); non-gated experts have fc1 = E repacked [I, H]
+ * weights, expert e at fc1 + e * nvfp4_repack_size(I, H) (SGLang PR 40022,
+ * review thread: relu2 and silu non-gated experts).  fc1_split = 1 (gated
+ * only): the gate and up projections were quantized separately, each with its
+ * own global scale (per-shard w1/w3 globals, same thread), and are repacked
+ * separately as two [I, H] weights: expert e's gate at fc1 + e * 2 * S and its
+ * up projection at fc1 + (2e + 1) * S, S = nvfp4_repack_size(I, H).  f16 = 1
+ * for FP16 activations.  Everything else as nvfp4_w4a16_moe_grouped; the
+ * workspace size is the same.
+ */
+typedef enum { NVFP4_MOE_SWIGLU = 0, NVFP4_MOE_RELU2 = 1, NVFP4_MOE_SILU = 2 } nvfp4_moe_activation;
+
+nvfp4_status nvfp4_w4a16_moe_grouped_ex(const void* X, const float* router_logits,
+                                        const void* fc1, const void* fc2,
+                                        const void* fc1_pre_quant_scale,
+                                        int64_t T, int E, int topk, int64_t H, int64_t I,
+                                        int activation, int fc1_split, int f16,
+                                        void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                        int32_t* perm_out, int32_t* offsets_out,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The layer's FC1 activation scale from per-expert AWQ pre-quant scales (a
+ * load-time step): out[k] = max over experts e of max(w3_e[k], w1_e[k])
+ * ("[None][fix] Apply the NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL",
+ * Description: the finalization writes max(w3, w1) into the [1, hidden] FC1
+ * input scale).  w1_pre_quant_scale, w3_pre_quant_scale: device [E, H] BF16
+ * (FP16 when f16 = 1); out: device [H], the fc1_pre_quant_scale of the MoE
+ * calls.  NaN entries are ignored by the max.
+ */
+nvfp4_status nvfp4_moe_finalize_pre_quant_scale(const void* w1_pre_quant_scale,
+                                                const void* w3_pre_quant_scale, int E, int64_t H,
+                                                int f16, void* out, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Dense gated MLP (FC1 gate/up + SwiGLU, FC2)                               */
 /* ------------------------------------------------------------------------ */

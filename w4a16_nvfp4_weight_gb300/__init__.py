@@ -23,7 +23,8 @@ from . import _lib
 from ._lib import Nvfp4Error
 
 __all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "dequant", "gemm",
-           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "mlp", "mlp_workspace_size",
+           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "moe_finalize_pre_quant_scale",
+           "mlp", "mlp_workspace_size",
            "device_status",
            "abi_version"]
 
@@ -135,11 +136,17 @@ def moe_workspace_size(T, E, topk, H, I):
     return int(_lib.load().nvfp4_w4a16_moe_workspace(T, E, topk, H, I))
 
 
+MOE_ACTIVATIONS = {"swiglu": 0, "relu2": 1, "silu": 2}
+
+
 def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, out=None,
-                return_routing=False, workspace=None):
+                return_routing=False, workspace=None, activation="swiglu", fc1_split=False):
     """Top-k MoE layer.  ``fc1``/``fc2``: uint8 device buffers holding E repacked
     expert weights back to back ([2I, H] and [H, I] each).  x is BF16 or FP16;
-    out and fc1_pre_quant_scale have its type."""
+    out and fc1_pre_quant_scale have its type.  ``activation`` "relu2" or
+    "silu": non-gated experts, fc1 holds E repacked [I, H] weights.
+    ``fc1_split``: gated experts whose gate and up projections are repacked
+    separately (each with its own global), gate then up per expert."""
     h = _lib.load()
     dt = _act_dtype(x, "x")
     _require_cuda(x, "x", dt)
@@ -162,13 +169,39 @@ def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, o
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    fn = h.nvfp4_w4a16_moe_grouped_f16 if dt == torch.float16 else h.nvfp4_w4a16_moe_grouped
-    _lib.check(fn(
-        _ptr(x), _ptr(router_logits), _ptr(fc1), _ptr(fc2), _ptr(fc1_pre_quant_scale),
-        T, E, topk, H, I, _ptr(out), _ptr(idx), _ptr(wts), _ptr(perm), _ptr(offs),
-        _ptr(workspace), ws_bytes, _stream()))
+    if activation not in MOE_ACTIVATIONS:
+        raise Nvfp4Error(1, f"activation must be one of {sorted(MOE_ACTIVATIONS)}")
+    if activation != "swiglu" or fc1_split:
+        _lib.check(h.nvfp4_w4a16_moe_grouped_ex(
+            _ptr(x), _ptr(router_logits), _ptr(fc1), _ptr(fc2), _ptr(fc1_pre_quant_scale),
+            T, E, topk, H, I, MOE_ACTIVATIONS[activation], 1 if fc1_split else 0,
+            1 if dt == torch.float16 else 0, _ptr(out), _ptr(idx), _ptr(wts), _ptr(perm), _ptr(offs),
+            _ptr(workspace), ws_bytes, _stream()))
+    else:
+        fn = h.nvfp4_w4a16_moe_grouped_f16 if dt == torch.float16 else h.nvfp4_w4a16_moe_grouped
+        _lib.check(fn(
+            _ptr(x), _ptr(router_logits), _ptr(fc1), _ptr(fc2), _ptr(fc1_pre_quant_scale),
+            T, E, topk, H, I, _ptr(out), _ptr(idx), _ptr(wts), _ptr(perm), _ptr(offs),
+            _ptr(workspace), ws_bytes, _stream()))
     if return_routing:
         return out, dict(idx=idx, p=wts, perm=perm, offsets=offs)
+    return out
+
+
+def moe_finalize_pre_quant_scale(w1_pre_quant_scale, w3_pre_quant_scale, out=None):
+    """[H] FC1 activation scale = max over experts of max(w3_e, w1_e); inputs [E, H]
+    BF16 or FP16 (same type), the output has their type."""
+    h = _lib.load()
+    dt = _act_dtype(w1_pre_quant_scale, "w1_pre_quant_scale")
+    _require_cuda(w1_pre_quant_scale, "w1_pre_quant_scale", dt)
+    _require_cuda(w3_pre_quant_scale, "w3_pre_quant_scale", dt)
+    if w1_pre_quant_scale.shape != w3_pre_quant_scale.shape or w1_pre_quant_scale.dim() != 2:
+        raise Nvfp4Error(2, "w1/w3 pre-quant scales must both be [E, H]")
+    E, H = w1_pre_quant_scale.shape
+    if out is None:
+        out = torch.empty(H, dtype=dt, device=w1_pre_quant_scale.device)
+    _lib.check(h.nvfp4_moe_finalize_pre_quant_scale(_ptr(w1_pre_quant_scale), _ptr(w3_pre_quant_scale), E, H,
+                                                    1 if dt == torch.float16 else 0, _ptr(out), _stream()))
     return out
 
 

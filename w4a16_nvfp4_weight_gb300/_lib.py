@@ -32,6 +32,10 @@ SIGNATURES = {
                                         c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_moe_grouped_f16": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
                                             c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "nvfp4_w4a16_moe_grouped_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,
+                                           c_i64, c_int, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                           c_size, c_vp]),
+    "nvfp4_moe_finalize_pre_quant_scale": (c_int, [c_vp, c_vp, c_int, c_i64, c_int, c_vp, c_vp]),
     "nvfp4_w4a16_mlp_workspace": (c_size, [c_i64, c_i64, c_i64]),
     "nvfp4_w4a16_mlp": (c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_mlp_f16": (c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),

@@ -46,13 +46,15 @@ struct TcSmem {
     static constexpr size_t a = 0;                                            // 1024-aligned
     static constexpr size_t bdeq = a + (size_t)kS1 * SUBM * kATileBytes;      // 1024-aligned
     static constexpr size_t braw = bdeq + (size_t)kS2 * kBDeqBytes;
-    static constexpr size_t lut = braw + (size_t)kS1 * kBRawBytes;
-    static constexpr size_t bars = lut + kLutBytes;
+    static constexpr size_t lut = braw + (size_t)kS1 * kBRawBytes;          // + a second table
+    static constexpr size_t bars = lut + 2 * kLutBytes;                      //   for gate/up shards
     static constexpr size_t misc = bars + 16 * 8;
     static constexpr size_t total = misc + 64;
 };
 
-enum class TcMode { kDense, kMoeFc1, kMoeFc2 };
+// kMoeFc1: gated FC1 (gate/up + SwiGLU -> H); kMoeFc1Plain: non-gated FC1
+// (relu2 or silu -> H); kMoeFc2: x p -> FP32 rows per routing slot.
+enum class TcMode { kDense, kMoeFc1, kMoeFc1Plain, kMoeFc2 };
 
 struct TcKParams {
     const uint8_t* rp;        // dense: the repacked weight; MoE: expert 0 of the stacked weights
@@ -66,6 +68,9 @@ struct TcKParams {
     const float* wts;         // MoE FC2: routing weights per slot
     int64_t M, N, K, KB;      // dense M; weight rows N (FC1: 2I) and inner K
     int64_t I;                // MoE FC1: intermediate size
+    size_t half_stride;       // gated FC1: 0 = one [2I, K] weight, else bytes from the gate
+                              //   shard [I, K] to the up shard [I, K] (own globals)
+    int act;                  // non-gated FC1: 1 = relu2, 2 = silu
     int kb_per_split;         // dense split-K: 64-k blocks per split (grid z = split)
     float* partial;           // dense split-K: FP32 partials [splits, M, N], or null
     int* status;
@@ -78,6 +83,14 @@ __device__ __forceinline__ uint32_t sw128_offset(int n, int c) {
 }
 
 __device__ __forceinline__ float silu_tc(float v) { return v / (1.0f + expf(-v)); }
+
+__device__ __forceinline__ float plain_act_tc(float v, int act) {
+    if (act == 1) {
+        const float r = fmaxf(v, 0.0f);
+        return r * r;
+    }
+    return silu_tc(v);
+}
 
 template <int SUBM, TcMode MODE, bool F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -125,6 +138,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
         m_end = p.M;
     }
     const int64_t n0 = (int64_t)blockIdx.x * (MODE == TcMode::kMoeFc1 ? kBN / 2 : kBN);
+    const bool shards = MODE == TcMode::kMoeFc1 && p.half_stride != 0;
+    const uint8_t* wbase_up = shards ? wbase + p.half_stride : wbase;
     // dense split-K: this CTA covers 64-k blocks [kb_first, kb_first + nkb)
     const int kb_first = kMoe ? 0 : (int)blockIdx.z * p.kb_per_split;
     const int64_t kb_left = p.KB - kb_first;
@@ -157,22 +172,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const Header* hdr = reinterpret_cast<const Header*>(wbase);
-            const bool ok_hdr = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            const Header* hdr_up = reinterpret_cast<const Header*>(wbase_up);
+            const bool ok_hdr = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K &&
+                                (!shards || (hdr_up->magic == kMagic && hdr_up->N == p.N && hdr_up->K == p.K));
             *hdr_flag = ok_hdr ? 1 : 0;
             if (!ok_hdr) {
                 record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
                 mbar_arrive(lut_bar);
             } else {
-                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)((shards ? 2 : 1) * kLutBytes));
                 bulk_g2s(lut, wbase + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
-                // FC1: 128 gate rows j0.. and the 128 matching up rows I + j0.. (two
-                // half tiles); otherwise one 256-row tile
-                auto half_tile = [&](int64_t row0) {
+                if (shards) bulk_g2s(lut + 256, wbase_up + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
+                // FC1: 128 gate rows j0.. and the 128 matching up rows (I + j0.. of the
+                // same weight, or j0.. of the up shard): two half tiles; otherwise one
+                // 256-row tile
+                auto half_tile = [&](const uint8_t* base, int64_t row0) {
                     const int64_t rbg = row0 / kAtomRows;
-                    return wbase + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, 0, rbg % kAtomsPerTileK, p.KB);
+                    return base + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, 0, rbg % kAtomsPerTileK, p.KB);
                 };
-                const uint8_t* wtile = half_tile(n0);
-                const uint8_t* wtile_up = MODE == TcMode::kMoeFc1 ? half_tile(p.I + n0) : nullptr;
+                const uint8_t* wtile = half_tile(wbase, n0);
+                const uint8_t* wtile_up =
+                    MODE == TcMode::kMoeFc1 ? half_tile(wbase_up, (shards ? 0 : p.I) + n0) : nullptr;
                 int issued = 0;
                 for (int kb = 0; kb < nkb; ++kb) {
                     const int s = kb % kS1;
@@ -227,6 +247,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
         // ------------------------------------------------ dequant, then epilogue
         const int dw = warp - 2;                        // 0..7: atoms 2dw, 2dw+1 of each block
         const int r = lane >> 2, q = lane & 3;
+        const uint4* const dlut = (shards && dw >= 4) ? lut + 256 : lut;     // rows 128.. are up rows
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
         for (int kb = 0; kb < nkb && ok; ++kb) {
             const int s1 = kb % kS1, s2 = kb % kS2;
@@ -241,8 +262,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 const uint8_t* a = raw + atom * kAtomBytes;
                 const uint4 codes = *reinterpret_cast<const uint4*>(a + 16 * lane);
                 const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(a + kAtomCodeBytes + 2 * lane);
-                const Lut t0 = lut_from_uint4(lut[sc2 & 0xFF]);
-                const Lut t1 = lut_from_uint4(lut[(sc2 >> 8) & 0xFF]);
+                const Lut t0 = lut_from_uint4(dlut[sc2 & 0xFF]);
+                const Lut t1 = lut_from_uint4(dlut[(sc2 >> 8) & 0xFF]);
                 uint32_t e0[8], e1[8];
                 expand8(codes.x, t0, e0);
                 expand8(codes.y, t0, e0 + 4);
@@ -325,6 +346,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                             packed[i] = (uint32_t)f32_to_act_bits<F16>(h0) | ((uint32_t)f32_to_act_bits<F16>(h1) << 16);
                         }
                         uint16_t* hrow = p.Y + m * p.I + n0 + col;      // I and n0 are multiples of 64
+                        *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        *reinterpret_cast<uint4*>(hrow + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                } else if constexpr (MODE == TcMode::kMoeFc1Plain) {
+                    // h = RN(act(v)) for 128 of the tile's 256 columns (N = I, a multiple of 64)
+                    #pragma unroll 1
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const int col = half * 128 + c16 * 16;
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(trow + col, v);
+                        tmem_ld_wait();
+                        const int64_t n = n0 + col;
+                        if (m >= m_end || n >= p.N) continue;
+                        uint32_t packed[8];
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float h0 = plain_act_tc(__uint_as_float(v[2 * i]), p.act);
+                            const float h1 = plain_act_tc(__uint_as_float(v[2 * i + 1]), p.act);
+                            packed[i] = (uint32_t)f32_to_act_bits<F16>(h0) | ((uint32_t)f32_to_act_bits<F16>(h1) << 16);
+                        }
+                        uint16_t* hrow = p.Y + m * p.N + n;
                         *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         *reinterpret_cast<uint4*>(hrow + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
                     }
@@ -508,19 +550,21 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
 nvfp4_status launch_tc_moe(const TcMoeParams& m, cudaStream_t stream) {
     TcKParams kp{};
     kp.rp = m.w; kp.w_stride = m.w_stride; kp.items = m.items; kp.n_items = m.n_items;
-    kp.M = m.rows;
+    kp.M = m.rows; kp.half_stride = m.half_stride; kp.act = m.act;
     kp.perm = m.perm; kp.wts = m.wts; kp.I = m.I; kp.status = m.status;
     kp.N = m.N; kp.K = m.K; kp.KB = round_up(m.K, kBlockK) / kBlockK;
     kp.kb_per_split = (int)kp.KB;
-    const bool fc1 = m.fc1;
+    const bool gated_fc1 = m.fc1 && m.act == 0, plain_fc1 = m.fc1 && m.act != 0;
     kp.Y = m.H; kp.Yp = m.Yp;
-    const unsigned gx = fc1 ? (unsigned)(m.I / 128) : (unsigned)ceil_div(m.N, kBN);
+    const unsigned gx = gated_fc1 ? (unsigned)(m.I / 128) : (unsigned)ceil_div(m.N, kBN);
     const dim3 grid(gx, (unsigned)m.max_items);
     if (m.subm == 1)
-        return fc1 ? launch_tc_impl<1, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
-                   : launch_tc_impl<1, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
-    return fc1 ? launch_tc_impl<2, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
-               : launch_tc_impl<2, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
+        return gated_fc1 ? launch_tc_impl<1, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
+             : plain_fc1 ? launch_tc_impl<1, TcMode::kMoeFc1Plain>(m.X, m.x_rows, kp, grid, m.f16, stream)
+                         : launch_tc_impl<1, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
+    return gated_fc1 ? launch_tc_impl<2, TcMode::kMoeFc1>(m.X, m.x_rows, kp, grid, m.f16, stream)
+         : plain_fc1 ? launch_tc_impl<2, TcMode::kMoeFc1Plain>(m.X, m.x_rows, kp, grid, m.f16, stream)
+                     : launch_tc_impl<2, TcMode::kMoeFc2>(m.X, m.x_rows, kp, grid, m.f16, stream);
 }
 
 }  // namespace nvfp4

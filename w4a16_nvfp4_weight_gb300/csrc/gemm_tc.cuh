@@ -19,14 +19,16 @@ struct TcParams {
 // Grouped MoE use of the tile kernel: work items of up to 128*subm permuted
 // rows of one expert; X rows are already in permuted (expert-contiguous) order.
 struct TcMoeParams {
-    bool fc1;                 // FC1 (gate/up + SwiGLU -> H) or FC2 (x p -> Yp)
+    bool fc1;                 // FC1 (-> H) or FC2 (x p -> Yp)
+    int act;                  // FC1: 0 = gated (gate/up + SwiGLU), 1 = relu2, 2 = silu (non-gated)
+    size_t half_stride;       // gated FC1: 0, or bytes from the gate shard to the up shard
     bool f16;                 // FP16 activations (else BF16)
     int subm;                 // 1 or 2: 128 or 256 rows per work item
     const uint16_t* X;        // [x_rows, K] BF16 or FP16, permuted rows
     int64_t x_rows;
     const uint8_t* w;         // stacked repacked experts
     size_t w_stride;
-    int64_t N, K, I;          // weight rows (FC1: 2I), inner dimension, intermediate size
+    int64_t N, K, I;          // weight rows (gated FC1: 2I, or I per shard), inner dimension, intermediate size
     const int4* items;        // null: one dense weight, items are runs of 128*subm rows
     const int32_t* n_items;
     int64_t max_items;

@@ -252,13 +252,25 @@ struct MoeLinParams {
     const int32_t* n_items;    //   weight and consecutive runs of TOK token rows
     int64_t rows;              // dense use: token rows
     int64_t I;                 // gated: intermediate size (gate rows [0, I), up rows [I, 2I))
-    uint16_t* H;               // gated output [T*k, I]
-    float* Yp;                 // ungated output [T*k, N], scaled by the routing weight
+    size_t half_stride;        // gated: 0 = one [2I, K] weight; else bytes from the gate
+                               //   shard [I, K] to the up shard [I, K] (own globals)
+    int act;                   // ungated: 0 = FC2 (x p -> Yp); 1 relu2 / 2 silu FC1 -> H
+    uint16_t* H;               // gated (and non-gated FC1) output [T*k, I]
+    float* Yp;                 // FC2 output [T*k, N], scaled by the routing weight
     const float* wts;          // [T*k] routing weights
     int* status;
 };
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+
+// Activation of a non-gated expert: 1 = squared ReLU, 2 = SiLU.
+__device__ __forceinline__ float plain_act(float v, int act) {
+    if (act == 1) {
+        const float r = fmaxf(v, 0.0f);
+        return r * r;
+    }
+    return silu_f(v);
+}
 
 template <int MT, bool GATED, bool F16>
 __global__ void __launch_bounds__(kThreads)
@@ -275,8 +287,10 @@ moe_linear_kernel(const MoeLinParams p) {
     uint64_t* empty = full + kStages;
     uint64_t* lut_bar = empty + kStages;
     volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + 120);
+    // magnitude tables: one, or two with gate/up shards (gate first)
+    const bool shards = GATED && p.half_stride != 0;
     uint4* lut = reinterpret_cast<uint4*>(smem + kRingOffset);
-    uint8_t* ring = smem + kRingOffset + kLutBytes;
+    uint8_t* ring = smem + kRingOffset + (shards ? 2 : 1) * kLutBytes;
     float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -305,10 +319,11 @@ moe_linear_kernel(const MoeLinParams p) {
     // weight rows of this CTA: gated -> 64 gate rows + the 64 matching up rows
     // (two runs of four atoms); ungated -> 128 consecutive rows (one run of eight)
     const int64_t row_a = GATED ? (int64_t)cgi * 64 : (int64_t)cgi * 128;
-    const int64_t row_b = GATED ? p.I + (int64_t)cgi * 64 : 0;
-    auto atom_src = [&](int64_t row0, int kb) {
+    const int64_t row_b = GATED ? (shards ? 0 : p.I) + (int64_t)cgi * 64 : 0;
+    const uint8_t* wup = shards ? wexp + p.half_stride : wexp;      // where the up rows live
+    auto atom_src = [&](const uint8_t* base, int64_t row0, int kb) {
         const int64_t rbg = row0 / kAtomRows;
-        return wexp + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, kb, rbg % kAtomsPerTileK, p.KB);
+        return base + kTilesOffset + atom_offset(rbg / kAtomsPerTileK, kb, rbg % kAtomsPerTileK, p.KB);
     };
 
     if (tid == 0) {
@@ -335,19 +350,24 @@ moe_linear_kernel(const MoeLinParams p) {
     if (warp == kWarps) {
         if (lane == 0) {
             const Header* hdr = reinterpret_cast<const Header*>(wexp);
-            const bool hdr_ok = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            const Header* hdr_up = reinterpret_cast<const Header*>(wup);
+            const bool hdr_ok = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K &&
+                                (!shards || (hdr_up->magic == kMagic && hdr_up->N == p.N && hdr_up->K == p.K));
             *hdr_flag = hdr_ok ? 1 : 0;
             if (!hdr_ok) {
                 record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
                 mbar_arrive(lut_bar);
             } else {
-                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)((shards ? 2 : 1) * kLutBytes));
                 bulk_g2s(lut, wexp + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
-                // activation row of each of this item's routed rows
+                if (shards) bulk_g2s(lut + 256, wup + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
+                // activation row of each of this item's routed rows (FC1 reads token
+                // rows through the permutation, FC2 the permuted rows of H)
+                const bool token_rows = (GATED || p.act != 0) && p.perm != nullptr;
                 const uint16_t* xrow[TOK];
                 for (int t = 0; t < nrows; ++t) {
                     const int64_t r = r0 + t;
-                    const int64_t src_row = (GATED && p.perm) ? (int64_t)(p.perm[r] / p.topk) : r;
+                    const int64_t src_row = token_rows ? (int64_t)(p.perm[r] / p.topk) : r;
                     xrow[t] = p.X + src_row * p.K;
                 }
                 int issued = 0;
@@ -365,10 +385,11 @@ moe_linear_kernel(const MoeLinParams p) {
                     for (int b = 0; b < nb; ++b) {
                         const int kb = kb0 + i * kBlocksPerStage + b;
                         if (GATED) {
-                            bulk_g2s(st + b * kBlockBytes, atom_src(row_a, kb), kBlockBytes / 2, &full[s]);
-                            bulk_g2s(st + b * kBlockBytes + kBlockBytes / 2, atom_src(row_b, kb), kBlockBytes / 2, &full[s]);
+                            bulk_g2s(st + b * kBlockBytes, atom_src(wexp, row_a, kb), kBlockBytes / 2, &full[s]);
+                            bulk_g2s(st + b * kBlockBytes + kBlockBytes / 2, atom_src(wup, row_b, kb), kBlockBytes / 2,
+                                     &full[s]);
                         } else {
-                            bulk_g2s(st + b * kBlockBytes, atom_src(row_a, kb), kBlockBytes, &full[s]);
+                            bulk_g2s(st + b * kBlockBytes, atom_src(wexp, row_a, kb), kBlockBytes, &full[s]);
                         }
                     }
                     uint16_t* xsb = reinterpret_cast<uint16_t*>(st + kWeightStageBytes);
@@ -386,6 +407,7 @@ moe_linear_kernel(const MoeLinParams p) {
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
         const bool rows_valid = GATED || row_a + warp * kAtomRows < p.N;
+        const uint4* const wlut = (shards && warp >= 4) ? lut + 256 : lut;   // warps 4-7 hold up rows
         const uint8_t* const a0 = ring + warp * kAtomBytes;
         const uint16_t* const x0 = reinterpret_cast<const uint16_t*>(ring + kWeightStageBytes) +
                                    g * kXRowElems + q * 16;
@@ -406,7 +428,7 @@ moe_linear_kernel(const MoeLinParams p) {
                 const int nb = nkb - i * kBlocksPerStage;
                 #pragma unroll
                 for (int b = 0; b < kBlocksPerStage; ++b)
-                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], lut, xr + b * kBlockK, acc);
+                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], wlut, xr + b * kBlockK, acc);
             }
             fence_proxy_async();
             __syncwarp();
@@ -472,8 +494,12 @@ moe_linear_kernel(const MoeLinParams p) {
                 const int t = ei / 128, row = ei % 128;
                 const int64_t n = row_a + row;
                 if (t < nrows && n < p.N) {
-                    const int32_t slot = p.perm[r0 + t];
-                    p.Yp[(int64_t)slot * p.N + n] = p.wts[slot] * sum;
+                    if (p.act != 0) {        // non-gated FC1: h = RN(act(v)) in permuted row order
+                        p.H[(int64_t)(r0 + t) * p.N + n] = f32_to_act_bits<F16>(plain_act(sum, p.act));
+                    } else {
+                        const int32_t slot = p.perm[r0 + t];
+                        p.Yp[(int64_t)slot * p.N + n] = p.wts[slot] * sum;
+                    }
                 }
             }
         }
@@ -544,17 +570,17 @@ nvfp4_status launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, si
     return check_cuda(cudaLaunchKernelEx(&cfg, kernel, args...), what);
 }
 
-size_t moe_lin_smem(int MT, bool gated) {
+size_t moe_lin_smem(int MT, bool gated, bool shards) {
     const int tok = 8 * MT;
     const size_t part = gated ? ((size_t)tok * 64 + 8) * 2 : (size_t)tok * 128 + 8;
     const size_t ring = MT == 1 ? MoeRing<1>::G::kStages * MoeRing<1>::G::kStageBytes
                                 : MoeRing<2>::G::kStages * MoeRing<2>::G::kStageBytes;
-    return kRingOffset + kLutBytes + ring + part * 4;
+    return kRingOffset + (shards ? 2 : 1) * kLutBytes + ring + part * 4;
 }
 
 template <int MT, bool GATED, bool F16>
 nvfp4_status launch_moe_linear_typed(const MoeLinParams& p, unsigned gx, unsigned max_items, cudaStream_t s) {
-    const size_t smem = moe_lin_smem(MT, GATED);
+    const size_t smem = moe_lin_smem(MT, GATED, GATED && p.half_stride != 0);
     cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "MoE linear: shared memory attribute");
@@ -642,9 +668,15 @@ namespace {
 
 nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1, const void* fc2,
                       const void* fc1_pre_quant_scale, int64_t T, int E, int topk, int64_t H, int64_t I,
-                      void* out, int32_t* topk_idx_out, float* topk_weight_out, int32_t* perm_out,
-                      int32_t* offsets_out, void* workspace, size_t workspace_bytes, bool f16, void* stream) {
-    const char* fn = f16 ? "nvfp4_w4a16_moe_grouped_f16" : "nvfp4_w4a16_moe_grouped";
+                      int activation, int fc1_split, void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                      int32_t* perm_out, int32_t* offsets_out, void* workspace, size_t workspace_bytes, bool f16,
+                      void* stream) {
+    const bool ex = activation != NVFP4_MOE_SWIGLU || fc1_split != 0;
+    const char* fn = ex ? "nvfp4_w4a16_moe_grouped_ex" : f16 ? "nvfp4_w4a16_moe_grouped_f16" : "nvfp4_w4a16_moe_grouped";
+    if (activation < NVFP4_MOE_SWIGLU || activation > NVFP4_MOE_SILU)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: activation=%d is not one of SWIGLU, RELU2, SILU", fn, activation);
+    if (fc1_split != 0 && (fc1_split != 1 || activation != NVFP4_MOE_SWIGLU))
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: fc1_split=%d (1 only with the gated SWIGLU experts)", fn, fc1_split);
     if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
     if (E < 1 || E > kMaxExperts) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: E=%d outside [1, %d]", fn, E, kMaxExperts);
     if (topk < 1 || topk > kMaxTopk || topk > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: topk=%d outside [1, min(E, %d)]", fn, topk, kMaxTopk);
@@ -678,6 +710,13 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
     uint16_t* hbuf = (uint16_t*)(ws + L.h);
     float* yp = (float*)(ws + L.yp);
     nvfp4_status st;
+    // FC1 of one expert: gated [2I, H] (gate rows, then up rows), or gate and up
+    // shards [I, H] each with its own global, or non-gated [I, H]
+    const bool gated = activation == NVFP4_MOE_SWIGLU;
+    const size_t shard_bytes = nvfp4_repack_size(I, H);
+    const size_t fc1_stride = !gated ? shard_bytes : fc1_split ? 2 * shard_bytes : nvfp4_repack_size(2 * I, H);
+    const size_t half_stride = fc1_split ? shard_bytes : 0;
+    const int64_t fc1_rows = (gated && !fc1_split) ? 2 * I : I;          // rows of one repacked FC1 buffer
 
     const uint16_t* xin = (const uint16_t*)X;
     if (fc1_pre_quant_scale && !L.tile) {
@@ -717,27 +756,35 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         if (st != NVFP4_OK) return st;
         TcMoeParams t1{};
         t1.fc1 = true; t1.f16 = f16; t1.subm = L.subm; t1.X = xp; t1.x_rows = n;
-        t1.w = (const uint8_t*)fc1; t1.w_stride = nvfp4_repack_size(2 * I, H);
-        t1.N = 2 * I; t1.K = H; t1.I = I; t1.items = items; t1.n_items = n_items; t1.max_items = L.max_items;
+        t1.act = gated ? 0 : activation; t1.half_stride = half_stride;
+        t1.w = (const uint8_t*)fc1; t1.w_stride = fc1_stride;
+        t1.N = fc1_rows; t1.K = H; t1.I = I; t1.items = items; t1.n_items = n_items; t1.max_items = L.max_items;
         t1.perm = perm; t1.wts = wts; t1.H = hbuf; t1.status = status;
         if ((st = launch_tc_moe(t1, s)) != NVFP4_OK) return st;
         TcMoeParams t2 = t1;
-        t2.fc1 = false; t2.X = hbuf; t2.w = (const uint8_t*)fc2; t2.w_stride = nvfp4_repack_size(H, I);
+        t2.fc1 = false; t2.act = 0; t2.half_stride = 0;
+        t2.X = hbuf; t2.w = (const uint8_t*)fc2; t2.w_stride = nvfp4_repack_size(H, I);
         t2.N = H; t2.K = I; t2.Yp = yp; t2.H = nullptr;
         if ((st = launch_tc_moe(t2, s)) != NVFP4_OK) return st;
     } else {
         // expected work items in flight, for the split-K choice
         const int64_t est_items = std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
         MoeLinParams p1{};
-        p1.w = (const uint8_t*)fc1; p1.w_stride = nvfp4_repack_size(2 * I, H);
-        p1.N = 2 * I; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
-        p1.splits = moe_splits((I / 64) * est_items, p1.KB, 4);
+        p1.w = (const uint8_t*)fc1; p1.w_stride = fc1_stride; p1.half_stride = half_stride;
+        p1.N = fc1_rows; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
+        const int64_t fc1_groups = gated ? I / 64 : ceil_div(I, 128);     // CTAs per item along the rows
+        p1.splits = moe_splits(fc1_groups * est_items, p1.KB, 4);
         p1.kbs = (int)ceil_div(p1.KB, p1.splits);
         p1.splits = (int)ceil_div(p1.KB, p1.kbs);
         p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
         p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
-        st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, f16, s)
-                       : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)L.max_items, f16, s);
+        p1.act = gated ? 0 : activation;
+        if (gated)
+            st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
+                           : launch_moe_linear<2, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
+        else
+            st = L.mt == 1 ? launch_moe_linear<1, false>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
+                           : launch_moe_linear<2, false>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
 
         MoeLinParams p2{};
@@ -768,8 +815,8 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped(const void* X, const float* rout
                                                 void* out, int32_t* topk_idx_out, float* topk_weight_out,
                                                 int32_t* perm_out, int32_t* offsets_out,
                                                 void* workspace, size_t workspace_bytes, void* stream) {
-    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out, topk_idx_out,
-                    topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, false, stream);
+    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, NVFP4_MOE_SWIGLU, 0, out,
+                    topk_idx_out, topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, false, stream);
 }
 
 extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* router_logits,
@@ -779,8 +826,60 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_f16(const void* X, const float* 
                                                     void* out, int32_t* topk_idx_out, float* topk_weight_out,
                                                     int32_t* perm_out, int32_t* offsets_out,
                                                     void* workspace, size_t workspace_bytes, void* stream) {
-    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, out, topk_idx_out,
-                    topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, true, stream);
+    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, NVFP4_MOE_SWIGLU, 0, out,
+                    topk_idx_out, topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, true, stream);
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_moe_grouped_ex(const void* X, const float* router_logits,
+                                                   const void* fc1, const void* fc2,
+                                                   const void* fc1_pre_quant_scale,
+                                                   int64_t T, int E, int topk, int64_t H, int64_t I,
+                                                   int activation, int fc1_split, int f16,
+                                                   void* out, int32_t* topk_idx_out, float* topk_weight_out,
+                                                   int32_t* perm_out, int32_t* offsets_out,
+                                                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (f16 != 0 && f16 != 1) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_w4a16_moe_grouped_ex: f16=%d must be 0 or 1", f16);
+    return moe_impl(X, router_logits, fc1, fc2, fc1_pre_quant_scale, T, E, topk, H, I, activation, fc1_split, out,
+                    topk_idx_out, topk_weight_out, perm_out, offsets_out, workspace, workspace_bytes, f16 != 0, stream);
+}
+
+// ------------------------------------------- AWQ pre-quant scale finalization --
+namespace nvfp4 {
+namespace {
+
+// s[k] = max over experts of max(w3_e[k], w1_e[k]); the result is one of the
+// inputs, so it converts back to the 16-bit type exactly.
+template <bool F16>
+__global__ void finalize_pqs_kernel(const uint16_t* __restrict__ w1, const uint16_t* __restrict__ w3, int E,
+                                    int64_t H, uint16_t* __restrict__ out) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= H) return;
+    auto val = [](uint16_t b) { return F16 ? f16_bits_to_f32(b) : __uint_as_float((uint32_t)b << 16); };
+    float m = fmaxf(val(w1[k]), val(w3[k]));
+    for (int e = 1; e < E; ++e) m = fmaxf(m, fmaxf(val(w1[(int64_t)e * H + k]), val(w3[(int64_t)e * H + k])));
+    out[k] = f32_to_act_bits<F16>(m);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_moe_finalize_pre_quant_scale(const void* w1_pre_quant_scale,
+                                                           const void* w3_pre_quant_scale, int E, int64_t H,
+                                                           int f16, void* out, void* stream) {
+    const char* fn = "nvfp4_moe_finalize_pre_quant_scale";
+    if (E < 1 || H <= 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: E=%d H=%lld must be positive", fn, E, (long long)H);
+    if (f16 != 0 && f16 != 1) return fail(NVFP4_ERR_INVALID_ARG, "%s: f16=%d must be 0 or 1", fn, f16);
+    if (!w1_pre_quant_scale || !w3_pre_quant_scale || !out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(w1_pre_quant_scale, 2) || !aligned(w3_pre_quant_scale, 2) || !aligned(out, 2))
+        return fail(NVFP4_ERR_ALIGNMENT, "%s: pointers must be 2-byte aligned", fn);
+    const unsigned grid = (unsigned)ceil_div(H, 256);
+    if (f16)
+        finalize_pqs_kernel<true><<<grid, 256, 0, (cudaStream_t)stream>>>(
+            (const uint16_t*)w1_pre_quant_scale, (const uint16_t*)w3_pre_quant_scale, E, H, (uint16_t*)out);
+    else
+        finalize_pqs_kernel<false><<<grid, 256, 0, (cudaStream_t)stream>>>(
+            (const uint16_t*)w1_pre_quant_scale, (const uint16_t*)w3_pre_quant_scale, E, H, (uint16_t*)out);
+    return check_cuda(cudaGetLastError(), "nvfp4_moe_finalize_pre_quant_scale: launch");
 }
 
 // ---------------------------------------------------------- dense MLP --
