@@ -122,6 +122,28 @@ nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
                           int64_t N, int64_t K,
                           void* out, size_t out_bytes, void* stream);
 
+/*
+ * Scales in the checkpoint's swizzled layout.  The source pages keep NVFP4
+ * per-block scales swizzled and derive the linear view ("[TRTLLM-12288][feat]
+ * Support Nemotron-H nvfp4 ckpt on Hopper", Linear: "Per-block scales stay in
+ * swizzled layout; the unswizzled view is a derived non-persistent buffer")
+ * without printing the layout; the one read here is the 128 x 4 tile layout of
+ * NVIDIA's block-scaled GEMMs: rows padded to 128 and 16-groups to 4, tiles of
+ * 128 rows x 4 groups stored row-tile-major (512 bytes each), and inside a
+ * tile the scale of row r (0..127), group c (0..3) at (r % 32)*16 + (r / 32)*4 + c.
+ * nvfp4_repack_ex with scale_layout = NVFP4_SCALES_SWIZZLED_128x4 reads
+ * scales_e4m3 in that layout (nvfp4_swizzled_scales_size(N, K) bytes, padding
+ * ignored) and writes exactly what nvfp4_repack writes from the linear view;
+ * NVFP4_SCALES_LINEAR is nvfp4_repack.
+ */
+typedef enum { NVFP4_SCALES_LINEAR = 0, NVFP4_SCALES_SWIZZLED_128x4 = 1 } nvfp4_scale_layout;
+
+size_t nvfp4_swizzled_scales_size(int64_t N, int64_t K);
+nvfp4_status nvfp4_repack_ex(const uint8_t* packed, const uint8_t* scales_e4m3, int scale_layout,
+                             float global_scale, int global_is_divisor,
+                             int64_t N, int64_t K,
+                             void* out, size_t out_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Standalone dequant                                                        */
 /* ------------------------------------------------------------------------ */

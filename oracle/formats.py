@@ -169,3 +169,39 @@ def act_to_float(bits, act):
 def act_nan_bits(act):
     """The quiet-NaN pattern (sign bit clear) the rounding functions produce."""
     return 0x7FC0 if act == "bf16" else 0x7E00
+
+
+def swizzled_scale_offset(n, j, G):
+    """Byte offset of the scale of row n, 16-group j in the swizzled checkpoint
+    layout of a weight with G = K/16 groups per row.
+
+    The pages keep NVFP4 per-block scales in a swizzled layout and derive the
+    linear [N, K/16] view from it ("[TRTLLM-12288][feat] Support Nemotron-H
+    nvfp4 ckpt on Hopper", Linear section: "Per-block scales stay in swizzled
+    layout; the unswizzled view is a derived non-persistent buffer"), without
+    printing the layout.  The reading taken: the 128 x 4 tiles of NVIDIA's
+    block-scaled GEMMs -- rows padded to 128 and groups to 4, tiles of 128 rows
+    x 4 groups stored row-tile-major as 512 bytes each, and inside a tile the
+    scale of (r, c) at (r % 32) * 16 + (r // 32) * 4 + c.
+    """
+    n = np.asarray(n, dtype=np.int64)
+    j = np.asarray(j, dtype=np.int64)
+    tiles_per_row = (int(G) + 3) // 4
+    tile = (n // 128) * tiles_per_row + j // 4
+    r, c = n % 128, j % 4
+    return tile * 512 + (r % 32) * 16 + (r // 32) * 4 + c
+
+
+def swizzled_scales_size(N, K):
+    """Bytes of the swizzled scale tensor of an N x K weight."""
+    G = K // 16
+    return ((N + 127) // 128 * 128) * ((G + 3) // 4 * 4)
+
+
+def unswizzle_scales(swizzled, N, K):
+    """Linear scale codes uint8 [N, K/16] from the swizzled bytes."""
+    G = K // 16
+    sw = np.asarray(swizzled, dtype=np.uint8).reshape(-1)
+    n = np.arange(N)[:, None]
+    j = np.arange(G)[None, :]
+    return sw[swizzled_scale_offset(n, j, G)]

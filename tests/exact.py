@@ -125,3 +125,20 @@ def f16_exact(bits):
     else:
         mag = (1 + Fraction(f, 1024)) * Fraction(2) ** (e - 15)
     return -mag if s else mag
+
+
+def swizzle_scales_by_tiles(lin, N, K):
+    """Independent construction: walk the 128 x 4 tiles and the 32 x (4 x 4)
+    interleave inside each, writing bytes in storage order."""
+    G = K // 16
+    Np, Gp = -(-N // 128) * 128, -(-G // 4) * 4
+    pad = np.zeros((Np, Gp), dtype=np.uint8)
+    pad[:N, :G] = lin
+    out = []
+    for rt in range(Np // 128):
+        for ct in range(Gp // 4):
+            for r32 in range(32):
+                for quarter in range(4):
+                    for c in range(4):
+                        out.append(pad[rt * 128 + quarter * 32 + r32, ct * 4 + c])
+    return np.array(out, dtype=np.uint8)

@@ -99,3 +99,13 @@ def test_python_binding_refuses_non_bf16_activations():
         nv.gemm(torch.zeros(2, 64, dtype=torch.float8_e4m3fn), w)
     with pytest.raises(nv.Nvfp4Error):
         nv.gemm(torch.zeros(2, 64, dtype=torch.bfloat16), w)     # CPU tensor
+
+
+def test_swizzled_scales_size_and_layout_flag(lib):
+    assert lib.nvfp4_swizzled_scales_size(1, 16) == 128 * 4
+    assert lib.nvfp4_swizzled_scales_size(129, 80) == 256 * 8
+    assert lib.nvfp4_swizzled_scales_size(0, 16) == 0
+    V = ctypes.c_void_p
+    good = V(0x10000)
+    st = lib.nvfp4_repack_ex(good, good, 7, 1.0, 1, 16, 64, good, 1 << 20, None)
+    assert st == 1 and "scale_layout" in _err(lib)

@@ -259,3 +259,21 @@ def test_gemm_bitwise_deterministic_across_runs():
     gu.check_device_status()
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("K,N", [(720, 300), (2064, 1000), (64, 129), (4096, 512)])
+def test_repack_from_swizzled_scales(K, N):
+    """Scales given in the checkpoint's 128 x 4 swizzled layout repack to the same
+    bytes as the linear view, and dequantize to the oracle's weights."""
+    from tests.exact import swizzle_scales_by_tiles
+    c = synth.gaussian_case(1, K, N, seed=300 + K + N)
+    sw = swizzle_scales_by_tiles(c.scales, N, K)
+    assert sw.size == nv.swizzled_scales_size(N, K) == formats.swizzled_scales_size(N, K)
+    w_lin = gu.repack_case(c)
+    w_swz = nv.repack(gu.u8(c.packed), gu.u8(sw), float(c.divisor), N, K, swizzled_scales=True)
+    torch.cuda.synchronize()
+    assert torch.equal(w_lin.buf, w_swz.buf)
+    got = gu.tensor_to_bits(nv.dequant(w_swz))
+    gu.check_device_status()
+    want = dense.dequant(c.packed, formats.unswizzle_scales(sw, N, K), c.divisor, True, K)
+    assert np.array_equal(got, want)

@@ -16,7 +16,8 @@ import pytest
 import torch
 
 from oracle import formats
-from tests.exact import bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f16_exact, f16_round_exact
+from tests.exact import (bf16_exact, bf16_round_exact, e2m1_exact, e4m3_exact, f16_exact, f16_round_exact,
+                         swizzle_scales_by_tiles)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -232,3 +233,27 @@ def test_plant_f16_wrong_tie_rule_is_caught(monkeypatch):
     monkeypatch.setattr(formats, "f16_bits", bad)
     with pytest.raises(AssertionError):
         test_f16_rounding_is_single_rounding()
+
+
+# ----------------------------------------------------- swizzled scales ---
+def test_swizzled_offsets_worked_values():
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "swizzled_scale_offsets.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(v) for v in line.split()])
+    for n, j, off in rows:
+        assert int(formats.swizzled_scale_offset(n, j, 12)) == off, (n, j)
+
+
+@pytest.mark.parametrize("N,K", [(1, 16), (128, 64), (300, 192), (257, 2064)])
+def test_unswizzle_inverts_the_tile_walk(N, K):
+    r = np.random.default_rng(N + K)
+    lin = r.integers(0, 256, size=(N, K // 16), dtype=np.uint8)
+    sw = swizzle_scales_by_tiles(lin, N, K)
+    assert sw.size == formats.swizzled_scales_size(N, K)
+    assert np.array_equal(formats.unswizzle_scales(sw, N, K), lin)
+    # every (n, j) lands on a distinct byte
+    offs = formats.swizzled_scale_offset(np.arange(N)[:, None], np.arange(K // 16)[None, :], K // 16)
+    assert np.unique(offs).size == offs.size

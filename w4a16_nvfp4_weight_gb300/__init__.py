@@ -22,7 +22,7 @@ import torch
 from . import _lib
 from ._lib import Nvfp4Error
 
-__all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "dequant", "gemm",
+__all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "swizzled_scales_size", "dequant", "gemm",
            "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "moe_finalize_pre_quant_scale",
            "mlp", "mlp_workspace_size",
            "device_status",
@@ -74,18 +74,30 @@ class NVFP4Weight:
         return self.buf.numel()
 
 
-def repack(packed, scales, global_scale, N, K, global_is_divisor=True, out=None):
-    """Checkpoint tensors (uint8 [N, K/2] codes, uint8 [N, K/16] E4M3 scales) ->
-    NVFP4Weight.  ``global_scale`` is a Python float (the stored value)."""
+def repack(packed, scales, global_scale, N, K, global_is_divisor=True, out=None, swizzled_scales=False):
+    """Checkpoint tensors (uint8 [N, K/2] codes, uint8 E4M3 scales) -> NVFP4Weight.
+    ``scales`` is the linear [N, K/16] view, or with ``swizzled_scales`` the
+    checkpoint's 128 x 4 swizzled layout (swizzled_scales_size(N, K) bytes).
+    ``global_scale`` is a Python float (the stored value)."""
     h = _lib.load()
     _require_cuda(packed, "packed", torch.uint8)
     _require_cuda(scales, "scales", torch.uint8)
     size = int(h.nvfp4_repack_size(N, K))
     if out is None:
         out = torch.empty(max(size, 256), dtype=torch.uint8, device=packed.device)
-    _lib.check(h.nvfp4_repack(_ptr(packed), _ptr(scales), float(global_scale),
-                              1 if global_is_divisor else 0, N, K, _ptr(out), out.numel(), _stream()))
+    if swizzled_scales:
+        if scales.numel() < swizzled_scales_size(N, K):
+            raise Nvfp4Error(2, f"swizzled scales need {swizzled_scales_size(N, K)} bytes")
+        _lib.check(h.nvfp4_repack_ex(_ptr(packed), _ptr(scales), 1, float(global_scale),
+                                     1 if global_is_divisor else 0, N, K, _ptr(out), out.numel(), _stream()))
+    else:
+        _lib.check(h.nvfp4_repack(_ptr(packed), _ptr(scales), float(global_scale),
+                                  1 if global_is_divisor else 0, N, K, _ptr(out), out.numel(), _stream()))
     return NVFP4Weight(out, N, K)
+
+
+def swizzled_scales_size(N, K):
+    return int(_lib.load().nvfp4_swizzled_scales_size(N, K))
 
 
 def dequant(w, out=None, dtype=torch.bfloat16):

@@ -22,6 +22,8 @@ SIGNATURES = {
     "nvfp4_device_status": (c_int, [ctypes.POINTER(c_int), c_int, c_vp]),
     "nvfp4_repack_size": (c_size, [c_i64, c_i64]),
     "nvfp4_repack": (c_int, [c_vp, c_vp, c_float, c_int, c_i64, c_i64, c_vp, c_size, c_vp]),
+    "nvfp4_swizzled_scales_size": (c_size, [c_i64, c_i64]),
+    "nvfp4_repack_ex": (c_int, [c_vp, c_vp, c_int, c_float, c_int, c_i64, c_i64, c_vp, c_size, c_vp]),
     "nvfp4_dequant": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
     "nvfp4_dequant_f16": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
     "nvfp4_w4a16_gemm_workspace": (c_size, [c_i64, c_i64, c_i64, c_int]),

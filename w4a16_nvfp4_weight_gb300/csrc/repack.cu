@@ -119,11 +119,20 @@ __device__ __forceinline__ uint32_t to_sign_split(uint32_t w) {
     return out;
 }
 
+// Byte offset of the scale of row n, 16-group j in the swizzled checkpoint
+// layout (G groups per row): 128-row x 4-group tiles of 512 bytes, row-tile
+// major, and inside a tile (r % 32) * 16 + (r / 32) * 4 + (j % 4), r = n % 128.
+__device__ __forceinline__ int64_t swizzled_scale_offset(int64_t n, int64_t j, int64_t G) {
+    const int64_t tile = (n / 128) * ((G + 3) / 4) + j / 4;
+    const int64_t r = n % 128;
+    return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (j % 4);
+}
+
 // One warp per atom.  Lane L = 4r + q writes its 16 code bytes (rows r, r+8 of
 // the atom, group q) and its 2 scale bytes.
 __global__ void tiles_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                              uint8_t* __restrict__ out, int64_t N, int64_t K, int64_t KB,
-                             int64_t total_atoms) {
+                             int64_t total_atoms, int swizzled) {
     const int64_t atom = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     if (atom >= total_atoms) return;
     const int lane = threadIdx.x & 31;
@@ -140,7 +149,8 @@ __global__ void tiles_kernel(const uint8_t* __restrict__ packed, const uint8_t* 
         uint8_t s = 0;
         if (n < N && k0 < K) {
             raw = *reinterpret_cast<const uint2*>(packed + n * (K / 2) + k0 / 2);
-            s = scales[n * (K / kGroup) + k0 / kGroup];
+            const int64_t G = K / kGroup, j = k0 / kGroup;
+            s = swizzled ? scales[swizzled_scale_offset(n, j, G)] : scales[n * G + j];
         }
         words[2 * h] = to_sign_split(raw.x);
         words[2 * h + 1] = to_sign_split(raw.y);
@@ -204,23 +214,31 @@ extern "C" size_t nvfp4_repack_size(int64_t N, int64_t K) {
     return (size_t)round_up((int64_t)(kTilesOffset + atoms * kAtomBytes), 256);
 }
 
-extern "C" nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
-                                     float global_scale, int global_is_divisor,
-                                     int64_t N, int64_t K, void* out, size_t out_bytes,
-                                     void* stream) {
-    if (N <= 0 || K <= 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_repack: N=%lld K=%lld must be positive", (long long)N, (long long)K);
-    if (K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_repack: K=%lld is not a multiple of the group size 16", (long long)K);
-    if (!packed || !scales_e4m3 || !out) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_repack: null pointer (packed=%p scales=%p out=%p)", (const void*)packed, (const void*)scales_e4m3, out);
-    if (global_is_divisor != 0 && global_is_divisor != 1) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_repack: global_is_divisor must be 0 or 1");
-    if (!aligned(packed, 16)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_repack: packed weight must be 16-byte aligned");
-    if (!aligned(out, 256)) return fail(NVFP4_ERR_ALIGNMENT, "nvfp4_repack: out must be 256-byte aligned");
+extern "C" size_t nvfp4_swizzled_scales_size(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || K % kGroup != 0) return 0;
+    return (size_t)(round_up(N, 128) * round_up(K / kGroup, 4));
+}
+
+extern "C" nvfp4_status nvfp4_repack_ex(const uint8_t* packed, const uint8_t* scales_e4m3, int scale_layout,
+                                        float global_scale, int global_is_divisor,
+                                        int64_t N, int64_t K, void* out, size_t out_bytes,
+                                        void* stream) {
+    const char* fn = scale_layout == NVFP4_SCALES_LINEAR ? "nvfp4_repack" : "nvfp4_repack_ex";
+    if (scale_layout != NVFP4_SCALES_LINEAR && scale_layout != NVFP4_SCALES_SWIZZLED_128x4)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: scale_layout=%d is not LINEAR or SWIZZLED_128x4", fn, scale_layout);
+    if (N <= 0 || K <= 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: N=%lld K=%lld must be positive", fn, (long long)N, (long long)K);
+    if (K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld is not a multiple of the group size 16", fn, (long long)K);
+    if (!packed || !scales_e4m3 || !out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer (packed=%p scales=%p out=%p)", fn, (const void*)packed, (const void*)scales_e4m3, out);
+    if (global_is_divisor != 0 && global_is_divisor != 1) return fail(NVFP4_ERR_INVALID_ARG, "%s: global_is_divisor must be 0 or 1", fn);
+    if (!aligned(packed, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: packed weight must be 16-byte aligned", fn);
+    if (!aligned(out, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: out must be 256-byte aligned", fn);
     const size_t need = nvfp4_repack_size(N, K);
-    if (out_bytes < need) return fail(NVFP4_ERR_WORKSPACE, "nvfp4_repack: out has %zu bytes, needs %zu", out_bytes, need);
+    if (out_bytes < need) return fail(NVFP4_ERR_WORKSPACE, "%s: out has %zu bytes, needs %zu", fn, out_bytes, need);
     // g = RN_fp32(1/d): one IEEE single-precision division.
     volatile float one = 1.0f;
     const float g = global_is_divisor ? one / global_scale : global_scale;
     if (!(g == g) || g == 0.0f || g == INFINITY || g == -INFINITY)
-        return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_repack: global multiplier %g (from %g, divisor=%d) must be finite and nonzero", (double)g, (double)global_scale, global_is_divisor);
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: global multiplier %g (from %g, divisor=%d) must be finite and nonzero", fn, (double)g, (double)global_scale, global_is_divisor);
     const int64_t Np = round_up(N, kTileRows), Kp = round_up(K, kBlockK);
     const int64_t KB = Kp / kBlockK;
     const int64_t atoms = (Np / kAtomRows) * KB;
@@ -229,8 +247,17 @@ extern "C" nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scale
     nvfp4_status st = check_cuda(cudaGetLastError(), "nvfp4_repack: magnitude-table launch");
     if (st != NVFP4_OK) return st;
     const int warps = 8;
-    tiles_kernel<<<(unsigned)ceil_div(atoms, warps), warps * 32, 0, s>>>(packed, scales_e4m3, (uint8_t*)out, N, K, KB, atoms);
+    tiles_kernel<<<(unsigned)ceil_div(atoms, warps), warps * 32, 0, s>>>(packed, scales_e4m3, (uint8_t*)out, N, K, KB,
+                                                                         atoms, scale_layout);
     return check_cuda(cudaGetLastError(), "nvfp4_repack: tile launch");
+}
+
+extern "C" nvfp4_status nvfp4_repack(const uint8_t* packed, const uint8_t* scales_e4m3,
+                                     float global_scale, int global_is_divisor,
+                                     int64_t N, int64_t K, void* out, size_t out_bytes,
+                                     void* stream) {
+    return nvfp4_repack_ex(packed, scales_e4m3, NVFP4_SCALES_LINEAR, global_scale, global_is_divisor, N, K, out,
+                           out_bytes, stream);
 }
 
 namespace nvfp4 {
