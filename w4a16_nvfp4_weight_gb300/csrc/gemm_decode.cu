@@ -311,6 +311,19 @@ int decode_ctas_per_sm(int MT, int ring) {
 }
 
 template <int MT, int R>
+cudaError_t launch_decode_ex(const cudaLaunchConfig_t& cfg, bool f16, const DecodeParams& p) {
+    return f16 ? cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, true>, p)
+               : cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, false>, p);
+}
+
+cudaError_t launch_decode_typed(const cudaLaunchConfig_t& cfg, int MT, int ring, bool f16, const DecodeParams& p) {
+    if (MT == 1) return ring == kRingDeep ? launch_decode_ex<1, kRingDeep>(cfg, f16, p)
+                                          : launch_decode_ex<1, kRingShallow>(cfg, f16, p);
+    return ring == kRingDeep ? launch_decode_ex<2, kRingDeep>(cfg, f16, p)
+                             : launch_decode_ex<2, kRingShallow>(cfg, f16, p);
+}
+
+template <int MT, int R>
 const void* decode_fn(bool f16) {
     return f16 ? (const void*)decode_kernel<MT, R, true> : (const void*)decode_kernel<MT, R, false>;
 }
@@ -355,8 +368,7 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, bool f16,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    void* args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fn, args);
+    e = launch_decode_typed(cfg, MT, ring, f16, p);
     return check_cuda(e, "decode GEMM: launch");
 }
 
