@@ -73,39 +73,54 @@ int sm_count() {
 
 // Split-K plan of the decode kernel for an M x N x K problem.
 struct DecodePlan {
-    int MT, ring, splits, kbs;
+    int MT, ring, W, splits, kbs;
+    int64_t ctas;
     bool ok;
 };
 
 DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
-    DecodePlan pl{};
-    pl.MT = M <= 8 ? 1 : 2;
-    const int64_t TOK = 8 * pl.MT;
+    const int MT = M <= 8 ? 1 : 2;
+    const int64_t TOK = 8 * MT;
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
-    const int64_t RG = ceil_div(N, 128);
-    const int64_t base = RG * ceil_div(M, TOK);
+    const int64_t mchunks = ceil_div(M, TOK);
+    const int64_t sms = sm_count();
     // Split K until the CTAs fill one wave (as many per SM as shared memory
     // holds), with at most 8 CTAs per cluster (larger, non-portable clusters
     // measured slower) and at least two 64-k blocks per CTA.
-    auto split_for = [&](int ring) {
-        const int64_t target = (int64_t)decode_ctas_per_sm(pl.MT, ring) * sm_count();
+    auto plan_for = [&](int ring, int W) {
+        DecodePlan pl{};
+        pl.MT = MT; pl.ring = ring; pl.W = W; pl.ok = true;
+        const int64_t base = ceil_div(N, (int64_t)W * kAtomRows) * mchunks;
+        const int64_t target = (int64_t)decode_ctas_per_sm(MT, ring, W) * sms;
         int64_t splits = std::max<int64_t>(1, target / std::max<int64_t>(base, 1));
         splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / 2)));
         const int64_t kbs = ceil_div(KB, splits);
         pl.splits = (int)ceil_div(KB, kbs);
         pl.kbs = (int)kbs;
-        pl.ring = ring;
+        pl.ctas = base * pl.splits;
+        return pl;
     };
     // Slices of at most 16 blocks spend much of their time filling the ring
     // and reducing: those take the shallow ring, which packs more CTAs per SM,
     // when that buys a finer split.
-    split_for(kRingDeep);
-    if (pl.kbs <= 16) {
-        const DecodePlan deep = pl;
-        split_for(kRingShallow);
-        if (pl.splits <= deep.splits) pl = deep;
+    auto plan_rings = [&](int W) {
+        DecodePlan pl = plan_for(kRingDeep, W);
+        if (pl.kbs <= 16) {
+            const DecodePlan shallow = plan_for(kRingShallow, W);
+            if (shallow.splits > pl.splits) pl = shallow;
+        }
+        return pl;
+    };
+    DecodePlan pl = plan_rings(8);
+    // A grid of 128-row CTAs that fills under three quarters of a wave (few
+    // output rows, the split capped by the cluster size) leaves SMs idle -- the
+    // block scheduler also stacks such grids' clusters on part of the SMs --
+    // so it takes 64-row CTAs instead, twice as many.
+    const int64_t wave = (int64_t)decode_ctas_per_sm(MT, pl.ring, 8) * sms;
+    if (pl.ctas * 4 < wave * 3) {
+        const DecodePlan half = plan_rings(4);
+        if (half.ctas > pl.ctas) pl = half;
     }
-    pl.ok = true;
     return pl;
 }
 
@@ -186,7 +201,7 @@ nvfp4_status nvfp4::run_dense_gemm(const void* X, const void* repacked, const vo
     p.M = M; p.N = N; p.K = K;
     p.KB = round_up(K, kBlockK) / kBlockK;
     p.kbs = pl.kbs; p.splits = pl.splits; p.status = status;
-    return launch_decode(p, pl.MT, pl.ring, f16, s);
+    return launch_decode(p, pl.MT, pl.ring, pl.W, f16, s);
 }
 
 extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,

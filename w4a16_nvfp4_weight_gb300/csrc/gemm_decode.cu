@@ -40,10 +40,14 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kWarps = 8;                      // consumer warps: 8 x 16 = 128 weight rows
-constexpr int kThreads = (kWarps + 1) * 32;    // + 1 producer warp
-constexpr int kRowsPerCta = kWarps * kAtomRows;
-constexpr uint32_t kBlockBytes = kStreamBlockBytes;            // 4608: 128 rows x 64 k, contiguous
+// CTA shape: W consumer warps of 16 weight rows each (W = 8: 128 rows; W = 4:
+// 64 rows, for grids that would otherwise fill less than a wave) + 1 producer.
+template <int W> struct Cta {
+    static constexpr int kWarps = W;
+    static constexpr int kThreads = (W + 1) * 32;
+    static constexpr int kRowsPerCta = W * kAtomRows;
+    static constexpr uint32_t kBlockBytes = W * kAtomBytes;      // W x 576: one 64-k block, contiguous
+};
 
 // Ring shape per number of 8-token MMA tiles (MT) and ring kind: stages x
 // 64-k blocks per stage.  Larger stages amortise the per-stage barrier work;
@@ -57,8 +61,8 @@ template <> struct Ring<2, kRingDeep> { static constexpr int kStages = 2, kBlock
 template <> struct Ring<1, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
 template <> struct Ring<2, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
 
-template <int MT, int R>
-using RingGeom = StreamRing<MT, Ring<MT, R>::kStages, Ring<MT, R>::kBlocksPerStage>;
+template <int MT, int R, int W>
+using RingGeom = StreamRing<MT, Ring<MT, R>::kStages, Ring<MT, R>::kBlocksPerStage, W>;
 
 struct Smem {
     // offsets in bytes from the dynamic shared memory base
@@ -68,11 +72,15 @@ struct Smem {
     static constexpr size_t ring = lut + kLutBytes;
 };
 
-template <int MT, int R, bool F16>
-__global__ void __launch_bounds__(kThreads)
+template <int MT, int R, bool F16, int W>
+__global__ void __launch_bounds__(Cta<W>::kThreads)
 decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    using G = RingGeom<MT, R>;
+    using G = RingGeom<MT, R, W>;
+    constexpr int kWarps = Cta<W>::kWarps;
+    constexpr int kThreads = Cta<W>::kThreads;
+    constexpr int kRowsPerCta = Cta<W>::kRowsPerCta;
+    constexpr uint32_t kBlockBytes = Cta<W>::kBlockBytes;
     constexpr int TOK = G::kTok;
     constexpr int kStages = G::kStages;
     constexpr int kBlocksPerStage = G::kBlocksPerStage;
@@ -100,7 +108,7 @@ decode_kernel(const DecodeParams p) {
     const int64_t m_left = p.M - m0;
     const int rows_x = (int)(m_left < TOK ? m_left : TOK);           // token rows with data (>= 1)
     const int64_t nt = ((int64_t)rg * kRowsPerCta) / kTileRows;
-    const int rb0 = (rg * kRowsPerCta) % kTileRows / kAtomRows;      // 0 or 8
+    const int rb0 = (rg * kRowsPerCta) % kTileRows / kAtomRows;      // first 16-row block in the tile
     const uint8_t* wsrc = p.rp + kTilesOffset + atom_offset(nt, kb0, rb0, p.KB);
     const size_t kb_stride = (size_t)kAtomsPerTileK * kAtomBytes;
 
@@ -290,73 +298,82 @@ nvfp4_status launch_awq_scale(const uint16_t* X, const uint16_t* pqs, uint16_t* 
     return check_cuda(cudaGetLastError(), "AWQ activation scaling: launch");
 }
 
-template <int MT, int R>
+template <int MT, int R, int W>
 constexpr size_t smem_bytes_of() {
-    // partial slots: splits x ceil(128 * TOK / splits) floats <= 128 * TOK + 15 (splits <= 16)
-    return Smem::ring + RingGeom<MT, R>::kStages * RingGeom<MT, R>::kStageBytes +
-           ((size_t)kRowsPerCta * MT * 8 + 16) * 4;
+    // partial slots: splits x ceil(rows * TOK / splits) floats <= rows * TOK + 15 (splits <= 16)
+    return Smem::ring + RingGeom<MT, R, W>::kStages * RingGeom<MT, R, W>::kStageBytes +
+           ((size_t)Cta<W>::kRowsPerCta * MT * 8 + 16) * 4;
 }
 
-size_t decode_smem_bytes(int MT, int ring) {
-    if (MT == 1) return ring == kRingDeep ? smem_bytes_of<1, kRingDeep>() : smem_bytes_of<1, kRingShallow>();
-    return ring == kRingDeep ? smem_bytes_of<2, kRingDeep>() : smem_bytes_of<2, kRingShallow>();
+template <int MT, int R>
+size_t smem_bytes_w(int W) { return W == 8 ? smem_bytes_of<MT, R, 8>() : smem_bytes_of<MT, R, 4>(); }
+
+size_t decode_smem_bytes(int MT, int ring, int W) {
+    if (MT == 1) return ring == kRingDeep ? smem_bytes_w<1, kRingDeep>(W) : smem_bytes_w<1, kRingShallow>(W);
+    return ring == kRingDeep ? smem_bytes_w<2, kRingDeep>(W) : smem_bytes_w<2, kRingShallow>(W);
 }
 
-int decode_ctas_per_sm(int MT, int ring) {
-    // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+int decode_ctas_per_sm(int MT, int ring, int W) {
+    // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA;
+    // 2048 threads per SM
     constexpr size_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
-    const size_t per_cta = decode_smem_bytes(MT, ring) + kReservedPerCta;
-    const int n = (int)(kSmemPerSm / per_cta);
-    return n < 1 ? 1 : (n > 7 ? 7 : n);        // 7 x 288 threads fit in 2048
+    const size_t per_cta = decode_smem_bytes(MT, ring, W) + kReservedPerCta;
+    const int by_smem = (int)(kSmemPerSm / per_cta);
+    const int by_threads = 2048 / ((W + 1) * 32);
+    const int n = by_smem < by_threads ? by_smem : by_threads;
+    return n < 1 ? 1 : n;
 }
 
-template <int MT, int R>
+template <int MT, int R, int W>
 cudaError_t launch_decode_ex(const cudaLaunchConfig_t& cfg, bool f16, const DecodeParams& p) {
-    return f16 ? cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, true>, p)
-               : cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, false>, p);
+    return f16 ? cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, true, W>, p)
+               : cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, false, W>, p);
 }
 
-cudaError_t launch_decode_typed(const cudaLaunchConfig_t& cfg, int MT, int ring, bool f16, const DecodeParams& p) {
-    if (MT == 1) return ring == kRingDeep ? launch_decode_ex<1, kRingDeep>(cfg, f16, p)
-                                          : launch_decode_ex<1, kRingShallow>(cfg, f16, p);
-    return ring == kRingDeep ? launch_decode_ex<2, kRingDeep>(cfg, f16, p)
-                             : launch_decode_ex<2, kRingShallow>(cfg, f16, p);
-}
-
-template <int MT, int R>
+template <int MT, int R, int W>
 const void* decode_fn(bool f16) {
-    return f16 ? (const void*)decode_kernel<MT, R, true> : (const void*)decode_kernel<MT, R, false>;
+    return f16 ? (const void*)decode_kernel<MT, R, true, W> : (const void*)decode_kernel<MT, R, false, W>;
 }
 
-nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, bool f16, cudaStream_t stream) {
-    DecodeParams p = p_in;
-    const int64_t rgs = ceil_div(p.N, kRowsPerCta);
-    const int64_t mchunks = ceil_div(p.M, 8 * MT);
-    size_t smem = decode_smem_bytes(MT, ring);
-    // A grid smaller than a full wave is spread over the SMs: the block
-    // scheduler would otherwise stack CTAs (clusters) on some SMs while others
-    // idle.  Asking for more dynamic shared memory than the ring needs caps the
-    // CTAs an SM accepts at the even share.  The request stays 8 KB under the
-    // cap: at the exact cap the launches failed under the profiler.  (A smaller
-    // shared-memory carve-out spreads as well, but switching the carve-out
-    // between consecutive kernels cost more than the spreading gained.)
-    const int64_t ctas = rgs * p.splits * mchunks;
-    const int64_t even = ceil_div(ctas, (int64_t)sm_count());
-    if (even < decode_ctas_per_sm(MT, ring)) {
-        const size_t cap_smem = (size_t)(228 * 1024) / (size_t)even - 1024 - 8192;
-        smem = std::max(smem, cap_smem);
+// The kernel instance for (MT, ring, W): its address and a launch of it.
+template <int W>
+cudaError_t launch_decode_w(const cudaLaunchConfig_t& cfg, int MT, int ring, bool f16, const DecodeParams& p,
+                            const void** fn_out) {
+    if (MT == 1) {
+        if (ring == kRingDeep) {
+            if (fn_out) { *fn_out = decode_fn<1, kRingDeep, W>(f16); return cudaSuccess; }
+            return launch_decode_ex<1, kRingDeep, W>(cfg, f16, p);
+        }
+        if (fn_out) { *fn_out = decode_fn<1, kRingShallow, W>(f16); return cudaSuccess; }
+        return launch_decode_ex<1, kRingShallow, W>(cfg, f16, p);
     }
-    const void* fn = MT == 1 ? (ring == kRingDeep ? decode_fn<1, kRingDeep>(f16) : decode_fn<1, kRingShallow>(f16))
-                             : (ring == kRingDeep ? decode_fn<2, kRingDeep>(f16) : decode_fn<2, kRingShallow>(f16));
+    if (ring == kRingDeep) {
+        if (fn_out) { *fn_out = decode_fn<2, kRingDeep, W>(f16); return cudaSuccess; }
+        return launch_decode_ex<2, kRingDeep, W>(cfg, f16, p);
+    }
+    if (fn_out) { *fn_out = decode_fn<2, kRingShallow, W>(f16); return cudaSuccess; }
+    return launch_decode_ex<2, kRingShallow, W>(cfg, f16, p);
+}
+
+nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, int W, bool f16, cudaStream_t stream) {
+    DecodeParams p = p_in;
+    if (W != 8 && W != 4) return fail(NVFP4_ERR_INVALID_ARG, "decode GEMM: unsupported CTA shape %d", W);
+    const int64_t rows_per_cta = (int64_t)W * kAtomRows;
+    const int64_t rgs = ceil_div(p.N, rows_per_cta);
+    const int64_t mchunks = ceil_div(p.M, 8 * MT);
+    const size_t smem = decode_smem_bytes(MT, ring, W);
+    cudaLaunchConfig_t cfg = {};
+    const void* fn = nullptr;
+    if (W == 8) launch_decode_w<8>(cfg, MT, ring, f16, p, &fn);
+    else launch_decode_w<4>(cfg, MT, ring, f16, p, &fn);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "decode GEMM: shared memory attribute");
     if (p.splits > 8) {            // clusters of up to 16 CTAs are not portable: opt in
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return check_cuda(e, "decode GEMM: cluster size attribute");
     }
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rgs, (unsigned)p.splits, (unsigned)mchunks);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)((W + 1) * 32), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -368,7 +385,7 @@ nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, bool f16,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = launch_decode_typed(cfg, MT, ring, f16, p);
+    e = W == 8 ? launch_decode_w<8>(cfg, MT, ring, f16, p, nullptr) : launch_decode_w<4>(cfg, MT, ring, f16, p, nullptr);
     return check_cuda(e, "decode GEMM: launch");
 }
 

@@ -21,16 +21,18 @@ struct DecodeParams {
 // that one CTA's pipeline fill and reduction overlap another's work.
 enum DecodeRing { kRingDeep = 0, kRingShallow = 1 };
 
-// Dynamic shared memory of one CTA for MT token tiles of 8 and the given ring.
-size_t decode_smem_bytes(int MT, int ring);
+// Dynamic shared memory of one CTA for MT token tiles of 8, the given ring and
+// W consumer warps (8: 128 weight rows per CTA; 4: 64 rows).
+size_t decode_smem_bytes(int MT, int ring, int W);
 
-// CTAs of the decode kernel that fit on one SM at once (shared memory bound).
-int decode_ctas_per_sm(int MT, int ring);
+// CTAs of the decode kernel that fit on one SM at once (shared memory and
+// thread bound).
+int decode_ctas_per_sm(int MT, int ring, int W);
 
 // MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
-// covered by a third grid dimension.
+// covered by a third grid dimension.  W = 8 or 4 consumer warps.
 // f16: FP16 activations and output (else BF16).
-nvfp4_status launch_decode(const DecodeParams& p, int MT, int ring, bool f16, cudaStream_t stream);
+nvfp4_status launch_decode(const DecodeParams& p, int MT, int ring, int W, bool f16, cudaStream_t stream);
 
 // Xs = RN(X * pqs) in the activation type (FP16 when f16, else BF16) for an
 // M x K activation (K a multiple of 16).

@@ -8,16 +8,18 @@
 namespace nvfp4 {
 
 // Shared-memory ring of the streaming kernels: kStages stages, each holding
-// kBlocksPerStage 64-k blocks of 128 weight rows (4608 contiguous bytes each)
-// followed by the activation chunk of 8*MT token rows (row stride padded by
-// 16 bytes so that the rows fall on different banks).
-constexpr uint32_t kStreamBlockBytes = 8 * kAtomBytes;
+// kBlocksPerStage 64-k blocks of 16*W weight rows (W x 576 contiguous bytes
+// each; W consumer warps of 16 rows) followed by the activation chunk of 8*MT
+// token rows (row stride padded by 16 bytes so that the rows fall on different
+// banks).
+constexpr uint32_t kStreamBlockBytes = 8 * kAtomBytes;   // the 128-row block
 
-template <int MT, int S, int B> struct StreamRing {
+template <int MT, int S, int B, int W = 8> struct StreamRing {
     static constexpr int kTok = 8 * MT;
     static constexpr int kStages = S;
     static constexpr int kBlocksPerStage = B;
-    static constexpr uint32_t kWeightStageBytes = B * kStreamBlockBytes;
+    static constexpr uint32_t kBlockBytes = W * kAtomBytes;
+    static constexpr uint32_t kWeightStageBytes = B * kBlockBytes;
     static constexpr int kXRowElems = B * kBlockK + 8;
     static constexpr size_t kXStageBytes = (size_t)kTok * kXRowElems * 2;
     static constexpr size_t kStageBytes = kWeightStageBytes + kXStageBytes;
