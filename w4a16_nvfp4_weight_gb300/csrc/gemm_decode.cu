@@ -49,20 +49,26 @@ template <int W> struct Cta {
     static constexpr uint32_t kBlockBytes = W * kAtomBytes;      // W x 576: one 64-k block, contiguous
 };
 
-// Ring shape per number of 8-token MMA tiles (MT) and ring kind: stages x
-// 64-k blocks per stage.  Larger stages amortise the per-stage barrier work;
-// with 16 tokens the activation chunks are twice as large, and two stages
-// keep three CTAs resident per SM.  The shallow rings fit four CTAs per SM.
-// The shapes were chosen by timing the alternatives on GB300 over the decode
-// layer shapes.
-template <int MT, int R> struct Ring;
-template <> struct Ring<1, kRingDeep> { static constexpr int kStages = 3, kBlocksPerStage = 4; };
-template <> struct Ring<2, kRingDeep> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
-template <> struct Ring<1, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
-template <> struct Ring<2, kRingShallow> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
+// Ring shape per number of 8-token MMA tiles (MT), ring kind and CTA shape:
+// stages x 64-k blocks per stage.  Larger stages amortise the per-stage
+// barrier work; with 16 tokens the activation chunks are twice as large, and
+// two stages keep three 128-row CTAs resident per SM.  The shallow rings fit
+// more CTAs per SM.  The shapes were chosen by timing the alternatives on
+// GB300 over the decode layer shapes.
+template <int MT, int R, int W> struct Ring;
+template <> struct Ring<1, kRingDeep, 8> { static constexpr int kStages = 3, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingDeep, 8> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
+template <> struct Ring<1, kRingShallow, 8> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingShallow, 8> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
+// 64-row CTAs: four per SM (a grid of 512 such CTAs then covers 128 SMs
+// evenly instead of stacking five on fewer SMs)
+template <> struct Ring<1, kRingDeep, 4> { static constexpr int kStages = 3, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingDeep, 4> { static constexpr int kStages = 3, kBlocksPerStage = 3; };
+template <> struct Ring<1, kRingShallow, 4> { static constexpr int kStages = 2, kBlocksPerStage = 4; };
+template <> struct Ring<2, kRingShallow, 4> { static constexpr int kStages = 2, kBlocksPerStage = 3; };
 
 template <int MT, int R, int W>
-using RingGeom = StreamRing<MT, Ring<MT, R>::kStages, Ring<MT, R>::kBlocksPerStage, W>;
+using RingGeom = StreamRing<MT, Ring<MT, R, W>::kStages, Ring<MT, R, W>::kBlocksPerStage, W>;
 
 struct Smem {
     // offsets in bytes from the dynamic shared memory base
