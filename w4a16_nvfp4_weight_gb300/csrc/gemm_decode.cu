@@ -2,10 +2,12 @@
 // dequant fused into the tensor-core operand registers.
 //
 // The weight is the only large operand, so every byte of it is read once.  A
-// CTA owns 128 weight rows (8 consumer warps x 16 rows) and one K slice.  A
+// CTA owns 128 weight rows (8 consumer warps x 16 rows; 64 rows with 4 warps
+// for grids that would otherwise fill less than a wave) and one K slice.  A
 // producer warp streams the slice through a shared-memory ring with bulk
-// (TMA) copies: per stage four 64-k blocks of weights (4 x 4608 contiguous
-// bytes) and the matching activation chunk, one copy per token row.  Per 64-k atom a lane reads 16 code bytes and 2 scale bytes, looks its
+// (TMA) copies: per stage three or four 64-k blocks of weights (contiguous
+// 576 bytes per 16 rows) and the matching activation chunk, one copy per token
+// row.  Per 64-k atom a lane reads 16 code bytes and 2 scale bytes, looks its
 // two group tables up and expands the codes straight into mma.sync A
 // fragments (weights on the M side, tokens on the N side).  Within a
 // 16-element group the MMA's k order is permuted so that one lane consumes one
@@ -14,7 +16,7 @@
 // CTAs of a thread-block cluster, which reduce their FP32 partials through
 // distributed shared memory in rank order: deterministic, and no global
 // workspace.  The AWQ pre-quant scale, when present, is applied by a small
-// pass that writes x' = RN_bf16(x * s) into the workspace first.
+// pass that writes x' = RN(x * s) (BF16 or FP16) into the workspace first.
 //
 // The kernel is launched with programmatic dependent launch: it lets the next
 // kernel of the stream start early, and it streams its first weight stages

@@ -11,11 +11,15 @@
 //               the matching up rows of the expert's FC1 weight, streamed like
 //               the dense decode kernel (bulk-copy ring, split-K across a
 //               cluster, push-based reduction); the epilogue applies
-//               h = RN_bf16(silu(g) * u) and writes H in permuted row order.
+//               h = RN(silu(g) * u) and writes H in permuted row order.
+//               Non-gated experts (relu2 / silu): 128 rows of [I, H] per CTA,
+//               h = RN(act(v)).  With many rows per expert the tcgen05 tile
+//               kernel (gemm_tc.cu) runs FC1 and FC2 instead.
 //   fc2      -- the same over FC2 with H as input; the epilogue scales by the
 //               slot's routing weight and writes FP32 rows per routing slot.
-//   combine  -- out[t] = RN_bf16(sum over slots j of the FP32 rows), in slot
+//   combine  -- out[t] = RN(sum over slots j of the FP32 rows), in slot
 //               order.
+// RN rounds to the activation type, BF16 or FP16.
 // Only experts that received tokens have work items, so only their weights are
 // read.  Nothing is read back to the host: the grid is sized by an upper bound
 // on the number of work items, surplus CTAs exit at once, and the whole layer
