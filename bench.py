@@ -136,17 +136,27 @@ PROFILE_FOR = {
 }
 
 
-def traffic_ratio(kind):
+def kernel_sources_sha(srcs):
+    """Hash of the kernel's sources with comments and blank lines removed, so
+    that editing a comment does not invalidate a capture."""
     import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in srcs:
+        text = open(os.path.join(ROOT, "w4a16_nvfp4_weight_gb300", "csrc", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    return h.hexdigest()[:16]
+
+
+def traffic_ratio(kind):
     path, srcs = PROFILE_FOR[kind]
     try:
         text = open(os.path.join(ROOT, path)).read()
         kv = dict(line.split(":", 1) for line in text.splitlines()
                   if line.startswith(("traffic_ratio:", "kernel_sources_sha:")))
-        h = hashlib.sha256()
-        for f in srcs:
-            h.update(open(os.path.join(ROOT, "w4a16_nvfp4_weight_gb300", "csrc", f), "rb").read())
-        if h.hexdigest()[:16] != kv["kernel_sources_sha"].strip():
+        if kernel_sources_sha(srcs) != kv["kernel_sources_sha"].strip():
             return None
         return float(kv["traffic_ratio"])
     except (OSError, KeyError, ValueError):
