@@ -233,6 +233,27 @@ def test_gemm_prefill_full_size_sampled(K, N):
         assert np.all(np.isfinite(formats.bf16_to_float(yb)))
 
 
+@pytest.mark.parametrize("M,K,N", [(100, 1024, 20480), (300, 1040, 20480), (1000, 1024, 20480),
+                                   (520, 4096, 2560), (777, 1536, 9990), (130, 2048, 19456)])
+def test_gemm_tile_kernels_sampled(M, K, N):
+    """Shapes that the tile planner sends to each dense tile kernel: the
+    tensor-memory-A kernel with 128-token tiles (M=100) and 192-token tiles
+    (partial last tile at M=300 and 130, K tail at K=1040, N tail at N=9990, a
+    5-way K split at 520x4096x2560) and the shared-memory-operand kernel with
+    256-token tiles (M=1000); every output row band of 16 is sampled."""
+    r = synth.rng(synth.seed_for(6, M + K + N))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(6, M * 3 + K * 7 + N))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = np.unique(np.concatenate([_sampled_rows(N, r, n=32), np.arange(0, N, 16), [N - 1]]))
+    x_bits = synth.normal_bf16(r, (M, K))
+    y = nv.gemm(gu.bits_to_bf16_tensor(x_bits), w)
+    gu.check_device_status()
+    yb = gu.tensor_to_bits(y)
+    _, ref = dense.linear(x_bits, packed, scales, d, True, rows=rows)
+    gu.compare(yb[:, rows], ref, f"tile M={M} K={K} N={N}")
+    assert np.all(np.isfinite(formats.bf16_to_float(yb)))
+
+
 def test_lm_head_full_size_sampled():
     K, N = 4096, 151936
     r = synth.rng(synth.seed_for(4, 0))

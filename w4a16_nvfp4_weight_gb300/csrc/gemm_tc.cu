@@ -400,6 +400,231 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     }
 }
 
+// ------------------------------------------------------------------------
+// Dense tile GEMM with the weights as the tensor-memory A operand.
+//
+// The kernel above writes the dequantized weights into shared memory, where
+// they compete with the MMAs' own operand reads for shared-memory bandwidth
+// (removing those stores alone made it ~20% faster on GB300).  Here the dequant
+// threads write them straight into tensor memory with tcgen05.st, and the MMA
+// takes A from there: D[weight row, token] = W x X^T.
+//
+// One CTA covers 256 weight rows x NT tokens (NT = 128 or 192) over its K range:
+//   warp 0       producer: per 64-k block, a TMA tile load of the activations
+//                (NT rows x 64 k, 128-byte swizzle, zero fill past M and K) and a
+//                bulk copy of the raw 256-row weight block into a kWaS1-stage ring;
+//   warp 1       allocates all 512 tensor-memory columns and issues, per block,
+//                2 x 4 tcgen05 MMAs (M = 128 weight rows from tensor memory,
+//                N = NT tokens from shared memory, K = 16);
+//   warps 2..17  dequant: a thread owns one weight row (its tensor-memory lane)
+//                and half of the block's k (two 16-k groups); it reads their
+//                codes and scales, expands them through the magnitude table and
+//                stores 16 packed columns; afterwards the epilogue (tensor memory
+//                -> registers -> Y[token, row]).
+// Tensor-memory columns: accumulator of weight half s at [256 s, 256 s + NT);
+// A stage st, half s at (st ? 256 : 0) + NT + 32 s (32 columns = 64 k).
+constexpr int kWaS1 = 4;                 // activation + raw-weight ring
+constexpr int kWaS2 = 2;                 // A stages in tensor memory
+constexpr int kWaDeqWarps = 16;
+constexpr int kWaThreads = (kWaDeqWarps + 2) * 32;
+
+template <int NT>
+struct WaSmem {
+    static constexpr size_t kXBytes = (size_t)NT * 128;                     // NT rows x 64 k
+    static constexpr size_t x = 0;                                           // 1024-aligned
+    static constexpr size_t raw = x + (size_t)kWaS1 * kXBytes;
+    static constexpr size_t lut = raw + (size_t)kWaS1 * kBRawBytes;
+    static constexpr size_t bars = lut + kLutBytes;
+    static constexpr size_t misc = bars + 16 * 8;
+    static constexpr size_t total = misc + 64;
+};
+
+__device__ __forceinline__ uint32_t wa_a_col(int NT, int st, int s) { return (uint32_t)((st ? 256 : 0) + NT + 32 * s); }
+
+template <int NT, bool F16>
+__global__ void __launch_bounds__(kWaThreads, 1)
+tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
+    static_assert(NT == 128 || NT == 192, "token tile");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = WaSmem<NT>;
+    uint8_t* x_ring = smem + L::x;
+    uint8_t* raw_ring = smem + L::raw;
+    uint4* lut = reinterpret_cast<uint4*>(smem + L::lut);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+    uint64_t* tma_full = bars;                      // [kWaS1]
+    uint64_t* tma_empty = bars + kWaS1;             // [kWaS1]
+    uint64_t* deq_full = bars + 2 * kWaS1;          // [kWaS2]
+    uint64_t* deq_empty = bars + 2 * kWaS1 + kWaS2; // [kWaS2]
+    uint64_t* acc_full = bars + 2 * kWaS1 + 2 * kWaS2;
+    uint64_t* lut_bar = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
+    volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t n0 = (int64_t)blockIdx.x * kBN;
+    const int64_t m0 = (int64_t)blockIdx.y * NT;
+    const int kb_first = (int)blockIdx.z * p.kb_per_split;
+    const int64_t kb_left = p.KB - kb_first;
+    const int nkb = (int)(kb_left < p.kb_per_split ? kb_left : p.kb_per_split);
+
+    if (tid == 0) {
+        for (int s = 0; s < kWaS1; ++s) {
+            mbar_init(&tma_full[s], 1);
+            mbar_init(&tma_empty[s], 1 + kWaDeqWarps);   // MMA commit + every dequant warp
+        }
+        for (int s = 0; s < kWaS2; ++s) {
+            mbar_init(&deq_full[s], kWaDeqWarps);
+            mbar_init(&deq_empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(lut_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t idesc = umma_idesc(128, NT, F16);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const Header* hdr = reinterpret_cast<const Header*>(p.rp);
+            const bool ok_hdr = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K;
+            *hdr_flag = ok_hdr ? 1 : 0;
+            if (!ok_hdr) {
+                record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
+                mbar_arrive(lut_bar);
+            } else {
+                mbar_arrive_expect_tx(lut_bar, (uint32_t)kLutBytes);
+                bulk_g2s(lut, p.rp + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
+                const uint8_t* wtile = p.rp + kTilesOffset + atom_offset(n0 / kTileRows, 0, 0, p.KB);
+                int issued = 0;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int s = kb % kWaS1;
+                    if (kb >= kWaS1 && !mbar_wait(&tma_empty[s], ((kb / kWaS1) - 1) & 1, p.status)) break;
+                    mbar_arrive_expect_tx(&tma_full[s], (uint32_t)L::kXBytes + kBRawBytes);
+                    tma_load_2d(x_ring + (size_t)s * L::kXBytes, &tmap_x, (kb_first + kb) * 64, (int)m0, &tma_full[s]);
+                    bulk_g2s(raw_ring + (size_t)s * kBRawBytes, wtile + (size_t)(kb_first + kb) * kBRawBytes,
+                             kBRawBytes, &tma_full[s]);
+                    ++issued;
+                }
+                // no copy may still target this CTA when it exits
+                mbar_wait(lut_bar, 0, p.status);
+                for (int kb = issued > kWaS1 ? issued - kWaS1 : 0; kb < issued; ++kb)
+                    mbar_wait(&tma_full[kb % kWaS1], (kb / kWaS1) & 1, p.status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+                const int s1 = kb % kWaS1, s2 = kb % kWaS2;
+                ok = mbar_wait(&tma_full[s1], (kb / kWaS1) & 1, p.status) &&
+                     mbar_wait(&deq_full[s2], (kb / kWaS2) & 1, p.status);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t x_base = smem_u32(x_ring + (size_t)s1 * L::kXBytes);
+                #pragma unroll
+                for (int s = 0; s < 2; ++s)
+                    #pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f16kind_ts(tmem + 256 * s, tmem + wa_a_col(NT, s2, s) + 8 * kk,
+                                        sw128_kmajor_desc(x_base + kk * 32), idesc, (kb | kk) != 0);
+                umma_commit(&tma_empty[s1]);
+                umma_commit(&deq_empty[s2]);
+            }
+            umma_commit(acc_full);          // also waits out every MMA issued above
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ dequant, then epilogue
+        // Warp -> (lane quarter Q: the hardware warp index decides which 32
+        // tensor-memory lanes a warp may access; weight half s; group pair gp).
+        // Lane t = (a, h, r) -> atom 8s + 2Q + a, row r + 8h of that atom; the
+        // row's group j codes are the 8 bytes at 16 (4r + j) + 8h of the atom.
+        // Loading the pair in an order rotated by r spreads a half warp's
+        // 8-byte loads over 8 bank pairs.
+        const int idx = (warp - 2) >> 2, Q = warp & 3;
+        const int s = idx >> 1, gp = idx & 1;
+        const int a = lane & 1, h = (lane >> 1) & 1, r = (lane >> 2) & 7;
+        const int atom = 8 * s + 2 * Q + a;
+        const int n_local = 128 * s + 32 * Q + 16 * a + 8 * h + r;
+        const uint32_t lane_addr = (uint32_t)(32 * Q) << 16;
+        const int rot = r & 1;
+        bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s1 = kb % kWaS1, s2 = kb % kWaS2;
+            ok = mbar_wait(&tma_full[s1], (kb / kWaS1) & 1, p.status);
+            if (ok && kb >= kWaS2) ok = mbar_wait(&deq_empty[s2], ((kb / kWaS2) - 1) & 1, p.status);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint8_t* at = raw_ring + (size_t)s1 * kBRawBytes + atom * kAtomBytes;
+            const uint2 v0 = *reinterpret_cast<const uint2*>(at + 16 * (4 * r + 2 * gp + rot) + 8 * h);
+            const uint2 v1 = *reinterpret_cast<const uint2*>(at + 16 * (4 * r + 2 * gp + (rot ^ 1)) + 8 * h);
+            const uint2 g0 = rot ? v1 : v0, g1 = rot ? v0 : v1;
+            // scales of groups 2gp, 2gp + 1: bytes 2 (2gp + i) + h of the 8 at 512 + 8r
+            const uint32_t sc = *reinterpret_cast<const uint32_t*>(at + kAtomCodeBytes + 8 * r + 4 * gp) >> (8 * h);
+            const Lut t0 = lut_from_uint4(lut[sc & 0xFFu]);
+            const Lut t1 = lut_from_uint4(lut[(sc >> 16) & 0xFFu]);
+            uint32_t e[16];
+            expand8(g0.x, t0, e);
+            expand8(g0.y, t0, e + 4);
+            expand8(g1.x, t1, e + 8);
+            expand8(g1.y, t1, e + 12);
+            tmem_st_32x32b_x16(tmem + lane_addr + wa_a_col(NT, s2, s) + 16 * gp, e);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            fence_proxy_async();       // raw reads before the next copy into the stage
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&deq_full[s2]);
+                mbar_arrive(&tma_empty[s1]);
+            }
+        }
+        // epilogue: this thread's row of the half-s accumulator, half gp of the NT tokens
+        if (*hdr_flag != 0 && mbar_wait(acc_full, 0, p.status)) {
+            tc_fence_after_sync();
+            const int64_t n = n0 + n_local;
+            const bool n_ok = n < p.N;
+            const uint32_t trow = tmem + lane_addr + 256 * s;
+            #pragma unroll 1
+            for (int c16 = gp * (NT / 32); c16 < (gp + 1) * (NT / 32); ++c16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(trow + c16 * 16, v);
+                tmem_ld_wait();
+                const int64_t mb = m0 + c16 * 16;
+                if (!n_ok || mb >= p.M) continue;
+                const int cnt = p.M - mb < 16 ? (int)(p.M - mb) : 16;
+                if (p.partial != nullptr) {
+                    float* col = p.partial + ((int64_t)blockIdx.z * p.M + mb) * p.N + n;
+                    #pragma unroll
+                    for (int i = 0; i < 16; ++i, col += p.N)
+                        if (i < cnt) *col = __uint_as_float(v[i]);
+                } else {
+                    uint16_t* col = p.Y + mb * p.N + n;
+                    #pragma unroll
+                    for (int i = 0; i < 16; ++i, col += p.N)
+                        if (i < cnt) *col = f32_to_act_bits<F16>(__uint_as_float(v[i]));
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // Y = RN(sum over splits of the FP32 partials) in the activation type, splits in order.
 template <bool F16>
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t MN,
@@ -434,12 +659,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-nvfp4_status encode_rows_map(CUtensorMap* tmap, const uint16_t* X, int64_t rows, int64_t K, bool f16) {
+nvfp4_status encode_rows_map(CUtensorMap* tmap, const uint16_t* X, int64_t rows, int64_t K, bool f16,
+                             uint32_t box_rows = 128) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(NVFP4_ERR_CUDA, "tile GEMM: cuTensorMapEncodeTiled unavailable");
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult cr = enc(tmap, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -468,38 +694,75 @@ nvfp4_status launch_tc_impl(const uint16_t* X, int64_t x_rows, const TcKParams& 
                : launch_tc_typed<SUBM, MODE, false>(X, x_rows, kp, grid, stream);
 }
 
+template <int NT, bool F16>
+nvfp4_status launch_wa_typed(const uint16_t* X, const TcKParams& kp, dim3 grid, cudaStream_t stream) {
+    CUtensorMap tmap;
+    nvfp4_status st = encode_rows_map(&tmap, X, kp.M, kp.K, F16, NT);
+    if (st != NVFP4_OK) return st;
+    // The kernel takes all 512 tensor-memory columns: request enough shared
+    // memory that a second CTA, which would have to wait for them, never
+    // becomes resident on the same SM.
+    constexpr size_t kOneCtaPerSm = 116 * 1024;
+    const size_t smem = WaSmem<NT>::total + 1024 > kOneCtaPerSm ? WaSmem<NT>::total + 1024 : kOneCtaPerSm;
+    cudaError_t e = cudaFuncSetAttribute(tc_wa_kernel<NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return check_cuda(e, "tile GEMM: shared memory attribute");
+    tc_wa_kernel<NT, F16><<<grid, kWaThreads, smem, stream>>>(tmap, kp);
+    return check_cuda(cudaGetLastError(), "tile GEMM: launch");
+}
+
+template <int NT>
+nvfp4_status launch_wa(const uint16_t* X, const TcKParams& kp, dim3 grid, bool f16, cudaStream_t stream) {
+    return f16 ? launch_wa_typed<NT, true>(X, kp, grid, stream) : launch_wa_typed<NT, false>(X, kp, grid, stream);
+}
+
 size_t awq_ws_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
 
-// Split-K plan of the dense tile GEMM from a simple cost model (measured on
-// GB300): a wave of tile CTAs costs about 0.78 us per 64-k block with two M
-// sub-tiles (0.45 us with one) plus 3 us, and a split adds its FP32 partials'
-// write and read at ~6 TB/s plus a 2 us reduction.  Split (<= 8 ways, >= 12
-// blocks per split) only when the model predicts at least 20% less time.
-struct TcSplit {
+// Plan of a dense tile GEMM: which of the two tile kernels, its token tile
+// and its split of K, from a cost model fitted to GB300 timings.  A wave of
+// CTAs costs t_blk per 64-k block plus 3 us: 0.82 us for the shared-memory
+// kernel's 256-token tiles (0.74 us for 128), 0.64 us for the tensor-memory-A
+// kernel's tiles of 192 or 128 tokens -- about the same cost per FLOP, so the
+// choice mostly follows how evenly each tiling fills the SMs.  A K split adds
+// its FP32 partials' write and read at ~6 TB/s plus a 2 us reduction; K is
+// split (<= 8 ways, >= 12 blocks per split) only when the model predicts at
+// least 20% less time.
+struct TcPlan {
+    bool wa;        // tensor-memory-A kernel (else shared-memory operands)
+    int tok;        // tokens per tile: 128 / 256 (SUBM 1 / 2) or 128 / 192 (NT)
     int splits, kbs;
 };
 
-TcSplit plan_tc_split(int64_t M, int64_t N, int64_t K) {
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K) {
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
-    const int64_t tiles = ceil_div(N, kBN) * (M <= 128 ? ceil_div(M, 128) : ceil_div(M, 256));
     const int64_t sms = sm_count();
-    const double t_blk = M <= 128 ? 0.45 : 0.78;
-    auto cost = [&](int64_t s) {
-        const int64_t kbs = ceil_div(KB, s);
-        double t = (double)ceil_div(tiles * s, sms) * ((double)kbs * t_blk + 3.0);
-        if (s > 1) t += 2.0 * (double)s * (double)M * (double)N * 4.0 / 6.0e6 + 2.0;
-        return t;
+    auto split_plan = [&](TcPlan pl, double t_blk, double* cost_out) {
+        const int64_t tiles = ceil_div(N, kBN) * ceil_div(M, pl.tok);
+        auto cost = [&](int64_t sp) {
+            const int64_t kbs = ceil_div(KB, sp);
+            double t = (double)ceil_div(tiles * sp, sms) * ((double)kbs * t_blk + 3.0);
+            if (sp > 1) t += 2.0 * (double)sp * (double)M * (double)N * 4.0 / 6.0e6 + 2.0;
+            return t;
+        };
+        pl.splits = 1;
+        pl.kbs = (int)KB;
+        double best_t = cost(1);
+        if ((M % 4) == 0 && (N % 4) == 0) {
+            const double limit = 0.8 * best_t;
+            for (int sp = 2; sp <= 8 && KB / sp >= 12; ++sp) {
+                const double t = cost(sp);
+                if (t < limit && t < best_t) { best_t = t; pl.splits = sp; pl.kbs = (int)ceil_div(KB, sp); }
+            }
+            if (pl.splits > 1) pl.splits = (int)ceil_div(KB, pl.kbs);
+        }
+        *cost_out = best_t;
+        return pl;
     };
-    TcSplit best{1, (int)KB};
-    if ((M % 4) != 0 || (N % 4) != 0) return best;
-    double best_t = cost(1);
-    const double limit = 0.8 * best_t;
-    for (int s = 2; s <= 8 && KB / s >= 12; ++s) {
-        const double t = cost(s);
-        if (t < limit && t < best_t) { best_t = t; best = TcSplit{s, (int)ceil_div(KB, s)}; }
-    }
-    if (best.splits > 1) best.splits = (int)ceil_div(KB, best.kbs);
-    return best;
+    double t_sm, t_wa;
+    const int sub = M <= 128 ? 1 : 2;
+    const TcPlan sm = split_plan(TcPlan{false, 128 * sub, 1, 1}, sub == 1 ? 0.74 : 0.82, &t_sm);
+    const int nt = ceil_div(M, 192) < ceil_div(M, 128) ? 192 : 128;
+    const TcPlan wa = split_plan(TcPlan{true, nt, 1, 1}, 0.64, &t_wa);
+    return t_wa < t_sm ? wa : sm;
 }
 
 }  // namespace
@@ -511,7 +774,7 @@ bool use_tc_path(int64_t M, int64_t N) {
 }
 
 size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs) {
-    const TcSplit sp = plan_tc_split(M, N, K);
+    const TcPlan sp = plan_tc(M, N, K);
     const size_t part = sp.splits > 1 ? (size_t)round_up((int64_t)sp.splits * M * N * 4, 256) : 0;
     return (has_pqs ? awq_ws_bytes(M, K) : 0) + part;
 }
@@ -527,18 +790,18 @@ nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream) {
     kp.rp = p.rp; kp.Y = p.Y; kp.M = p.M; kp.N = p.N; kp.K = p.K;
     kp.KB = round_up(p.K, kBlockK) / kBlockK;
     kp.status = p.status;
-    const TcSplit sp = plan_tc_split(p.M, p.N, p.K);
+    const TcPlan sp = plan_tc(p.M, p.N, p.K);
     kp.kb_per_split = sp.kbs;
     if (sp.splits > 1)
         kp.partial = reinterpret_cast<float*>((uint8_t*)p.workspace + (p.pqs ? awq_ws_bytes(p.M, p.K) : 0));
-    const unsigned gx = (unsigned)ceil_div(p.N, kBN);
+    const dim3 grid((unsigned)ceil_div(p.N, kBN), (unsigned)ceil_div(p.M, sp.tok), sp.splits);
     nvfp4_status st;
-    if (p.M <= 128)
-        st = launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 128), sp.splits), p.f16,
-                                               stream);
+    if (sp.wa)
+        st = sp.tok == 192 ? launch_wa<192>(X, kp, grid, p.f16, stream) : launch_wa<128>(X, kp, grid, p.f16, stream);
+    else if (sp.tok == 128)
+        st = launch_tc_impl<1, TcMode::kDense>(X, p.M, kp, grid, p.f16, stream);
     else
-        st = launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, dim3(gx, (unsigned)ceil_div(p.M, 256), sp.splits), p.f16,
-                                               stream);
+        st = launch_tc_impl<2, TcMode::kDense>(X, p.M, kp, grid, p.f16, stream);
     if (st != NVFP4_OK || sp.splits == 1) return st;
     const int64_t MN = p.M * p.N;
     const unsigned rgrid = (unsigned)ceil_div(MN / 4, 256);
