@@ -179,8 +179,11 @@ size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_q
  *  workspace       device, >= nvfp4_w4a16_gemm_workspace(...) bytes, 256-byte
  *                  aligned (may be NULL when that size is 0).  Contents on entry
  *                  do not matter.
- * M == 0 or N == 0 returns NVFP4_OK and launches nothing.  M <= 16 runs the
- * split-K HBM-streaming decode kernel; larger M the tensor-core tile kernel.
+ * M == 0 or N == 0 returns NVFP4_OK and launches nothing.  M <= 16 (and, up
+ * to M = 511, shapes whose output tiles would leave most SMs idle) runs the
+ * split-K HBM-streaming decode kernel; other shapes one of two tensor-core
+ * tile kernels (dequantized weight in shared memory, or in tensor memory as
+ * the MMA's A operand), chosen per shape; results agree within rounding.
  * The GEMM kernels use programmatic dependent launch: they may begin reading
  * the repacked weight before the preceding kernel of the stream has finished
  * (only if that kernel itself allows its dependents to start early), and read
