@@ -422,9 +422,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
 //                stores 16 packed columns; afterwards the epilogue (tensor memory
 //                -> registers -> Y[token, row]).
 // Tensor-memory columns: accumulator of weight half s at [256 s, 256 s + NT);
-// A stage st, half s at (st ? 256 : 0) + NT + 32 s (32 columns = 64 k).
+// the S2 A stages (64 columns each: two halves of 32 columns = 64 k) fill the
+// rest, S2 / 2 after each accumulator: 2 stages with 192-token tiles, 4 with 128.
 constexpr int kWaS1 = 4;                 // activation + raw-weight ring
-constexpr int kWaS2 = 2;                 // A stages in tensor memory
+constexpr int kWaS2Max = 4;
+template <int NT> __host__ __device__ constexpr int wa_stages() { return NT == 128 ? 4 : 2; }
 constexpr int kWaDeqWarps = 16;
 constexpr int kWaThreads = (kWaDeqWarps + 2) * 32;
 
@@ -435,11 +437,15 @@ struct WaSmem {
     static constexpr size_t raw = x + (size_t)kWaS1 * kXBytes;
     static constexpr size_t lut = raw + (size_t)kWaS1 * kBRawBytes;
     static constexpr size_t bars = lut + kLutBytes;
-    static constexpr size_t misc = bars + 16 * 8;
+    static constexpr size_t misc = bars + 24 * 8;
     static constexpr size_t total = misc + 64;
 };
 
-__device__ __forceinline__ uint32_t wa_a_col(int NT, int st, int s) { return (uint32_t)((st ? 256 : 0) + NT + 32 * s); }
+template <int NT>
+__device__ __forceinline__ uint32_t wa_a_col(int st, int s) {
+    constexpr int half = wa_stages<NT>() / 2;
+    return (uint32_t)((st < half ? NT + 64 * st : 256 + NT + 64 * (st - half)) + 32 * s);
+}
 
 template <int NT, bool F16>
 __global__ void __launch_bounds__(kWaThreads, 1)
@@ -454,9 +460,10 @@ tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
     uint64_t* tma_full = bars;                      // [kWaS1]
     uint64_t* tma_empty = bars + kWaS1;             // [kWaS1]
-    uint64_t* deq_full = bars + 2 * kWaS1;          // [kWaS2]
-    uint64_t* deq_empty = bars + 2 * kWaS1 + kWaS2; // [kWaS2]
-    uint64_t* acc_full = bars + 2 * kWaS1 + 2 * kWaS2;
+    constexpr int kWaS2 = wa_stages<NT>();
+    uint64_t* deq_full = bars + 2 * kWaS1;             // [kWaS2]
+    uint64_t* deq_empty = bars + 2 * kWaS1 + kWaS2Max; // [kWaS2]
+    uint64_t* acc_full = bars + 2 * kWaS1 + 2 * kWaS2Max;
     uint64_t* lut_bar = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
     volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + L::misc + 8);
@@ -536,7 +543,7 @@ tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 for (int s = 0; s < 2; ++s)
                     #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_f16kind_ts(tmem + 256 * s, tmem + wa_a_col(NT, s2, s) + 8 * kk,
+                        umma_f16kind_ts(tmem + 256 * s, tmem + wa_a_col<NT>(s2, s) + 8 * kk,
                                         sw128_kmajor_desc(x_base + kk * 32), idesc, (kb | kk) != 0);
                 umma_commit(&tma_empty[s1]);
                 umma_commit(&deq_empty[s2]);
@@ -579,7 +586,7 @@ tc_wa_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
             expand8(g0.y, t0, e + 4);
             expand8(g1.x, t1, e + 8);
             expand8(g1.y, t1, e + 12);
-            tmem_st_32x32b_x16(tmem + lane_addr + wa_a_col(NT, s2, s) + 16 * gp, e);
+            tmem_st_32x32b_x16(tmem + lane_addr + wa_a_col<NT>(s2, s) + 16 * gp, e);
             tmem_st_wait();
             tc_fence_before_sync();
             fence_proxy_async();       // raw reads before the next copy into the stage
