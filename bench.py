@@ -743,10 +743,9 @@ def run_e2e(nv, launches, stream, args, bw_unit):
 
 
 # ----------------------------------------------------------- CPU baseline --
-def cpu_baseline(seconds_target=15.0, reps=None, base=None, rows_per_gemm=256):
-    """The oracle, as it stands, on a bounded sample of the decode workload:
-    every GEMM of a step restricted to a seeded subset of output rows."""
-    from oracle import dense
+def _baseline_cases(base, rows_per_gemm):
+    """The oracle's sample of the decode workload: every GEMM of a step
+    restricted to a seeded subset of output rows."""
     from w4a16_nvfp4_weight_gb300 import synth
 
     r = synth.rng(4242)
@@ -760,20 +759,56 @@ def cpu_baseline(seconds_target=15.0, reps=None, base=None, rows_per_gemm=256):
         sub_p, sub_s = packed[rows], scales[rows]
         for M in DECODE_M:
             cases.append((M, K, sub_p, sub_s, d, synth.normal_act(r, (M, K), ACT)))
+    return cases
+
+
+def _oracle_sweeps(job):
+    """Sweep the oracle over the sample for `seconds` (or `reps` sweeps);
+    returns (algorithmic bytes, elapsed s, sweeps)."""
+    cases, seconds, reps, act = job
+    from oracle import dense
+
+    rows = len(cases[0][2])
     t0 = time.perf_counter()
     n_sweeps = 0
     b = 0
     while True:
         for (M, K, p, s, d, x) in cases:
-            dense.linear(x, p, s, d, True, act=ACT)
-            b += algo_bytes(M, rows_per_gemm, K)
+            dense.linear(x, p, s, d, True, act=act)
+            b += algo_bytes(M, rows, K)
         n_sweeps += 1
         el = time.perf_counter() - t0
-        if (reps is not None and n_sweeps >= reps) or (reps is None and el >= seconds_target):
-            break
+        if (reps is not None and n_sweeps >= reps) or (reps is None and el >= seconds):
+            return b, el, n_sweeps
+
+
+def cpu_baseline(seconds_target=15.0, reps=None, base=None, rows_per_gemm=256):
+    """The oracle, as it stands, single-threaded on a bounded sample of the
+    decode workload."""
+    cases = _baseline_cases(base, rows_per_gemm)
+    b, el, n_sweeps = _oracle_sweeps((cases, seconds_target, reps, ACT))
     return {"value": round(b / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n_sweeps} sweep(s) of the 20 decode GEMMs restricted to {rows_per_gemm} seeded "
                       f"output rows each (numpy float64 oracle, single thread), {el:.1f} s"}
+
+
+def cpu_baseline_all_cores(seconds_target=10.0, base=None, rows_per_gemm=256):
+    """The same sample on every host core: one single-threaded oracle process
+    per core (spawned, so no process is forked from one that holds a CUDA
+    context), all sweeping at once; value = their bytes / the wall time."""
+    import multiprocessing as mp
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    cases = _baseline_cases(base, rows_per_gemm)
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_sweeps, [(cases[:1], 0.0, 1, ACT)] * cores)       # start every worker first
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_sweeps, [(cases, seconds_target, None, ACT)] * cores, chunksize=1)
+        wall = time.perf_counter() - t0
+    total = sum(r[0] for r in res)
+    return {"value": round(total / wall / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes x {min(r[2] for r in res)}+ sweep(s) of the single-thread sample "
+                      f"(20 decode GEMMs, {rows_per_gemm} seeded output rows each), {wall:.1f} s wall"}
 
 
 def run_reference(args, rank, world):
@@ -874,8 +909,9 @@ def main():
     res = run_ours(args, rank, world, device)
     base = res.pop("_base", None)
     if rank == 0:
-        if not args.no_cpu_baseline and args.workload == "decode":
+        if not args.no_cpu_baseline and args.workload == "decode" and world == 1:
             res["cpu_baseline"] = cpu_baseline(base=base)
+            res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base)
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
