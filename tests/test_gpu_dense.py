@@ -194,6 +194,21 @@ def test_mismatched_header_is_reported_not_trapped():
     gu.check_device_status()
 
 
+@pytest.mark.parametrize("M,K,N_hdr,N_claim", [(600, 256, 256, 128), (1000, 1024, 20480, 20224)])
+def test_mismatched_header_tile_kernels(M, K, N_hdr, N_claim):
+    """The same header check on the two tile kernels (the tensor-memory-A kernel
+    at 600x256, the shared-memory one at 1000x1024): status 7, Y untouched."""
+    packed, scales, d = synth.weight_only(K, N_hdr, 12)
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N_hdr, K)
+    bad = nv.NVFP4Weight(w.buf, N_claim, K)
+    x = gu.bits_to_bf16_tensor(synth.normal_bf16(synth.rng(13), (M, K)))
+    y = torch.full((M, N_claim), 3.0, dtype=torch.bfloat16, device="cuda")
+    nv.gemm(x, bad, out=y)
+    assert nv.device_status(clear=True) == 7
+    assert torch.all(y == 3.0)
+    gu.check_device_status()
+
+
 def _sampled_rows(N, r, n=48):
     rows = np.unique(np.concatenate([r.choice(N, size=n, replace=False), [0, N - 1]]))
     return rows
