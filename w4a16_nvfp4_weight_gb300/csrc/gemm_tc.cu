@@ -1,7 +1,11 @@
-// Tensor-core tile GEMM for the W4A16 NVFP4 linear at larger M (prefill, LM
-// head): dequant-fused, TMA-fed, tcgen05 MMAs accumulating in tensor memory.
+// Tensor-core tile GEMMs for the W4A16 NVFP4 linear at larger M (prefill, LM
+// head, MoE with many rows per expert): dequant-fused, TMA-fed, tcgen05 MMAs
+// accumulating in tensor memory.  Two kernels: tc_gemm_kernel (below; both
+// operands in shared memory; dense and the MoE / MLP epilogues) and
+// tc_wa_kernel (further down; dense only; the dequantized weights as the
+// tensor-memory A operand).  plan_tc picks one per dense shape.
 //
-// One CTA computes a (128*SUBM) x 256 output tile over the whole K:
+// tc_gemm_kernel: one CTA computes a (128*SUBM) x 256 output tile over its K range:
 //   warp 0      producer: per 64-k block, TMA tile loads of the activation
 //               (128 rows x 64 k, 128-byte swizzle, zero fill past M and K)
 //               and one bulk copy of the weight block (256 rows x 64 k of codes

@@ -41,7 +41,7 @@ struct TcMoeParams {
 };
 nvfp4_status launch_tc_moe(const TcMoeParams& p, cudaStream_t stream);
 
-// Shape rule between the streaming (decode) kernel and the tile kernel: tiles
+// Shape rule between the streaming (decode) kernel and the tile kernels: tiles
 // for M > 16 unless the tile grid would leave most SMs idle at M < 512.
 bool use_tc_path(int64_t M, int64_t N);
 size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs);
