@@ -799,6 +799,7 @@ def cpu_baseline_all_cores(seconds_target=10.0, base=None, rows_per_gemm=256):
     import multiprocessing as mp
 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    cores = min(cores, 64)          # each process imports torch: bound the memory and start-up
     cases = _baseline_cases(base, rows_per_gemm)
     with mp.get_context("spawn").Pool(cores) as pool:
         pool.map(_oracle_sweeps, [(cases[:1], 0.0, 1, ACT)] * cores)       # start every worker first
