@@ -109,3 +109,54 @@ def test_swizzled_scales_size_and_layout_flag(lib):
     good = V(0x10000)
     st = lib.nvfp4_repack_ex(good, good, 7, 1.0, 1, 16, 64, good, 1 << 20, None)
     assert st == 1 and "scale_layout" in _err(lib)
+
+
+def test_moe_and_mlp_reject_bad_arguments_on_host(lib):
+    """MoE, dense-MLP and AWQ-finalization entry points validate before any
+    launch (status 1 invalid argument, 2 unsupported shape, 3 alignment,
+    4 workspace); T = 0 returns OK without touching a pointer."""
+    V = ctypes.c_void_p
+    g, big = V(0x100000), 1 << 40
+
+    def moe(X=g, lg=g, w1=g, w2=g, pqs=None, T=1, E=128, k=8, H=2048, I=768, act=0, split=0, f16=0,
+            out=g, ws=g, wsb=big):
+        return lib.nvfp4_w4a16_moe_grouped_ex(X, lg, w1, w2, pqs, T, E, k, H, I, act, split, f16,
+                                              out, None, None, None, None, ws, wsb, None)
+
+    assert moe(f16=2) == 1
+    assert moe(act=3) == 1 and "SWIGLU" in _err(lib)
+    assert moe(act=1, split=1) == 1                       # shards only with the gated experts
+    assert moe(T=-1) == 1
+    assert moe(E=0) == 2 and moe(E=257) == 2
+    assert moe(k=0) == 2 and moe(E=4, k=5) == 2 and moe(k=17) == 2
+    assert moe(H=100) == 2 and moe(I=0) == 2
+    assert moe(X=None, lg=None, w1=None, w2=None, out=None, ws=None, wsb=0, T=0) == 0
+    assert moe(X=None) == 1 and "null" in _err(lib)
+    assert moe(X=V(0x100008)) == 3
+    assert moe(lg=V(0x100002)) == 3
+    assert moe(w1=V(0x100010)) == 3
+    assert moe(pqs=V(0x100008)) == 3
+    assert moe(wsb=0) == 4 and "needs" in _err(lib)
+    assert moe(ws=V(0x100040)) == 3
+    assert moe(T=10_000_000) == 2                         # more work items than one grid dimension holds
+
+    def mlp(X=g, w1=g, w2=g, pqs=None, T=4, H=4096, I=14336, out=g, ws=g, wsb=big):
+        return lib.nvfp4_w4a16_mlp(X, w1, w2, pqs, T, H, I, out, ws, wsb, None)
+
+    assert mlp(T=-1) == 1
+    assert mlp(H=100) == 2 and mlp(I=0) == 2
+    assert mlp(X=None, w1=None, w2=None, out=None, ws=None, wsb=0, T=0) == 0
+    assert mlp(w2=None) == 1
+    assert mlp(out=V(0x100008)) == 3
+    assert mlp(w1=V(0x100080)) == 3
+    assert mlp(pqs=V(0x100004)) == 3
+    assert mlp(wsb=16) == 4
+    assert mlp(ws=V(0x100010)) == 3
+    assert lib.nvfp4_w4a16_mlp_workspace(4, 4096, 14336) > lib.nvfp4_w4a16_mlp_workspace(1, 4096, 14336) > 0
+
+    fin = lib.nvfp4_moe_finalize_pre_quant_scale
+    assert fin(g, g, 0, 64, 0, g, None) == 1
+    assert fin(g, g, 2, 0, 0, g, None) == 1
+    assert fin(g, g, 2, 64, 2, g, None) == 1
+    assert fin(None, g, 2, 64, 0, g, None) == 1
+    assert fin(g, g, 2, 64, 0, V(0x100001), None) == 3
