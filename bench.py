@@ -344,6 +344,7 @@ def run_ours(args, rank, world, device):
         "gpu_launches": launches_per_step * args.steps,
     }
     res["_base"] = base
+    res["_cases"] = [(L["M"], L["K"], L["N"], L["x_bits"], L["pqs_bits"]) for L in launches]
     return res
 
 
@@ -377,7 +378,7 @@ def run_moe(args, rank, world, device, nv, synth):
         ws = torch.empty(nv.moe_workspace_size(T, MOE_E, MOE_TOPK, MOE_H, MOE_I), dtype=torch.uint8, device=device)
         out = torch.empty((T, MOE_H), dtype=act_torch(), device=device)
         offs = torch.empty(MOE_E + 1, dtype=torch.int32, device=device)
-        calls.append(dict(T=T, x=x, lg=lg, ws=ws, out=out, offs=offs))
+        calls.append(dict(T=T, x=x, lg=lg, ws=ws, out=out, offs=offs, case=c))
 
     def call(C, w=0):
         # routing tables come back through offsets_out so the bench can count active experts
@@ -465,6 +466,7 @@ def run_moe(args, rank, world, device, nv, synth):
                    "samples": clk["samples"]},
         "gpu_launches": sum(moe_launches(C["T"], MOE_E, MOE_TOPK, MOE_I) for C in calls) * args.steps,
         "_base": None,
+        "_moe": (fc1, fc2, calls[0]["case"]),
     }
 
 
@@ -812,6 +814,61 @@ def cpu_baseline_all_cores(seconds_target=10.0, base=None, rows_per_gemm=256):
                       f"(20 decode GEMMs, {rows_per_gemm} seeded output rows each), {wall:.1f} s wall"}
 
 
+def cpu_baseline_dense(cases, base, bw_unit, seconds_target=12.0):
+    """The oracle, single-threaded, on the prefill / LM-head / odd-shape
+    workloads: every GEMM of a step with its full activations but restricted to
+    a seeded subset of output rows (16 per GEMM for the byte-bound shapes, 4
+    for the tensor-bound ones); value in the workload's unit."""
+    from oracle import dense
+    from w4a16_nvfp4_weight_gb300 import synth
+
+    r = synth.rng(4243)
+    per = 16 if bw_unit else 4
+    work = []
+    for (M, K, N, x_bits, pqs_bits) in cases:
+        _, packed, scales, d = base[(K, N)]
+        rows = np.sort(r.choice(N, size=min(per, N), replace=False))
+        work.append((M, K, len(rows), packed[rows], scales[rows], d, x_bits, pqs_bits))
+    t0 = time.perf_counter()
+    n_sweeps, amount = 0, 0
+    while True:
+        for (M, K, nr, p, sc, d, x, pqs) in work:
+            dense.linear(x, p, sc, d, True, pqs_bits=pqs, act=ACT)
+            amount += algo_bytes(M, nr, K) if bw_unit else flops(M, nr, K)
+        n_sweeps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target:
+            break
+    return {"value": round(amount / el / (1e9 if bw_unit else 1e12), 6), "unit": "GB/s" if bw_unit else "TFLOP/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{n_sweeps} sweep(s) of the {len(work)} GEMMs with full activations, {per} seeded output "
+                      f"rows each (numpy float64 oracle, single thread), {el:.1f} s"}
+
+
+def cpu_baseline_moe(fc1, fc2, case, seconds_target=12.0):
+    """The oracle, single-threaded, on the T = 1 MoE layer (routing,
+    permutation, the 8 routed experts' FC1 + SwiGLU and FC2, combine); value
+    in GB/s of the routed experts' weights plus the input and output rows."""
+    from oracle import moe as omoe
+
+    w1 = [(p, sc, d, True) for (p, sc, d) in fc1]
+    w2 = [(p, sc, d, True) for (p, sc, d) in fc2]
+    T = case.x_bits.shape[0]
+    t0 = time.perf_counter()
+    n, amount = 0, 0
+    while True:
+        res = omoe.moe_layer(case.x_bits, case.logits, w1, w2, MOE_TOPK, act=ACT)
+        experts = int((np.asarray(res["counts"]) > 0).sum())
+        amount += experts * (3 * MOE_I * MOE_H) * 9 // 16 + 2 * 2 * T * MOE_H
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target:
+            break
+    return {"value": round(amount / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} call(s) of the whole T={T} layer ({experts} routed experts; numpy float64 oracle, "
+                      f"single thread), {el:.1f} s"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -909,10 +966,17 @@ def main():
     device = torch.device("cuda", local)
     res = run_ours(args, rank, world, device)
     base = res.pop("_base", None)
+    cases = res.pop("_cases", None)
+    moe_host = res.pop("_moe", None)
     if rank == 0:
-        if not args.no_cpu_baseline and args.workload == "decode" and world == 1:
-            res["cpu_baseline"] = cpu_baseline(base=base)
-            res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base)
+        if not args.no_cpu_baseline and world == 1:
+            if args.workload == "decode":
+                res["cpu_baseline"] = cpu_baseline(base=base)
+                res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base)
+            elif args.workload in ("prefill", "lmhead", "tails"):
+                res["cpu_baseline"] = cpu_baseline_dense(cases, base, args.workload != "prefill")
+            elif args.workload == "moe":
+                res["cpu_baseline"] = cpu_baseline_moe(*moe_host)
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
