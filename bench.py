@@ -70,6 +70,38 @@ def peaks():
                 source="fallback")
 
 
+def in_run_peaks(device):
+    """Copy bandwidth and cuBLAS BF16 GEMM throughput measured in this run
+    (context beside the peaks the roofline divides by): a 1 GiB
+    device-to-device copy (read + write bytes) and an 8192^3 BF16 matmul,
+    each timed with CUDA events over 10 repetitions after 3 warm-ups."""
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / 10
+    n = 1 << 29                                         # elements: 1 GiB of BF16
+    a = torch.empty(n, dtype=torch.bfloat16, device=device)
+    b = torch.empty_like(a)
+    t_copy = timed(lambda: b.copy_(a))
+    del a, b
+    m = 8192
+    A = torch.randn(m, m, dtype=torch.bfloat16, device=device)
+    B = torch.randn(m, m, dtype=torch.bfloat16, device=device)
+    t_mm = timed(lambda: torch.matmul(A, B))
+    del A, B
+    torch.cuda.empty_cache()
+    return {"hbm_copy_gbs": round(2 * 2 * n / t_copy / 1e9, 1),
+            "bf16_gemm_tflops": round(2 * m ** 3 / t_mm / 1e12, 1),
+            "note": "measured in this run (1 GiB D2D copy; cuBLAS 8192^3 BF16 matmul); context only"}
+
+
 def gpu_index():
     """nvidia-smi index of the current CUDA device."""
     if "CUDA_VISIBLE_DEVICES" not in os.environ:
@@ -343,9 +375,17 @@ def run_ours(args, rank, world, device):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if world == 1:
+        res["roofline"]["peaks_in_run"] = in_run_peaks(device)
     res["_base"] = base
-    res["_cases"] = [(L["M"], L["K"], L["N"], L["x_bits"], L["pqs_bits"]) for L in launches]
+    res["_cases"] = host_cases(launches)
     return res
+
+
+def host_cases(launches):
+    """Host copies of each launch's inputs for the oracle baselines:
+    (M, K, N, activation bits, AWQ scale bits or None)."""
+    return [(L["M"], L["K"], L["N"], L["x_bits"], L.get("pqs_bits")) for L in launches]
 
 
 MOE_E, MOE_TOPK, MOE_H, MOE_I = 128, 8, 2048, 768
@@ -869,6 +909,28 @@ def cpu_baseline_moe(fc1, fc2, case, seconds_target=12.0):
                       f"single thread), {el:.1f} s"}
 
 
+def strip_host_data(res):
+    """Remove the host-side inputs run_* hands to the baselines; returns them."""
+    return res.pop("_base", None), res.pop("_cases", None), res.pop("_moe", None)
+
+
+def attach_cpu_baselines(res, workload, world, skip, seconds=None):
+    """Time the oracle beside the GPU line (rank 0 of a one-GPU run only) and
+    drop the host data; `seconds` shortens every sample (tests)."""
+    base, cases, moe_host = strip_host_data(res)
+    if skip or world != 1:
+        return res
+    kw = {} if seconds is None else {"seconds_target": seconds}
+    if workload == "decode":
+        res["cpu_baseline"] = cpu_baseline(base=base, **kw)
+        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base, **kw)
+    elif workload in ("prefill", "lmhead", "tails"):
+        res["cpu_baseline"] = cpu_baseline_dense(cases, base, workload != "prefill", **kw)
+    elif workload == "moe":
+        res["cpu_baseline"] = cpu_baseline_moe(*moe_host, **kw)
+    return res
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -965,19 +1027,11 @@ def main():
         return
     device = torch.device("cuda", local)
     res = run_ours(args, rank, world, device)
-    base = res.pop("_base", None)
-    cases = res.pop("_cases", None)
-    moe_host = res.pop("_moe", None)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
-            if args.workload == "decode":
-                res["cpu_baseline"] = cpu_baseline(base=base)
-                res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base)
-            elif args.workload in ("prefill", "lmhead", "tails"):
-                res["cpu_baseline"] = cpu_baseline_dense(cases, base, args.workload != "prefill")
-            elif args.workload == "moe":
-                res["cpu_baseline"] = cpu_baseline_moe(*moe_host)
+        attach_cpu_baselines(res, args.workload, world, args.no_cpu_baseline)
         print(json.dumps(res), flush=True)
+    else:
+        strip_host_data(res)
     if world > 1:
         torch.distributed.destroy_process_group()
 
