@@ -510,55 +510,12 @@ def run_moe(args, rank, world, device, nv, synth):
     }
 
 
-def _sms():
-    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-
-
-def tc_plan(M, N, K, sms=None):
-    """(tile kernel?, K splits, tensor-memory-A kernel?, tokens per tile) of a
-    dense GEMM: the library's shape rule and tile cost model, restated to count
-    launches."""
-    sms = sms or _sms()
-    KB = -(-K // 64)
-    tiles_sm = -(-N // 256) * (-(-M // 128) if M <= 128 else -(-M // 256))
-    if M <= 16 or not (tiles_sm >= sms // 2 or M >= 512):
-        return False, 1, False, 0
-
-    def plan(tok, t_blk):
-        tiles = -(-N // 256) * -(-M // tok)
-
-        def cost(sp):
-            kbs = -(-KB // sp)
-            t = -(-(tiles * sp) // sms) * (kbs * t_blk + 3.0)
-            return t + (2.0 * sp * M * N * 4.0 / 6.0e6 + 2.0 if sp > 1 else 0.0)
-
-        best, best_t = 1, cost(1)
-        if M % 4 == 0 and N % 4 == 0:
-            limit = 0.8 * best_t
-            sp = 2
-            while sp <= 8 and KB // sp >= 12:
-                t = cost(sp)
-                if t < limit and t < best_t:
-                    best, best_t = sp, t
-                sp += 1
-            if best > 1:
-                best = -(-KB // -(-KB // best))
-        return best, best_t
-
-    sub = 1 if M <= 128 else 2
-    sp_sm, t_sm = plan(128 * sub, 0.74 if sub == 1 else 0.82)
-    nt = 192 if -(-M // 192) < -(-M // 128) else 128
-    sp_wa, t_wa = plan(nt, 0.64)
-    if t_wa < t_sm:
-        return True, sp_wa, True, nt
-    return True, sp_sm, False, 128 * sub
-
-
 def gemm_launches(M, N, K, awq=False):
-    """Library kernels one gemm call launches: the GEMM, the split-K reduction
-    when the tile kernel splits K, and the activation scaling pass for AWQ."""
-    tile, splits, _, _ = tc_plan(M, N, K)
-    return 1 + (1 if tile and splits > 1 else 0) + (1 if awq else 0)
+    """Library kernels one gemm call launches (the library's own plan: the
+    GEMM, a split-K reduction pass on the tile kernels, the AWQ activation
+    pass)."""
+    import w4a16_nvfp4_weight_gb300 as nv
+    return nv.gemm_plan(M, N, K, awq)["launches"]
 
 
 def launch_count(nv, L):

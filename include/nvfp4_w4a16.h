@@ -204,6 +204,24 @@ nvfp4_status nvfp4_w4a16_gemm_f16(const void* X, const void* repacked, const voi
                                   int64_t M, int64_t N, int64_t K, void* Y,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The launch plan nvfp4_w4a16_gemm / _f16 use for an M x N x K problem on the
+ * current device (the SM count decides wave sizes; without a device 148 SMs
+ * are assumed).  Host only: nothing is launched, no device memory is touched.
+ *  has_pre_quant_scale  0 or 1 (an AWQ scale adds one activation pass).
+ *  kernel_out    -1 nothing (M or N is 0), 0 split-K streaming decode kernel,
+ *                1 tile kernel with the dequantized weight in shared memory,
+ *                2 tile kernel with the dequantized weight in tensor memory.
+ *  tokens_out    activation rows per CTA tile (8 or 16 in the decode kernel).
+ *  splits_out    K splits (the decode kernel sums them inside a thread-block
+ *                cluster; the tile kernels add one FP32 reduction pass).
+ *  launches_out  kernels one call launches.
+ * Errors as nvfp4_w4a16_gemm's argument checks (null output pointer,
+ * negative size, K not a positive multiple of 16).
+ */
+nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale,
+                                   int* kernel_out, int* tokens_out, int* splits_out, int* launches_out);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped top-k MoE layer (FC1 gate/up + SwiGLU, FC2, weighted combine)     */
 /* ------------------------------------------------------------------------ */

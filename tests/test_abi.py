@@ -160,3 +160,30 @@ def test_moe_and_mlp_reject_bad_arguments_on_host(lib):
     assert fin(g, g, 2, 64, 2, g, None) == 1
     assert fin(None, g, 2, 64, 0, g, None) == 1
     assert fin(g, g, 2, 64, 0, V(0x100001), None) == 3
+
+
+def test_gemm_plan_on_host(lib):
+    """The launch plan query: host only, the same shape rules the GEMM entry
+    points use (no device here: 148 SMs assumed)."""
+    import w4a16_nvfp4_weight_gb300 as nv
+
+    assert nv.gemm_plan(0, 4096, 4096) == {"kernel": "none", "tokens": 0, "splits": 0, "launches": 0}
+    for M in (1, 8, 9, 16):
+        p = nv.gemm_plan(M, 4096, 4096)
+        assert p["kernel"] == "decode" and p["tokens"] == (8 if M <= 8 else 16) and p["launches"] == 1
+        assert 1 <= p["splits"] <= 8
+        assert nv.gemm_plan(M, 4096, 4096, has_pre_quant_scale=True)["launches"] == 2
+    # (M, N, K): tensor-memory-A tiles, shared-memory tiles, and a K split with its reduction pass
+    assert nv.gemm_plan(2048, 5120, 13824) == {"kernel": "tile_tmem", "tokens": 192, "splits": 1, "launches": 1}
+    assert nv.gemm_plan(2048, 13824, 5120) == {"kernel": "tile_smem", "tokens": 256, "splits": 1, "launches": 1}
+    p = nv.gemm_plan(512, 5120, 13824, has_pre_quant_scale=True)
+    assert p["kernel"] == "tile_smem" and p["splits"] > 1 and p["launches"] == 3
+    # few output tiles below M = 512 stay on the streaming kernel
+    assert nv.gemm_plan(300, 1000, 2064)["kernel"] == "decode"
+
+    out = [ctypes.c_int(0) for _ in range(4)]
+    refs = [ctypes.byref(o) for o in out]
+    assert lib.nvfp4_w4a16_gemm_plan(4, 64, 24, 0, *refs) == 2
+    assert lib.nvfp4_w4a16_gemm_plan(-1, 64, 64, 0, *refs) == 1
+    assert lib.nvfp4_w4a16_gemm_plan(4, 64, 64, 2, *refs) == 1
+    assert lib.nvfp4_w4a16_gemm_plan(4, 64, 64, 0, None, *refs[1:]) == 1

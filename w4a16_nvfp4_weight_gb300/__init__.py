@@ -118,6 +118,21 @@ def gemm_workspace_size(M, N, K, has_pre_quant_scale=False):
     return int(_lib.load().nvfp4_w4a16_gemm_workspace(M, N, K, 1 if has_pre_quant_scale else 0))
 
 
+GEMM_KERNELS = {-1: "none", 0: "decode", 1: "tile_smem", 2: "tile_tmem"}
+
+
+def gemm_plan(M, N, K, has_pre_quant_scale=False):
+    """The launch plan of gemm() for an M x N x K problem on the current device:
+    dict(kernel=name, tokens=rows per CTA tile, splits=K splits,
+    launches=kernels per call).  Host only."""
+    h = _lib.load()
+    out = [ctypes.c_int(0) for _ in range(4)]
+    _lib.check(h.nvfp4_w4a16_gemm_plan(M, N, K, 1 if has_pre_quant_scale else 0,
+                                       *[ctypes.byref(o) for o in out]))
+    kernel, tokens, splits, launches = (o.value for o in out)
+    return {"kernel": GEMM_KERNELS[kernel], "tokens": tokens, "splits": splits, "launches": launches}
+
+
 def gemm(x, w, pre_quant_scale=None, out=None, workspace=None):
     """Y[M, N] = X'[M, K] . W^T in the activation type of x (BF16 or FP16),
     X' = X or RN(X * pre_quant_scale)."""

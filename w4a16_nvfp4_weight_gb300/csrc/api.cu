@@ -210,6 +210,35 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, co
     return run_dense_gemm(X, repacked, pre_quant_scale, M, N, K, Y, workspace, workspace_bytes, false, stream);
 }
 
+extern "C" nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale,
+                                              int* kernel_out, int* tokens_out, int* splits_out,
+                                              int* launches_out) {
+    const char* fn = "nvfp4_w4a16_gemm_plan";
+    if (!kernel_out || !tokens_out || !splits_out || !launches_out)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: null output pointer", fn);
+    if (M < 0 || N < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: negative size M=%lld N=%lld", fn, (long long)M, (long long)N);
+    if (K <= 0 || K % kGroup != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld must be a positive multiple of 16", fn, (long long)K);
+    if (has_pre_quant_scale != 0 && has_pre_quant_scale != 1)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: has_pre_quant_scale=%d must be 0 or 1", fn, has_pre_quant_scale);
+    if (M == 0 || N == 0) {
+        *kernel_out = -1; *tokens_out = 0; *splits_out = 0; *launches_out = 0;
+        return NVFP4_OK;
+    }
+    if (use_tc_path(M, N)) {
+        bool wa = false;
+        int tok = 0, sp = 1;
+        tc_plan_info(M, N, K, &wa, &tok, &sp);
+        *kernel_out = wa ? 2 : 1; *tokens_out = tok; *splits_out = sp;
+        *launches_out = 1 + (sp > 1 ? 1 : 0) + has_pre_quant_scale;
+        return NVFP4_OK;
+    }
+    const DecodePlan pl = plan_decode(M, N, K);
+    if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld too large for the decode kernel", fn, (long long)K);
+    *kernel_out = 0; *tokens_out = 8 * pl.MT; *splits_out = pl.splits;
+    *launches_out = 1 + has_pre_quant_scale;
+    return NVFP4_OK;
+}
+
 extern "C" nvfp4_status nvfp4_w4a16_gemm_f16(const void* X, const void* repacked, const void* pre_quant_scale,
                                              int64_t M, int64_t N, int64_t K, void* Y,
                                              void* workspace, size_t workspace_bytes, void* stream) {

@@ -778,6 +778,13 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K) {
 
 }  // namespace
 
+void tc_plan_info(int64_t M, int64_t N, int64_t K, bool* wa, int* tokens, int* splits) {
+    const TcPlan pl = plan_tc(M, N, K);
+    *wa = pl.wa;
+    *tokens = pl.tok;
+    *splits = pl.splits;
+}
+
 bool use_tc_path(int64_t M, int64_t N) {
     if (M <= 16) return false;
     const int64_t tiles = ceil_div(N, kBN) * (M <= 128 ? ceil_div(M, 128) : ceil_div(M, 256));

@@ -44,6 +44,9 @@ nvfp4_status launch_tc_moe(const TcMoeParams& p, cudaStream_t stream);
 // Shape rule between the streaming (decode) kernel and the tile kernels: tiles
 // for M > 16 unless the tile grid would leave most SMs idle at M < 512.
 bool use_tc_path(int64_t M, int64_t N);
+// The dense tile plan of an M x N x K GEMM: the tensor-memory-A kernel (wa) or
+// the shared-memory-operand one, its tokens per tile and its K splits.
+void tc_plan_info(int64_t M, int64_t N, int64_t K, bool* wa, int* tokens, int* splits);
 size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs);
 nvfp4_status launch_tc(const TcParams& p, cudaStream_t stream);
 
