@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import Nvfp4Error
 
 __all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "swizzled_scales_size", "dequant", "gemm",
-           "gemm_workspace_size", "moe_grouped", "moe_workspace_size", "moe_finalize_pre_quant_scale",
+           "gemm_workspace_size", "gemm_plan", "moe_grouped", "moe_workspace_size", "moe_finalize_pre_quant_scale",
            "mlp", "mlp_workspace_size",
            "device_status",
            "abi_version"]
