@@ -217,33 +217,23 @@ decode_kernel(const DecodeParams p) {
                                    g * kXRowElems + q * 16;
         int s = 0;
         uint32_t phase = 0;
+        const uint32_t lut_s = smem_u32(lut);
         for (int i = 0; i < nst && ok; ++i) {
             if (!mbar_wait(&full[s], phase, p.status)) break;
-            const uint8_t* a = a0 + s * kStageBytes;
-            uint4 codes[kBlocksPerStage];
-            uint32_t sc[kBlocksPerStage];
-            #pragma unroll
-            for (int b = 0; b < kBlocksPerStage; ++b) {
-                codes[b] = *reinterpret_cast<const uint4*>(a + b * kBlockBytes + 16 * lane);
-                sc[b] = *reinterpret_cast<const uint16_t*>(a + b * kBlockBytes + kAtomCodeBytes + 2 * lane);
-            }
-            if (work) {
-                const uint16_t* xrow = x0 + s * (kStageBytes / 2);
-                const int nb = nkb - i * kBlocksPerStage;
-                #pragma unroll
-                for (int b = 0; b < kBlocksPerStage; ++b)
-                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], lut, xrow + b * kBlockK, acc);
-            }
+            if (work)
+                stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
+                    a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc);
             fence_proxy_async();           // reads of the stage before the next bulk copy into it
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (++s == kStages) { s = 0; phase ^= 1u; }
         }
 
-        // Push each partial to the CTA that reduces it: output e = token * 128 + row
-        // belongs to rank e / share and lands in that rank's slot for this rank.
+        // Push each partial of a token row with data to the CTA that reduces it:
+        // output e = token * rows + row belongs to rank e / share and lands in
+        // that rank's slot for this rank.  Token rows past M are never sent.
         const int c = lane & 3;
-        const int total = kRowsPerCta * TOK;
+        const int total = kRowsPerCta * rows_x;
         const int share = (total + p.splits - 1) / p.splits;
         #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -251,9 +241,11 @@ decode_kernel(const DecodeParams p) {
             for (int v = 0; v < 4; ++v) {
                 const int row = warp * 16 + g + (v >= 2 ? 8 : 0);
                 const int t = mt * 8 + 2 * c + (v & 1);
-                const int e = t * kRowsPerCta + row;
-                float* dst = cluster.map_shared_rank(part, e / share);
-                dst[split * share + e % share] = acc[mt][v];
+                if (t < rows_x) {
+                    const int e = t * kRowsPerCta + row;
+                    float* dst = cluster.map_shared_rank(part, e / share);
+                    dst[split * share + e % share] = acc[mt][v];
+                }
             }
         }
     }
@@ -261,7 +253,7 @@ decode_kernel(const DecodeParams p) {
 
     // Reduce this rank's share from local shared memory, ranks in order.
     if (*hdr_flag != 0) {
-        const int total = kRowsPerCta * TOK;
+        const int total = kRowsPerCta * rows_x;
         const int share = (total + p.splits - 1) / p.splits;
         const int e0 = split * share, e1 = min(total, e0 + share);
         for (int e = e0 + tid; e < e1; e += kThreads) {

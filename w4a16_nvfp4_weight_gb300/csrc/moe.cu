@@ -417,23 +417,12 @@ moe_linear_kernel(const MoeLinParams p) {
                                    g * kXRowElems + q * 16;
         int s = 0;
         uint32_t phase = 0;
+        const uint32_t lut_s = smem_u32(wlut);
         for (int i = 0; i < nst && ok; ++i) {
             if (!mbar_wait(&full[s], phase, p.status)) break;
-            const uint8_t* a = a0 + s * kStageBytes;
-            uint4 codes[kBlocksPerStage];
-            uint32_t sc[kBlocksPerStage];
-            #pragma unroll
-            for (int b = 0; b < kBlocksPerStage; ++b) {
-                codes[b] = *reinterpret_cast<const uint4*>(a + b * kBlockBytes + 16 * lane);
-                sc[b] = *reinterpret_cast<const uint16_t*>(a + b * kBlockBytes + kAtomCodeBytes + 2 * lane);
-            }
-            if (rows_valid) {
-                const uint16_t* xr = x0 + s * (kStageBytes / 2);
-                const int nb = nkb - i * kBlocksPerStage;
-                #pragma unroll
-                for (int b = 0; b < kBlocksPerStage; ++b)
-                    if (b < nb) atom_mma<MT, kXRowElems, F16>(codes[b], sc[b], wlut, xr + b * kBlockK, acc);
-            }
+            if (rows_valid)
+                stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
+                    a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc);
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);

@@ -4,6 +4,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace nvfp4 {
 
@@ -45,16 +46,37 @@ __device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint3
     }
 }
 
+// Magnitude-table entry `code` of the table at shared address `lut_s`: the
+// address is formed with a multiply-add, which issues on the FMA pipe and
+// leaves the integer pipe to the code expansion.
+__device__ __forceinline__ Lut lut_entry(uint32_t lut_s, uint32_t code) {
+    uint32_t addr;
+    asm("mad.lo.u32 %0, %1, 16, %2;" : "=r"(addr) : "r"(code), "r"(lut_s));
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return lut_from_uint4(v);
+}
+
+// One shared-memory byte, zero-extended by the load itself (no integer-pipe
+// extraction of the two scale codes a lane owns).
+__device__ __forceinline__ uint32_t lds_u8(uint32_t saddr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(saddr));
+    return v;
+}
+
 // One atom: a lane holds 16 code bytes (rows g and g+8 of the atom, group q)
-// and the two scale codes; xrow points at token row g, group q of the
-// activation chunk (row stride XS elements, 16-byte aligned).  Within the
-// group the MMA's k order is permuted -- MMA j consumes k = 4j..4j+3 of every
-// lane's group -- and the activation fragments use the same permutation.
+// and their two scale codes sc0 (row g) and sc1 (row g+8); xrow points at
+// token row g, group q of the activation chunk (row stride XS elements,
+// 16-byte aligned).  Within the group the MMA's k order is permuted -- MMA j
+// consumes k = 4j..4j+3 of every lane's group -- and the activation fragments
+// use the same permutation.
 template <int MT, int XS, bool F16>
-__device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const uint4* lut,
+__device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc0, uint32_t sc1, uint32_t lut_s,
                                          const uint16_t* xrow, float acc[MT][4]) {
-    const Lut t0 = lut_from_uint4(lut[sc2 & 0xFF]);
-    const Lut t1 = lut_from_uint4(lut[(sc2 >> 8) & 0xFF]);
+    const Lut t0 = lut_entry(lut_s, sc0);
+    const Lut t1 = lut_entry(lut_s, sc1);
     uint32_t ra[8], rb[8];
     expand8(codes.x, t0, ra);
     expand8(codes.y, t0, ra + 4);
@@ -72,6 +94,32 @@ __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc2, const 
         mma_16816<F16>(acc[mt], a1, b01.z, b01.w);
         mma_16816<F16>(acc[mt], a2, b23.x, b23.y);
         mma_16816<F16>(acc[mt], a3, b23.z, b23.w);
+    }
+}
+
+// One ring stage of B 64-k blocks (block stride BLK bytes; this warp's atom at
+// `a`, its activation chunk at `xrow`), nb of them holding data.  Full stages
+// take a loop without per-block bounds checks; only the last stage of a K
+// slice can be partial.
+template <int MT, int XS, bool F16, int B, uint32_t BLK>
+__device__ __forceinline__ void stage_mma(const uint8_t* a, int lane, uint32_t lut_s, const uint16_t* xrow,
+                                          int nb, float acc[MT][4]) {
+    uint4 codes[B];
+    uint32_t s0[B], s1[B];
+    const uint32_t sa = smem_u32(a) + kAtomCodeBytes + 2 * lane;
+    #pragma unroll
+    for (int b = 0; b < B; ++b) {
+        codes[b] = *reinterpret_cast<const uint4*>(a + b * BLK + 16 * lane);
+        s0[b] = lds_u8(sa + b * BLK);
+        s1[b] = lds_u8(sa + b * BLK + 1);
+    }
+    if (nb >= B) {
+        #pragma unroll
+        for (int b = 0; b < B; ++b) atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc);
+    } else {
+        #pragma unroll
+        for (int b = 0; b < B; ++b)
+            if (b < nb) atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc);
     }
 }
 
