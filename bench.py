@@ -215,8 +215,9 @@ def bits_tensor(bits, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(act_torch()).to(device)
 
 
-def build_decode_workload(nv, synth, device):
-    """Weights (distinct copy per GEMM of a step) and activations."""
+def build_decode_workload(nv, synth, device, awq=False):
+    """Weights (distinct copy per GEMM of a step) and activations (with a
+    per-channel AWQ pre-quant scale per GEMM when awq)."""
     launches = []
     base = {}
     for si, (K, N) in enumerate(DECODE_SHAPES):
@@ -230,8 +231,10 @@ def build_decode_workload(nv, synth, device):
             w0 = base[(K, N)][0]
             w = nv.NVFP4Weight(w0.buf.clone(), N, K)       # a copy per GEMM: no L2 reuse in a step
             x_bits = synth.normal_act(r, (M, K), ACT)
+            pqs_bits = synth.awq_scale_bits(r, K, ACT) if awq else None
             launches.append(dict(M=M, K=K, N=N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits,
-                                 pqs=None, y=torch.empty((M, N), dtype=act_torch(), device=device)))
+                                 pqs_bits=pqs_bits, pqs=bits_tensor(pqs_bits, device) if awq else None,
+                                 y=torch.empty((M, N), dtype=act_torch(), device=device)))
     return launches, base
 
 
@@ -263,9 +266,10 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     wl = args.workload
     if wl == "decode":
-        launches, base = build_decode_workload(nv, synth, device)
+        launches, base = build_decode_workload(nv, synth, device, awq=args.awq)
         config = {"workload": "decode dense linears M{1,2,4,8,16} x (K,N){(4096,4096),(4096,14336),"
-                              "(14336,4096),(5120,25600)}", "gemms_per_step": len(launches)}
+                              "(14336,4096),(5120,25600)}" + (" with AWQ" if args.awq else ""),
+                  "gemms_per_step": len(launches)}
     elif wl == "prefill":
         shapes = [(M, K, N) for M in (512, 2048, 8192) for (K, N) in ((5120, 13824), (13824, 5120), (8192, 28672))]
         launches, base = build_dense_workload(nv, synth, device, shapes, 2, awq=args.awq)

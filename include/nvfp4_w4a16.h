@@ -184,6 +184,10 @@ size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_q
  * split-K HBM-streaming decode kernel; other shapes one of two tensor-core
  * tile kernels (dequantized weight in shared memory, or in tensor memory as
  * the MMA's A operand), chosen per shape; results agree within rounding.
+ * The decode kernel applies pre_quant_scale to the activation fragments it
+ * feeds to the MMAs (one packed BF16/FP16 multiply, the same single rounding),
+ * so it needs no workspace and no extra launch; the tile kernels write X' into
+ * the workspace first.
  * The GEMM kernels use programmatic dependent launch: they may begin reading
  * the repacked weight before the preceding kernel of the stream has finished
  * (only if that kernel itself allows its dependents to start early), and read
@@ -225,6 +229,29 @@ nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int has_pre_
 /* ------------------------------------------------------------------------ */
 /* Grouped top-k MoE layer (FC1 gate/up + SwiGLU, FC2, weighted combine)     */
 /* ------------------------------------------------------------------------ */
+
+/*
+ * The MoE layer's routing step on its own (the same kernels the layer runs
+ * first): per token the top-k of its FP32 router logits (ties to the lower
+ * expert index, slots in descending-logit order) and p = softmax over the k
+ * selected logits; then the routing slots s = t*topk + j sorted by expert,
+ * then token, then slot (stable).  "[TRTLLM-12288][feat] Support Nemotron-H
+ * nvfp4 ckpt on Hopper", Changes table (MoE: only the routed, active experts'
+ * weights are dequantized -- the permutation groups each expert's rows).
+ *  router_logits    device FP32 [T, E].
+ *  topk_idx_out     device int32 [T, topk]: selected experts.
+ *  topk_weight_out  device FP32 [T, topk]: routing weights p.
+ *  perm_out         device int32 [T*topk]: perm[i] = the slot at sorted position i.
+ *  inv_out          device int32 [T*topk]: its inverse, inv[perm[i]] = i.
+ *  offsets_out      device int32 [E+1]: exclusive scan of the per-expert slot
+ *                   counts (expert e owns sorted positions [offsets[e], offsets[e+1])).
+ * All outputs are required and 4-byte aligned.  Limits as the layer: E <= 256,
+ * topk <= 16, topk <= E, T*topk < 2^31.  T == 0 returns NVFP4_OK and launches
+ * nothing (no output is written).  No workspace.
+ */
+nvfp4_status nvfp4_moe_route(const float* router_logits, int64_t T, int E, int topk,
+                             int32_t* topk_idx_out, float* topk_weight_out, int32_t* perm_out,
+                             int32_t* inv_out, int32_t* offsets_out, void* stream);
 
 size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t I);
 
@@ -350,12 +377,15 @@ nvfp4_status nvfp4_w4a16_mlp_f16(const void* X, const void* fc1, const void* fc2
  * device variable of this library, so every GPU that loads the library holds
  * it until the process exits.  Problems whose nvfp4_w4a16_moe_workspace()
  * exceeds that size are rejected with NVFP4_ERR_UNSUPPORTED_SHAPE (with
- * E=128, topk=8, H=2048, I=768 that allows up to T=204 tokens per call).  The entry point itself calls
+ * E=128, topk=8, H=2048, I=768 that allows up to T=215 tokens per call).  The entry point itself calls
  * no allocating routine.  The first call on a device looks the scratch address
  * up (cudaGetSymbolAddress, which may load the library's device code), so make
  * that first call before any stream capture.  Every call shares the one array;
  * nothing in it has to start at zero, but calls that overlap on the GPU (on
- * different streams) race on it and give wrong results.
+ * different streams) race on it and give wrong results.  The looked-up address
+ * (like that of the status word behind nvfp4_device_status) is kept for the
+ * life of the process, so the library must not be used across a reset of the
+ * device (cudaDeviceReset), which may load its device code at another address.
  */
 size_t nvfp4_w4a16_moe_noalloc_scratch_bytes(void);
 nvfp4_status nvfp4_w4a16_moe_grouped_noalloc(const void* X, const float* router_logits,

@@ -140,6 +140,16 @@ def test_moe_and_mlp_reject_bad_arguments_on_host(lib):
     assert moe(ws=V(0x100040)) == 3
     assert moe(T=10_000_000) == 2                         # more work items than one grid dimension holds
 
+    def route(lg=g, T=4, E=128, k=8, idx=g, p=g, perm=g, inv=g, offs=g):
+        return lib.nvfp4_moe_route(lg, T, E, k, idx, p, perm, inv, offs, None)
+
+    assert route(T=-1) == 1
+    assert route(E=0) == 2 and route(E=257) == 2 and route(E=4, k=5) == 2 and route(k=17) == 2
+    assert route(T=1 << 28) == 2                          # T * topk past int32 slot indices
+    assert route(lg=None, idx=None, p=None, perm=None, inv=None, offs=None, T=0) == 0
+    assert route(inv=None) == 1 and "null" in _err(lib)
+    assert route(perm=V(0x100002)) == 3
+
     def mlp(X=g, w1=g, w2=g, pqs=None, T=4, H=4096, I=14336, out=g, ws=g, wsb=big):
         return lib.nvfp4_w4a16_mlp(X, w1, w2, pqs, T, H, I, out, ws, wsb, None)
 
@@ -164,7 +174,11 @@ def test_moe_and_mlp_reject_bad_arguments_on_host(lib):
 
 def test_gemm_plan_on_host(lib):
     """The launch plan query: host only, the same shape rules the GEMM entry
-    points use (no device here: 148 SMs assumed)."""
+    points use (without a device 148 SMs are assumed; with one, its SM count
+    decides the wave sizes, so the exact tile plans are checked only at the SM
+    counts they were derived for)."""
+    import torch
+
     import w4a16_nvfp4_weight_gb300 as nv
 
     assert nv.gemm_plan(0, 4096, 4096) == {"kernel": "none", "tokens": 0, "splits": 0, "launches": 0}
@@ -172,14 +186,18 @@ def test_gemm_plan_on_host(lib):
         p = nv.gemm_plan(M, 4096, 4096)
         assert p["kernel"] == "decode" and p["tokens"] == (8 if M <= 8 else 16) and p["launches"] == 1
         assert 1 <= p["splits"] <= 8
-        assert nv.gemm_plan(M, 4096, 4096, has_pre_quant_scale=True)["launches"] == 2
-    # (M, N, K): tensor-memory-A tiles, shared-memory tiles, and a K split with its reduction pass
-    assert nv.gemm_plan(2048, 5120, 13824) == {"kernel": "tile_tmem", "tokens": 192, "splits": 1, "launches": 1}
-    assert nv.gemm_plan(2048, 13824, 5120) == {"kernel": "tile_smem", "tokens": 256, "splits": 1, "launches": 1}
-    p = nv.gemm_plan(512, 5120, 13824, has_pre_quant_scale=True)
-    assert p["kernel"] == "tile_smem" and p["splits"] > 1 and p["launches"] == 3
+        # the decode kernel applies the AWQ scale itself: no extra pass, no workspace
+        assert nv.gemm_plan(M, 4096, 4096, has_pre_quant_scale=True)["launches"] == 1
+        assert nv.gemm_workspace_size(M, 4096, 4096, True) == 0
     # few output tiles below M = 512 stay on the streaming kernel
     assert nv.gemm_plan(300, 1000, 2064)["kernel"] == "decode"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    if sms in (148, 152):
+        # (M, N, K): tensor-memory-A tiles, shared-memory tiles, and a K split with its reduction pass
+        assert nv.gemm_plan(2048, 5120, 13824) == {"kernel": "tile_tmem", "tokens": 192, "splits": 1, "launches": 1}
+        assert nv.gemm_plan(2048, 13824, 5120) == {"kernel": "tile_smem", "tokens": 256, "splits": 1, "launches": 1}
+        p = nv.gemm_plan(512, 5120, 13824, has_pre_quant_scale=True)
+        assert p["kernel"] == "tile_smem" and p["splits"] > 1 and p["launches"] == 3
 
     out = [ctypes.c_int(0) for _ in range(4)]
     refs = [ctypes.byref(o) for o in out]

@@ -132,8 +132,34 @@ def full_experts():
     return E, H, I, fc1, fc2, _device_experts(fc1, 2 * I, H), _device_experts(fc2, H, I)
 
 
+def _covering_tokens(idx, E, at_least, seed):
+    """A seeded token sample whose routed experts cover all E experts (tokens
+    are taken in a seeded order when they add an uncovered expert), topped up
+    with further seeded tokens to `at_least` (or all tokens)."""
+    T = idx.shape[0]
+    order = synth.rng(seed).permutation(T)
+    chosen, covered = [], set()
+    for t in order:
+        new = set(int(e) for e in idx[t]) - covered
+        if new:
+            chosen.append(int(t))
+            covered |= new
+        if len(covered) == E:
+            break
+    for t in order:
+        if len(chosen) >= min(at_least, T):
+            break
+        if int(t) not in chosen:
+            chosen.append(int(t))
+    return sorted(chosen), covered
+
+
 @pytest.mark.parametrize("T", [1, 16, 256, 4096])
 def test_moe_full_size_sampled(full_experts, T):
+    """The full layer.  At T = 256 (16 rows per expert: streaming kernels) and
+    T = 4096 (256 rows per expert: gathered rows on the tcgen05 tile kernels)
+    at least 64 tokens are compared, chosen so that their routing reaches every
+    one of the 128 experts, i.e. every expert's FC1 and FC2 work is checked."""
     E, H, I, fc1, fc2, d1, d2 = full_experts
     c = synth.moe_case(T, synth.seed_for(3, T), E=E, topk=8, H=H, I=I, weights=(fc1, fc2))
     x = gu.bits_to_bf16_tensor(c.x_bits)
@@ -142,7 +168,47 @@ def test_moe_full_size_sampled(full_experts, T):
     gu.check_device_status()
     out = gu.tensor_to_bits(out)
     routing = {k: v.cpu().numpy() for k, v in r.items()}
-    tokens = sorted(set([0, T - 1, T // 2]))
+    ref_routing = omoe.route(c.logits, 8)
+    if T >= 256:
+        tokens, covered = _covering_tokens(ref_routing[0], E, 64, seed=T)
+        assert len(covered) == E and len(tokens) >= 64
+    else:
+        tokens = sorted(set([0, T - 1, T // 2]))
     ref = _oracle(c, tokens=tokens)
     _check_routing(routing, ref, T, 8, E)
     gu.compare(out[tokens], ref["out_bits"], f"MoE T={T} sampled")
+
+
+@pytest.mark.parametrize("T", [1, 16, 64, 65, 256, 4096])
+def test_moe_route_tables_bit_exact(T):
+    """The standalone routing call (the same kernels the layer runs first: the
+    fused single-CTA kernel up to 64 tokens, two kernels above) against the
+    oracle: top-k indices, the stable permutation, its inverse and the expert
+    offsets bit for bit, the routing weights to float32 rounding; and the layer
+    reports the same tables."""
+    E, topk = 128, 8
+    c = synth.moe_case(T, synth.seed_for(3, T) + 7, E=E, topk=topk, H=64, I=64, weights=None)
+    logits = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
+    got = {k: v.cpu().numpy() for k, v in nv.moe_route(logits, topk).items()}
+    gu.check_device_status()
+    idx, p = omoe.route(c.logits, topk)
+    counts, offsets, perm, inv = omoe.permute(idx, E)
+    assert np.array_equal(got["idx"], idx)
+    assert np.allclose(got["p"], p, rtol=2e-6, atol=1e-7)
+    assert np.array_equal(got["perm"], perm)
+    assert np.array_equal(got["inv"], inv)
+    assert np.array_equal(got["offsets"], offsets)
+    assert np.array_equal(got["inv"][got["perm"]], np.arange(T * topk))
+
+
+def test_moe_route_ties_and_negative_zero():
+    logits = np.zeros((3, 8), dtype=np.float32)
+    logits[0, [6, 1, 4]] = 2.0                 # three-way tie at the top
+    logits[1, :] = -0.0
+    logits[2, 3] = np.float32(-0.0)
+    got = {k: v.cpu().numpy() for k, v in nv.moe_route(torch.from_numpy(logits).cuda(), 3).items()}
+    idx, p = omoe.route(logits, 3)
+    _, offsets, perm, inv = omoe.permute(idx, 8)
+    assert got["idx"][0].tolist() == [1, 4, 6]
+    for k, v in (("idx", idx), ("perm", perm), ("inv", inv), ("offsets", offsets)):
+        assert np.array_equal(got[k], v), k

@@ -33,12 +33,14 @@ def _experts(weights, N, K):
     return buf
 
 
-def test_noalloc_matches_workspace_entry_point(lib):
-    T, E, topk, H, I = 48, 16, 4, 256, 128
-    r = synth.rng(2024)
+def _check_against_workspace_entry_point(lib, T, E, topk, H, I, seed):
+    """Two allocation-free calls in a row give exactly the bytes of the regular
+    entry point: both run the same kernels on the same inputs, only the memory
+    that holds the intermediate tables and rows differs."""
+    r = synth.rng(seed)
     fc1 = [synth.quantize(synth.normal_weight(r, 2 * I, H)) for _ in range(E)]
     fc2 = [synth.quantize(synth.normal_weight(r, H, I)) for _ in range(E)]
-    c = synth.moe_case(T, 2025, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=True)
+    c = synth.moe_case(T, seed + 1, E=E, topk=topk, H=H, I=I, weights=(fc1, fc2), awq=True)
     d1, d2 = _experts(fc1, 2 * I, H), _experts(fc2, H, I)
     x = gu.bits_to_bf16_tensor(c.x_bits)
     pqs = gu.bits_to_bf16_tensor(c.pqs_bits)
@@ -56,12 +58,26 @@ def test_noalloc_matches_workspace_entry_point(lib):
         gu.check_device_status()
         got = gu.tensor_to_bits(out)
         gu.compare(got, ref, "allocation-free MoE")
+        assert np.array_equal(got, ref), "allocation-free MoE differs from the workspace entry point"
+
+
+def test_noalloc_matches_workspace_entry_point(lib):
+    # 48 tokens x top-4 over 16 experts: 12 rows per expert, the streaming kernels
+    _check_against_workspace_entry_point(lib, 48, 16, 4, 256, 128, 2024)
+
+
+def test_noalloc_tile_path_matches_workspace_entry_point(lib):
+    # 128 tokens x top-4 over 16 experts: 32 rows per expert and I a multiple of
+    # 128, so the layer gathers rows and runs the tcgen05 tile kernels, with the
+    # gathered rows and FP32 partials at their own offsets in the scratch array
+    _check_against_workspace_entry_point(lib, 128, 16, 4, 256, 128, 2026)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
-    # 128 experts, top-8, hidden 2048, intermediate 768: 205 tokens need more than 16 MiB
-    assert nv.moe_workspace_size(205, 128, 8, 2048, 768) > lib.nvfp4_w4a16_moe_noalloc_scratch_bytes()
-    st = lib.nvfp4_w4a16_moe_grouped_noalloc(None, None, None, None, None, 205, 128, 8, 2048, 768,
+    # 128 experts, top-8, hidden 2048, intermediate 768: 216 tokens need more than 16 MiB
+    assert nv.moe_workspace_size(215, 128, 8, 2048, 768) <= lib.nvfp4_w4a16_moe_noalloc_scratch_bytes()
+    assert nv.moe_workspace_size(216, 128, 8, 2048, 768) > lib.nvfp4_w4a16_moe_noalloc_scratch_bytes()
+    st = lib.nvfp4_w4a16_moe_grouped_noalloc(None, None, None, None, None, 216, 128, 8, 2048, 768,
                                              None, None, None, None, None, None)
     assert st == 2
     assert "scratch" in lib.nvfp4_last_error().decode()

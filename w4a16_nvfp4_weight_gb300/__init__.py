@@ -23,7 +23,8 @@ from . import _lib
 from ._lib import Nvfp4Error
 
 __all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "swizzled_scales_size", "dequant", "gemm",
-           "gemm_workspace_size", "gemm_plan", "moe_grouped", "moe_workspace_size", "moe_finalize_pre_quant_scale",
+           "gemm_workspace_size", "gemm_plan", "moe_grouped", "moe_route", "moe_workspace_size",
+           "moe_finalize_pre_quant_scale",
            "mlp", "mlp_workspace_size",
            "device_status",
            "abi_version"]
@@ -157,6 +158,25 @@ def gemm(x, w, pre_quant_scale=None, out=None, workspace=None):
     _lib.check(fn(_ptr(x), _ptr(w.buf), _ptr(pre_quant_scale), M, w.N, w.K,
                   _ptr(out), _ptr(workspace), ws_bytes, _stream()))
     return out
+
+
+def moe_route(router_logits, topk):
+    """The MoE routing step alone: dict(idx [T, topk] int32, p [T, topk]
+    float32, perm [T*topk] int32, inv [T*topk] int32, offsets [E+1] int32)."""
+    h = _lib.load()
+    _require_cuda(router_logits, "router_logits", torch.float32)
+    if router_logits.dim() != 2:
+        raise Nvfp4Error(2, f"router_logits must be [T, E], got {tuple(router_logits.shape)}")
+    T, E = router_logits.shape
+    dev = router_logits.device
+    idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    p = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    perm = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    _lib.check(h.nvfp4_moe_route(_ptr(router_logits), T, E, topk, _ptr(idx), _ptr(p), _ptr(perm), _ptr(inv),
+                                 _ptr(offsets), _stream()))
+    return dict(idx=idx, p=p, perm=perm, inv=inv, offsets=offsets)
 
 
 def moe_workspace_size(T, E, topk, H, I):

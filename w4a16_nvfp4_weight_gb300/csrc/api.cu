@@ -78,7 +78,7 @@ struct DecodePlan {
     bool ok;
 };
 
-DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
+DecodePlan plan_decode(int64_t M, int64_t N, int64_t K, bool f16, bool awq) {
     const int MT = M <= 8 ? 1 : 2;
     const int64_t TOK = 8 * MT;
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
@@ -91,7 +91,7 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
         DecodePlan pl{};
         pl.MT = MT; pl.ring = ring; pl.W = W; pl.ok = true;
         const int64_t base = ceil_div(N, (int64_t)W * kAtomRows) * mchunks;
-        const int64_t target = (int64_t)decode_ctas_per_sm(MT, ring, W) * sms;
+        const int64_t target = (int64_t)decode_ctas_per_sm(MT, ring, W, f16, awq) * sms;
         int64_t splits = std::max<int64_t>(1, target / std::max<int64_t>(base, 1));
         splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / 2)));
         const int64_t kbs = ceil_div(KB, splits);
@@ -116,16 +116,13 @@ DecodePlan plan_decode(int64_t M, int64_t N, int64_t K) {
     // output rows, the split capped by the cluster size) leaves SMs idle -- the
     // block scheduler also stacks such grids' clusters on part of the SMs --
     // so it takes 64-row CTAs instead, twice as many.
-    const int64_t wave = (int64_t)decode_ctas_per_sm(MT, pl.ring, 8) * sms;
+    const int64_t wave = (int64_t)decode_ctas_per_sm(MT, pl.ring, 8, f16, awq) * sms;
     if (pl.ctas * 4 < wave * 3) {
         const DecodePlan half = plan_rings(4);
         if (half.ctas > pl.ctas) pl = half;
     }
     return pl;
 }
-
-// Bytes of the AWQ-scaled activation copy the decode path keeps in the workspace.
-size_t awq_bytes(int64_t M, int64_t K) { return (size_t)round_up(M * K * 2, 256); }
 
 }  // namespace nvfp4
 
@@ -155,7 +152,7 @@ extern "C" nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stre
 extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
     if (use_tc_path(M, N)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
-    return has_pre_quant_scale ? awq_bytes(M, K) : 0;
+    return 0;               // the decode kernel applies AWQ to its activation fragments
 }
 
 nvfp4_status nvfp4::run_dense_gemm(const void* X, const void* repacked, const void* pre_quant_scale, int64_t M,
@@ -185,18 +182,10 @@ nvfp4_status nvfp4::run_dense_gemm(const void* X, const void* repacked, const vo
         tp.workspace = workspace; tp.workspace_bytes = workspace_bytes;
         return launch_tc(tp, s);
     }
-    const DecodePlan pl = plan_decode(M, N, K);
+    const DecodePlan pl = plan_decode(M, N, K, f16, pre_quant_scale != nullptr);
     if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld too large for the decode kernel", fn, (long long)K);
-    const uint16_t* xin = (const uint16_t*)X;
-    if (pre_quant_scale) {
-        // x' = RN(x * pre_quant_scale) into the workspace, then the GEMM reads x'
-        nvfp4_status st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)pre_quant_scale,
-                                           (uint16_t*)workspace, M, K, f16, s);
-        if (st != NVFP4_OK) return st;
-        xin = (const uint16_t*)workspace;
-    }
     DecodeParams p{};
-    p.X = xin; p.pqs = nullptr;
+    p.X = (const uint16_t*)X; p.pqs = (const uint16_t*)pre_quant_scale;
     p.rp = (const uint8_t*)repacked; p.Y = (uint16_t*)Y;
     p.M = M; p.N = N; p.K = K;
     p.KB = round_up(K, kBlockK) / kBlockK;
@@ -232,10 +221,10 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, i
         *launches_out = 1 + (sp > 1 ? 1 : 0) + has_pre_quant_scale;
         return NVFP4_OK;
     }
-    const DecodePlan pl = plan_decode(M, N, K);
+    const DecodePlan pl = plan_decode(M, N, K, false, has_pre_quant_scale != 0);
     if (!pl.ok) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: K=%lld too large for the decode kernel", fn, (long long)K);
     *kernel_out = 0; *tokens_out = 8 * pl.MT; *splits_out = pl.splits;
-    *launches_out = 1 + has_pre_quant_scale;
+    *launches_out = 1;            // AWQ is applied inside the decode kernel
     return NVFP4_OK;
 }
 

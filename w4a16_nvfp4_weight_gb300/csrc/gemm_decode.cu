@@ -15,8 +15,11 @@
 // same permutation, so the dot products are unchanged.  K is split across the
 // CTAs of a thread-block cluster, which reduce their FP32 partials through
 // distributed shared memory in rank order: deterministic, and no global
-// workspace.  The AWQ pre-quant scale, when present, is applied by a small
-// pass that writes x' = RN(x * s) (BF16 or FP16) into the workspace first.
+// workspace.  The AWQ pre-quant scale, when present, is applied to each ring
+// stage's activation rows in shared memory, once, by the consumer warps
+// together (each loads its share of the scales a stage ahead): x' = RN(x * s)
+// in BF16 (or FP16), one packed multiply per pair, no extra pass and no
+// workspace.
 //
 // The kernel is launched with programmatic dependent launch: it lets the next
 // kernel of the stream start early, and it streams its first weight stages
@@ -28,6 +31,7 @@
 // and run a BF16 GEMM); AWQ activation scaling from "[None][fix] Apply the
 // NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL" (Description).
 #include <algorithm>
+#include <mutex>
 
 #include <cooperative_groups.h>
 
@@ -80,7 +84,7 @@ struct Smem {
     static constexpr size_t ring = lut + kLutBytes;
 };
 
-template <int MT, int R, bool F16, int W>
+template <int MT, int R, bool F16, int W, bool AWQ>
 __global__ void __launch_bounds__(Cta<W>::kThreads)
 decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -205,11 +209,14 @@ decode_kernel(const DecodeParams p) {
             }
         }
         __syncwarp();
+        __syncwarp();
     } else {
         // ---------------- consumers
         const bool rows_valid = (int64_t)rg * kRowsPerCta + warp * kAtomRows < p.N;
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        // the AWQ stages synchronise the consumer warps: they must all run the loop
+        if constexpr (AWQ) ok = named_bar_red_and(1, kWarps * 32, ok);
         const bool work = rows_valid;
         // This lane's bytes of stage 0; stage s is kStageBytes further on.
         const uint8_t* const a0 = ring + warp * kAtomBytes;
@@ -218,8 +225,32 @@ decode_kernel(const DecodeParams p) {
         int s = 0;
         uint32_t phase = 0;
         const uint32_t lut_s = smem_u32(lut);
+        // AWQ: k of stage i and the k it holds (a multiple of 16)
+        auto stage_kx = [&](int i) { return (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK; };
+        auto stage_xk = [&](int i) {
+            const int64_t left = p.K - stage_kx(i);
+            const int full_k = min(kBlocksPerStage, nkb - i * kBlocksPerStage) * kBlockK;
+            return (int)(left < full_k ? left : full_k);
+        };
+        using AwqStagesT = AwqStages<F16, kXRowElems, TOK, kBlocksPerStage, kWarps * 32>;
+        AwqStagesT awq;
+        if constexpr (AWQ) if (ok && nst > 0) awq.prefetch(p.pqs + stage_kx(0), rows_x, stage_xk(0), tid);
         for (int i = 0; i < nst && ok; ++i) {
-            if (!mbar_wait(&full[s], phase, p.status)) break;
+            const bool got = mbar_wait(&full[s], phase, p.status);
+            if constexpr (!AWQ) {
+                if (!got) break;
+            } else {
+                // x' = RN(x * pre_quant_scale) once per stage, shared by the consumer
+                // warps; the next stage's scales are read while this one is scaled
+                AwqStagesT nxt = awq;
+                if (i + 1 < nst) nxt.prefetch(p.pqs + stage_kx(i + 1), rows_x, stage_xk(i + 1), tid);
+                if (got)
+                    awq.apply(reinterpret_cast<uint16_t*>(ring + s * kStageBytes + kWeightStageBytes), rows_x,
+                              stage_xk(i), tid);
+                awq = nxt;
+                // every consumer warp has scaled its share (or all stop together)
+                if (!named_bar_red_and(1, kWarps * 32, got)) break;
+            }
             if (work)
                 stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
                     a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc);
@@ -313,46 +344,80 @@ size_t decode_smem_bytes(int MT, int ring, int W) {
     return ring == kRingDeep ? smem_bytes_w<2, kRingDeep>(W) : smem_bytes_w<2, kRingShallow>(W);
 }
 
-int decode_ctas_per_sm(int MT, int ring, int W) {
+int decode_ctas_per_sm(int MT, int ring, int W, bool f16, bool awq) {
     // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA;
-    // 2048 threads per SM
+    // 2048 threads and 64 K registers per SM (registers are allocated per warp
+    // in units of 256); the kernel instance's register count is read once
     constexpr size_t kSmemPerSm = 228 * 1024, kReservedPerCta = 1024;
     const size_t per_cta = decode_smem_bytes(MT, ring, W) + kReservedPerCta;
     const int by_smem = (int)(kSmemPerSm / per_cta);
     const int by_threads = 2048 / ((W + 1) * 32);
-    const int n = by_smem < by_threads ? by_smem : by_threads;
+    int n = by_smem < by_threads ? by_smem : by_threads;
+    const int regs = decode_kernel_regs(MT, ring, W, f16, awq);
+    if (regs > 0) {
+        const int per_warp = (regs * 32 + 255) / 256 * 256;
+        const int by_regs = 65536 / (per_warp * (W + 1));
+        n = n < by_regs ? n : by_regs;
+    }
     return n < 1 ? 1 : n;
+}
+
+// The kernel instance for the activation type and AWQ choice of `p`.
+template <int MT, int R, int W>
+auto decode_instance(bool f16, bool awq) {
+    return f16 ? (awq ? decode_kernel<MT, R, true, W, true> : decode_kernel<MT, R, true, W, false>)
+               : (awq ? decode_kernel<MT, R, false, W, true> : decode_kernel<MT, R, false, W, false>);
 }
 
 template <int MT, int R, int W>
 cudaError_t launch_decode_ex(const cudaLaunchConfig_t& cfg, bool f16, const DecodeParams& p) {
-    return f16 ? cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, true, W>, p)
-               : cudaLaunchKernelEx(&cfg, decode_kernel<MT, R, false, W>, p);
+    return cudaLaunchKernelEx(&cfg, decode_instance<MT, R, W>(f16, p.pqs != nullptr), p);
 }
 
 template <int MT, int R, int W>
-const void* decode_fn(bool f16) {
-    return f16 ? (const void*)decode_kernel<MT, R, true, W> : (const void*)decode_kernel<MT, R, false, W>;
+const void* decode_fn(bool f16, bool awq) {
+    return (const void*)decode_instance<MT, R, W>(f16, awq);
 }
 
 // The kernel instance for (MT, ring, W): its address and a launch of it.
 template <int W>
 cudaError_t launch_decode_w(const cudaLaunchConfig_t& cfg, int MT, int ring, bool f16, const DecodeParams& p,
                             const void** fn_out) {
+    const bool awq = p.pqs != nullptr;
     if (MT == 1) {
         if (ring == kRingDeep) {
-            if (fn_out) { *fn_out = decode_fn<1, kRingDeep, W>(f16); return cudaSuccess; }
+            if (fn_out) { *fn_out = decode_fn<1, kRingDeep, W>(f16, awq); return cudaSuccess; }
             return launch_decode_ex<1, kRingDeep, W>(cfg, f16, p);
         }
-        if (fn_out) { *fn_out = decode_fn<1, kRingShallow, W>(f16); return cudaSuccess; }
+        if (fn_out) { *fn_out = decode_fn<1, kRingShallow, W>(f16, awq); return cudaSuccess; }
         return launch_decode_ex<1, kRingShallow, W>(cfg, f16, p);
     }
     if (ring == kRingDeep) {
-        if (fn_out) { *fn_out = decode_fn<2, kRingDeep, W>(f16); return cudaSuccess; }
+        if (fn_out) { *fn_out = decode_fn<2, kRingDeep, W>(f16, awq); return cudaSuccess; }
         return launch_decode_ex<2, kRingDeep, W>(cfg, f16, p);
     }
-    if (fn_out) { *fn_out = decode_fn<2, kRingShallow, W>(f16); return cudaSuccess; }
+    if (fn_out) { *fn_out = decode_fn<2, kRingShallow, W>(f16, awq); return cudaSuccess; }
     return launch_decode_ex<2, kRingShallow, W>(cfg, f16, p);
+}
+
+int decode_kernel_regs(int MT, int ring, int W, bool f16, bool awq) {
+    // registers per thread of each kernel instance, looked up once (0 when no
+    // device can be asked: the caller then counts shared memory and threads)
+    static int cache[2][2][2][2][2];
+    static std::once_flag once[2][2][2][2][2];
+    const int a = MT == 2, b = ring == kRingShallow, c = W == 4, d = f16, e = awq;
+    std::call_once(once[a][b][c][d][e], [&] {
+        DecodeParams dummy{};
+        dummy.pqs = awq ? reinterpret_cast<const uint16_t*>(16) : nullptr;
+        const void* fn = nullptr;
+        cudaLaunchConfig_t cfg = {};
+        if (W == 8) launch_decode_w<8>(cfg, MT, ring, f16, dummy, &fn);
+        else launch_decode_w<4>(cfg, MT, ring, f16, dummy, &fn);
+        cudaFuncAttributes attr{};
+        cache[a][b][c][d][e] = (fn && cudaFuncGetAttributes(&attr, fn) == cudaSuccess) ? attr.numRegs : 0;
+        if (cache[a][b][c][d][e] == 0) (void)cudaGetLastError();      // no device: not an error for later calls
+    });
+    return cache[a][b][c][d][e];
 }
 
 nvfp4_status launch_decode(const DecodeParams& p_in, int MT, int ring, int W, bool f16, cudaStream_t stream) {

@@ -6,7 +6,7 @@ namespace nvfp4 {
 
 struct DecodeParams {
     const uint16_t* X;        // BF16 or FP16 [M, K]
-    const uint16_t* pqs;      // unused by the kernel: AWQ scaling runs first (launch_awq_scale)
+    const uint16_t* pqs;      // AWQ pre-quant scale [K] in the activation type, or null
     const uint8_t* rp;        // repacked weight
     uint16_t* Y;              // BF16 or FP16 [M, N]
     int64_t M, N, K;
@@ -25,9 +25,12 @@ enum DecodeRing { kRingDeep = 0, kRingShallow = 1 };
 // W consumer warps (8: 128 weight rows per CTA; 4: 64 rows).
 size_t decode_smem_bytes(int MT, int ring, int W);
 
-// CTAs of the decode kernel that fit on one SM at once (shared memory and
-// thread bound).
-int decode_ctas_per_sm(int MT, int ring, int W);
+// CTAs of the decode kernel that fit on one SM at once (shared memory,
+// thread and register bound) for the given activation type and AWQ choice.
+int decode_ctas_per_sm(int MT, int ring, int W, bool f16, bool awq);
+
+// Registers per thread of that decode kernel instance (0 if unknown).
+int decode_kernel_regs(int MT, int ring, int W, bool f16, bool awq);
 
 // MT = 1 (up to 8 tokens per CTA) or 2 (up to 16); tokens beyond 8*MT are
 // covered by a third grid dimension.  W = 8 or 4 consumer warps.

@@ -177,14 +177,16 @@ __device__ void permute_block(const int32_t* __restrict__ idx, int64_t n, int E,
         }
         if (lane == 31) {
             offsets[E] = rows_incl;
-            *n_items = its_incl;
+            if (n_items != nullptr) *n_items = its_incl;
         }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kPermThreads) {
-        const int off = cnt[e], c = offsets[e + 1] - off;
-        for (int r = 0, k = 0; r < c; r += tok, ++k)
-            items[item_base[e] + k] = make_int4(e, off + r, min(tok, c - r), 0);
+    if (items != nullptr) {                                  // null: routing tables only
+        for (int e = tid; e < E; e += kPermThreads) {
+            const int off = cnt[e], c = offsets[e + 1] - off;
+            for (int r = 0, k = 0; r < c; r += tok, ++k)
+                items[item_base[e] + k] = make_int4(e, off + r, min(tok, c - r), 0);
+        }
     }
     for (int64_t c0 = s0; c0 < s1; c0 += 32) {
         const int64_t i = c0 + lane;
@@ -262,6 +264,8 @@ struct MoeLinParams {
     uint16_t* H;               // gated (and non-gated FC1) output [T*k, I]
     float* Yp;                 // FC2 output [T*k, N], scaled by the routing weight
     const float* wts;          // [T*k] routing weights
+    const uint16_t* pqs;       // FC1: AWQ pre-quant scale [K] applied to the activation
+                               //   fragments (x' = RN(x * s)); null = none
     int* status;
 };
 
@@ -276,7 +280,7 @@ __device__ __forceinline__ float plain_act(float v, int act) {
     return silu_f(v);
 }
 
-template <int MT, bool GATED, bool F16>
+template <int MT, bool GATED, bool F16, bool AWQ>
 __global__ void __launch_bounds__(kThreads)
 moe_linear_kernel(const MoeLinParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -410,6 +414,8 @@ moe_linear_kernel(const MoeLinParams p) {
     } else {
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
+        // the AWQ stages synchronise the consumer warps: they must all run the loop
+        if constexpr (AWQ) ok = named_bar_red_and(1, kWarps * 32, ok);
         const bool rows_valid = GATED || row_a + warp * kAtomRows < p.N;
         const uint4* const wlut = (shards && warp >= 4) ? lut + 256 : lut;   // warps 4-7 hold up rows
         const uint8_t* const a0 = ring + warp * kAtomBytes;
@@ -418,8 +424,32 @@ moe_linear_kernel(const MoeLinParams p) {
         int s = 0;
         uint32_t phase = 0;
         const uint32_t lut_s = smem_u32(wlut);
+        // AWQ: k of stage i and the k it holds (a multiple of 16)
+        auto stage_kx = [&](int i) { return (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK; };
+        auto stage_xk = [&](int i) {
+            const int64_t left = p.K - stage_kx(i);
+            const int full_k = min(kBlocksPerStage, nkb - i * kBlocksPerStage) * kBlockK;
+            return (int)(left < full_k ? left : full_k);
+        };
+        using AwqStagesT = AwqStages<F16, kXRowElems, TOK, kBlocksPerStage, kWarps * 32>;
+        AwqStagesT awq;
+        if constexpr (AWQ) if (ok && nst > 0) awq.prefetch(p.pqs + stage_kx(0), nrows, stage_xk(0), tid);
         for (int i = 0; i < nst && ok; ++i) {
-            if (!mbar_wait(&full[s], phase, p.status)) break;
+            const bool got = mbar_wait(&full[s], phase, p.status);
+            if constexpr (!AWQ) {
+                if (!got) break;
+            } else {
+                // x' = RN(x * pre_quant_scale) once per stage, shared by the consumer
+                // warps; the next stage's scales are read while this one is scaled
+                AwqStagesT nxt = awq;
+                if (i + 1 < nst) nxt.prefetch(p.pqs + stage_kx(i + 1), nrows, stage_xk(i + 1), tid);
+                if (got)
+                    awq.apply(reinterpret_cast<uint16_t*>(ring + s * kStageBytes + kWeightStageBytes), nrows,
+                              stage_xk(i), tid);
+                awq = nxt;
+                // every consumer warp has scaled its share (or all stop together)
+                if (!named_bar_red_and(1, kWarps * 32, got)) break;
+            }
             if (rows_valid)
                 stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
                     a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc);
@@ -571,10 +601,10 @@ size_t moe_lin_smem(int MT, bool gated, bool shards) {
     return kRingOffset + (shards ? 2 : 1) * kLutBytes + ring + part * 4;
 }
 
-template <int MT, bool GATED, bool F16>
+template <int MT, bool GATED, bool F16, bool AWQ>
 nvfp4_status launch_moe_linear_typed(const MoeLinParams& p, unsigned gx, unsigned max_items, cudaStream_t s) {
     const size_t smem = moe_lin_smem(MT, GATED, GATED && p.half_stride != 0);
-    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED, F16>,
+    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<MT, GATED, F16, AWQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "MoE linear: shared memory attribute");
     cudaLaunchConfig_t cfg = {};
@@ -591,24 +621,28 @@ nvfp4_status launch_moe_linear_typed(const MoeLinParams& p, unsigned gx, unsigne
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED, F16>, p);
+    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<MT, GATED, F16, AWQ>, p);
     return check_cuda(e, GATED ? "MoE FC1: launch" : "MoE FC2: launch");
 }
 
 template <int MT, bool GATED>
 nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_items, bool f16, cudaStream_t s) {
-    return f16 ? launch_moe_linear_typed<MT, GATED, true>(p, gx, max_items, s)
-               : launch_moe_linear_typed<MT, GATED, false>(p, gx, max_items, s);
+    // AWQ instances: FC1 with a pre-quant scale on its input
+    if (p.pqs != nullptr)
+        return f16 ? launch_moe_linear_typed<MT, GATED, true, true>(p, gx, max_items, s)
+                   : launch_moe_linear_typed<MT, GATED, false, true>(p, gx, max_items, s);
+    return f16 ? launch_moe_linear_typed<MT, GATED, true, false>(p, gx, max_items, s)
+               : launch_moe_linear_typed<MT, GATED, false, false>(p, gx, max_items, s);
 }
 
 struct MoeLayout {
-    size_t idx, wts, offsets, perm, inv, items, n_items, xs, xp, h, yp, total;
+    size_t idx, wts, offsets, perm, inv, items, n_items, xp, h, yp, total;
     bool tile;              // tensor-core tile path (many rows per expert) or the streaming path
     int tok, mt, subm;
     int64_t max_items;
 };
 
-MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq) {
+MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
     MoeLayout L{};
     const int64_t n = T * topk;
     const int64_t per_expert = n / std::max(E, 1);   // routed rows per expert on average
@@ -631,12 +665,36 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I, bool awq)
     L.inv = take(n * 4);
     L.items = take(L.max_items * 16);
     L.n_items = take(4);
-    L.xs = (awq && !L.tile) ? take(T * H * 2) : 0;
     L.xp = L.tile ? take(n * H * 2) : 0;
     L.h = take(n * I * 2);
     L.yp = take(n * H * 4);
     L.total = off;
     return L;
+}
+
+// Route (top-k + softmax over the selected logits) and permute (counts,
+// offsets, stable permutation, its inverse, and -- when `items` is not null --
+// the work list of `tok`-row items): one fused single-CTA kernel for few
+// tokens, else a routing kernel and a permutation kernel.
+nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int topk, int tok, int32_t* idx,
+                            float* wts, int32_t* offsets, int32_t* perm, int32_t* inv, int4* items,
+                            int32_t* n_items, cudaStream_t s) {
+    nvfp4_status st;
+    const size_t psmem = permute_smem_bytes(E);
+    if (T <= kFusedRouteMaxT) {
+        cudaError_t ce = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)psmem);
+        if ((st = check_cuda(ce, "MoE route+permute: shared memory attribute")) != NVFP4_OK) return st;
+        return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE route+permute: launch",
+                              router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items);
+    }
+    st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
+                        router_logits, T, E, topk, idx, wts);
+    if (st != NVFP4_OK) return st;
+    cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
+    return launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
+                          (const int32_t*)idx, T * topk, E, tok, offsets, perm, inv, items, n_items);
 }
 
 int moe_splits(int64_t base_ctas, int64_t KB, int kbs_min) {
@@ -650,10 +708,27 @@ int moe_splits(int64_t base_ctas, int64_t KB, int kbs_min) {
 
 using namespace nvfp4;
 
+extern "C" nvfp4_status nvfp4_moe_route(const float* router_logits, int64_t T, int E, int topk,
+                                       int32_t* topk_idx_out, float* topk_weight_out, int32_t* perm_out,
+                                       int32_t* inv_out, int32_t* offsets_out, void* stream) {
+    const char* fn = "nvfp4_moe_route";
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
+    if (E < 1 || E > kMaxExperts) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: E=%d outside [1, %d]", fn, E, kMaxExperts);
+    if (topk < 1 || topk > kMaxTopk || topk > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: topk=%d outside [1, min(E, %d)]", fn, topk, kMaxTopk);
+    if (T * topk >= ((int64_t)1 << 31)) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: T*topk=%lld exceeds int32 slots", fn, (long long)(T * topk));
+    if (T == 0) return NVFP4_OK;                  // a zero-token chunk launches no kernel
+    if (!router_logits || !topk_idx_out || !topk_weight_out || !perm_out || !inv_out || !offsets_out)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(router_logits, 4) || !aligned(topk_idx_out, 4) || !aligned(topk_weight_out, 4) ||
+        !aligned(perm_out, 4) || !aligned(inv_out, 4) || !aligned(offsets_out, 4))
+        return fail(NVFP4_ERR_ALIGNMENT, "%s: every pointer must be 4-byte aligned", fn);
+    return launch_routing(router_logits, T, E, topk, 1, topk_idx_out, topk_weight_out, offsets_out, perm_out,
+                          inv_out, nullptr, nullptr, (cudaStream_t)stream);
+}
+
 extern "C" size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t I) {
     if (T <= 0 || E <= 0 || topk <= 0 || H <= 0 || I <= 0) return 0;
-    // the AWQ activation copy is always budgeted so one size fits both calls
-    return moe_layout(T, E, topk, H, I, true).total;
+    return moe_layout(T, E, topk, H, I).total;
 }
 
 namespace nvfp4 {
@@ -681,7 +756,7 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
     if (!aligned(router_logits, 4)) return fail(NVFP4_ERR_ALIGNMENT, "%s: router_logits must be 4-byte aligned", fn);
     if (!aligned(fc1, 256) || !aligned(fc2, 256)) return fail(NVFP4_ERR_ALIGNMENT, "%s: expert weights must be 256-byte aligned", fn);
     if (fc1_pre_quant_scale && !aligned(fc1_pre_quant_scale, 16)) return fail(NVFP4_ERR_ALIGNMENT, "%s: fc1_pre_quant_scale must be 16-byte aligned", fn);
-    if (moe_layout(T, E, topk, H, I, false).max_items > 65535)
+    if (moe_layout(T, E, topk, H, I).max_items > 65535)
         return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: T=%lld routes too many rows for one call", fn, (long long)T);
     const size_t need = nvfp4_w4a16_moe_workspace(T, E, topk, H, I);
     if (!workspace || workspace_bytes < need) return fail(NVFP4_ERR_WORKSPACE, "%s: workspace %zu bytes, needs %zu", fn, workspace_bytes, need);
@@ -691,7 +766,7 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
 
     cudaStream_t s = (cudaStream_t)stream;
     uint8_t* ws = (uint8_t*)workspace;
-    const MoeLayout L = moe_layout(T, E, topk, H, I, fc1_pre_quant_scale != nullptr);
+    const MoeLayout L = moe_layout(T, E, topk, H, I);
     const int64_t n = T * topk;
     int32_t* idx = topk_idx_out ? topk_idx_out : (int32_t*)(ws + L.idx);
     float* wts = topk_weight_out ? topk_weight_out : (float*)(ws + L.wts);
@@ -711,33 +786,10 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
     const size_t half_stride = fc1_split ? shard_bytes : 0;
     const int64_t fc1_rows = (gated && !fc1_split) ? 2 * I : I;          // rows of one repacked FC1 buffer
 
-    const uint16_t* xin = (const uint16_t*)X;
-    if (fc1_pre_quant_scale && !L.tile) {
-        st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H,
-                              f16, s);
-        if (st != NVFP4_OK) return st;
-        xin = (const uint16_t*)(ws + L.xs);
-    }
-    {
-        const size_t psmem = permute_smem_bytes(E);
-        if (T <= kFusedRouteMaxT) {
-            cudaError_t ce = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  (int)psmem);
-            if ((st = check_cuda(ce, "MoE route+permute: shared memory attribute")) != NVFP4_OK) return st;
-            st = launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE route+permute: launch",
-                                router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items);
-            if (st != NVFP4_OK) return st;
-        } else {
-            st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
-                                router_logits, T, E, topk, idx, wts);
-            if (st != NVFP4_OK) return st;
-            cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
-            if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
-            st = launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
-                                (const int32_t*)idx, n, E, L.tok, offsets, perm, inv, items, n_items);
-            if (st != NVFP4_OK) return st;
-        }
-    }
+    // AWQ: the tile path scales the rows while gathering them, the streaming
+    // path the activation fragments inside FC1; no separate pass either way
+    st = launch_routing(router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items, s);
+    if (st != NVFP4_OK) return st;
 
     if (L.tile) {
         // gather the routed rows into expert-contiguous order, then two tile GEMMs
@@ -769,8 +821,9 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         p1.splits = moe_splits(fc1_groups * est_items, p1.KB, 4);
         p1.kbs = (int)ceil_div(p1.KB, p1.splits);
         p1.splits = (int)ceil_div(p1.KB, p1.kbs);
-        p1.X = xin; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
+        p1.X = (const uint16_t*)X; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
         p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
+        p1.pqs = (const uint16_t*)fc1_pre_quant_scale;
         p1.act = gated ? 0 : activation;
         if (gated)
             st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
@@ -926,13 +979,15 @@ nvfp4_status mlp_impl(const void* X, const void* fc1, const void* fc2, const voi
     nvfp4_status st;
 
     const uint16_t* xin = (const uint16_t*)X;
-    if (fc1_pre_quant_scale) {
+    const bool fc1_tile = mlp_fc1_tile(T, I);
+    if (fc1_pre_quant_scale && fc1_tile) {
+        // the tile FC1 reads X through TMA: scale it into the workspace first
         st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H,
                               f16, s);
         if (st != NVFP4_OK) return st;
         xin = (const uint16_t*)(ws + L.xs);
     }
-    if (mlp_fc1_tile(T, I)) {
+    if (fc1_tile) {
         TcMoeParams t1{};
         t1.fc1 = true; t1.f16 = f16; t1.subm = T > 128 ? 2 : 1;
         t1.X = xin; t1.x_rows = T; t1.w = (const uint8_t*)fc1; t1.w_stride = 0;
@@ -952,6 +1007,7 @@ nvfp4_status mlp_impl(const void* X, const void* fc1, const void* fc2, const voi
         p1.splits = (int)ceil_div(p1.KB, p1.kbs);
         p1.X = xin; p1.perm = nullptr; p1.topk = 1; p1.items = nullptr; p1.n_items = nullptr; p1.rows = T;
         p1.I = I; p1.H = hbuf; p1.wts = nullptr; p1.status = status;
+        p1.pqs = (const uint16_t*)fc1_pre_quant_scale;         // fused into the FC1 fragments
         st = mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)(I / 64), (unsigned)items, f16, s)
                      : launch_moe_linear<2, true>(p1, (unsigned)(I / 64), (unsigned)items, f16, s);
         if (st != NVFP4_OK) return st;

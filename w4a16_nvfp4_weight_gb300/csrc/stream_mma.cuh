@@ -66,6 +66,62 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t saddr) {
     return v;
 }
 
+// x' = RN(x * s) on a pair of activations: one packed multiply rounds the
+// exact product once, as the AWQ pre-quant scale is defined.
+template <bool F16>
+__device__ __forceinline__ uint32_t awq_mul2(uint32_t x, uint32_t s) {
+    uint32_t r;
+    if constexpr (F16) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+    else asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(s));
+    return r;
+}
+
+// Read-only 128-bit global load through L1 (the AWQ scale vector is small and
+// shared by every warp of the SM).
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// AWQ on the ring stages of a streaming kernel: x' = RN(x * s) in place on the
+// activation rows of a stage (row stride XS elements, rows <= TOK, B 64-k
+// blocks of which `xk` k hold data), s = the pre-quant scale at the stage's
+// k.  NTHR threads share a stage in 8-element chunks (chunk c: row
+// c / kPerRow, column c % kPerRow); each thread loads its chunks' scales one
+// stage ahead, so the scale reads never sit between a stage's arrival and its
+// MMAs.  The callers synchronise the threads before a stage is read.  Rows
+// past M and k past K are left alone (they only meet zero weights or are
+// never stored).
+template <bool F16, int XS, int TOK, int B, int NTHR>
+struct AwqStages {
+    static constexpr int kPerRow = B * kBlockK / 8;
+    static constexpr int kU = (TOK * kPerRow + NTHR - 1) / NTHR;     // chunks per thread
+    uint4 s[kU];
+
+    __device__ __forceinline__ void prefetch(const uint16_t* srow, int rows, int xk, int t) {
+        #pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int c = t + u * NTHR, col = c % kPerRow;
+            if (c < rows * kPerRow && col * 8 < xk) s[u] = ldg_nc_v4(srow + col * 8);
+        }
+    }
+
+    __device__ __forceinline__ void apply(uint16_t* xs, int rows, int xk, int t) const {
+        #pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int c = t + u * NTHR, r = c / kPerRow, col = c % kPerRow;
+            if (c < rows * kPerRow && col * 8 < xk) {
+                uint4* px = reinterpret_cast<uint4*>(xs + r * XS + col * 8);
+                uint4 xv = *px;
+                xv = make_uint4(awq_mul2<F16>(xv.x, s[u].x), awq_mul2<F16>(xv.y, s[u].y),
+                                awq_mul2<F16>(xv.z, s[u].z), awq_mul2<F16>(xv.w, s[u].w));
+                *px = xv;
+            }
+        }
+    }
+};
+
 // One atom: a lane holds 16 code bytes (rows g and g+8 of the atom, group q)
 // and their two scale codes sc0 (row g) and sc1 (row g+8); xrow points at
 // token row g, group q of the activation chunk (row stride XS elements,
