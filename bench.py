@@ -164,13 +164,14 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
-# DRAM traffic per launch of the dominant kernel, from a committed ncu summary:
-# dram bytes read + written / algorithmic bytes of the captured launch, valid
-# only while the kernel's sources are unchanged since the capture.
+# DRAM traffic per launch of the dominant kernel, from a committed ncu capture:
+# dram bytes read + written / algorithmic bytes of the captured launch, kept in
+# a small JSON beside the capture's summary under profiles/, valid only while
+# the kernel's sources hash to the value recorded there.
 PROFILE_FOR = {
-    "decode": ("profiles/decode_kernel_lmhead_m8_and_16x5120x25600.md",
+    "decode": ("profiles/decode_kernel_lmhead_m8.traffic.json",
                ["gemm_decode.cu", "stream_mma.cuh", "common.cuh", "ptx.cuh"]),
-    "tensor": ("profiles/tc_gemm_kernel_prefill_2048x5120x13824.md",
+    "tensor": ("profiles/tc_gemm_kernel_prefill_2048x5120x13824.traffic.json",
                ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "ptx.cuh"]),
 }
 
@@ -190,16 +191,15 @@ def kernel_sources_sha(srcs):
 
 
 def traffic_ratio(kind):
+    """(ratio, capture file) when the capture matches the current sources, else (None, reason)."""
     path, srcs = PROFILE_FOR[kind]
     try:
-        text = open(os.path.join(ROOT, path)).read()
-        kv = dict(line.split(":", 1) for line in text.splitlines()
-                  if line.startswith(("traffic_ratio:", "kernel_sources_sha:")))
-        if kernel_sources_sha(srcs) != kv["kernel_sources_sha"].strip():
-            return None
-        return float(kv["traffic_ratio"])
-    except (OSError, KeyError, ValueError):
-        return None
+        rec = json.load(open(os.path.join(ROOT, path)))
+    except (OSError, ValueError):
+        return None, f"no capture record ({path})"
+    if rec.get("kernel_sources_sha") != kernel_sources_sha(srcs):
+        return None, f"{path}: kernel sources changed since the capture"
+    return float(rec["traffic_ratio"]), path
 
 
 # ------------------------------------------------------------------ inputs --
@@ -236,6 +236,17 @@ def build_decode_workload(nv, synth, device, awq=False):
                                  pqs_bits=pqs_bits, pqs=bits_tensor(pqs_bits, device) if awq else None,
                                  y=torch.empty((M, N), dtype=act_torch(), device=device)))
     return launches, base
+
+
+def build_toy_workload(nv, synth, device):
+    """The small single linear: M=4, K=N=256, uniform codes, divisor 448."""
+    c = synth.uniform_codes_case()
+    w = nv.repack(torch.from_numpy(c.packed).to(device), torch.from_numpy(c.scales).to(device),
+                  float(c.divisor), c.N, c.K)
+    x_bits = c.x_bits if ACT == "bf16" else synth.normal_act(synth.rng(5), (c.M, c.K), ACT)
+    launch = dict(M=c.M, K=c.K, N=c.N, w=w, x=bits_tensor(x_bits, device), x_bits=x_bits, pqs=None,
+                  pqs_bits=None, y=torch.empty((c.M, c.N), dtype=act_torch(), device=device))
+    return [launch], {(c.K, c.N): (w, c.packed, c.scales, c.divisor)}
 
 
 def build_dense_workload(nv, synth, device, shapes, wl_index, awq=False):
@@ -283,6 +294,10 @@ def run_ours(args, rank, world, device):
         shapes = [(M, K, N) for M in (1, 8, 256) for (K, N) in ((2064, 1000), (720, 3000))]
         launches, base = build_dense_workload(nv, synth, device, shapes, 4)
         config = {"workload": "odd shapes M{1,8,256} x (K,N){(2064,1000),(720,3000)}", "gemms_per_step": len(launches)}
+    elif wl == "toy":
+        launches, base = build_toy_workload(nv, synth, device)
+        config = {"workload": "single linear M=4 K=256 N=256 (uniform random E2M1 codes, uniform E4M3 scales, "
+                              "global divisor 448; latency-bound)", "gemms_per_step": len(launches)}
     elif wl == "moe":
         return run_moe(args, rank, world, device, nv, synth)
     elif wl == "mlp":
@@ -341,21 +356,24 @@ def run_ours(args, rank, world, device):
     # per-launch kernel durations (CUDA events around graphs of back-to-back launches)
     kern = kernel_timing(nv, launches, base, stream, device)
 
-    bw_unit = wl in ("decode", "lmhead", "tails")
-    ratio = traffic_ratio("decode" if bw_unit else "tensor")
+    bw_unit = wl in ("decode", "lmhead", "tails", "toy")
+    ratio, traffic_src = traffic_ratio("decode" if bw_unit else "tensor")
     traffic = None if ratio is None else round(ratio * kern["bytes"] / len(launches))
-    e2e = run_e2e(nv, launches, stream, args, bw_unit)
+    e2e_graph = run_e2e(nv, launches, stream, args, bw_unit)
+    e2e = run_e2e_per_call(nv, launches, stream, args, bw_unit)
     pk = peaks()
     if bw_unit:
         unit, value = "GB/s", world * bytes_step / (ms_step * 1e-3) / 1e9
         bound, ach_unit = "hbm", "GB/s"
         achieved = kern["bytes"] / kern["seconds"] / 1e9
-        peak = pk["hbm"]
+        peak, peak_name = pk["hbm"], "HBM copy"
     else:
+        # the per-shape kernel times are short graphs of one shape (the kernel
+        # timed on its own): the burst BF16 peak is the matching denominator
         unit, value = "TFLOP/s", world * flops_step / (ms_step * 1e-3) / 1e12
         bound, ach_unit = "tensor", "TFLOP/s"
         achieved = kern["flops"] / kern["seconds"] / 1e12
-        peak = pk["bf16_sustained"]
+        peak, peak_name = pk["bf16"], "bf16 burst (kernels timed in isolation)"
     res = {
         "metric": "W4A16 NVFP4 GEMM TFLOPS & weight GB/s (1 GB300) and % of roofline",
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -370,13 +388,14 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": ach_unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "traffic_note": "bytes per launch: DRAM/algorithmic ratio of a committed ncu capture "
-                                     "(profiles/) times this workload's mean algorithmic bytes per launch",
-                     "peak_source": f"{pk['source']} ({'HBM copy' if bound == 'hbm' else 'bf16 sustained'})",
+                                     f"({traffic_src}) times this workload's mean algorithmic bytes per launch",
+                     "peak_source": f"{pk['source']} ({peak_name})",
                      "kernel": "nvfp4::decode_kernel" if bound == "hbm" else "nvfp4::tc_gemm_kernel",
                      "per_shape_us": kern["per_shape_us"]},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
         "e2e": e2e,
+        "e2e_graph": e2e_graph,
         "gpu_launches": launches_per_step * args.steps,
     }
     if world == 1:
@@ -505,6 +524,8 @@ def run_moe(args, rank, world, device, nv, synth):
         "tflops": round(world * flops_step / (ms_step * 1e-3) / 1e12, 2),
         "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(value / pk["hbm"], 4), "traffic": None, "peak_source": pk["source"],
+                     "kernel": "nvfp4::tc_gemm_kernel (MoE FC1 tile mode at T=4096, the largest share of a "
+                               "step); T <= 256 run nvfp4::moe_linear_kernel",
                      "per_call": per},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
@@ -745,6 +766,62 @@ def run_e2e(nv, launches, stream, args, bw_unit):
                     "(the step captured in a CUDA graph), device Y -> pinned host in one copy per step"}
 
 
+def run_e2e_per_call(nv, launches, stream, args, bw_unit):
+    """The step as a user calls it, with nothing captured: each step copies its
+    activations from pinned host memory to the device (one copy), calls
+    nvfp4_w4a16_gemm once per GEMM through the Python binding (argument checks,
+    the launch plan, the ctypes call and the launches all run every step), and
+    copies all outputs back to pinned host memory (one copy)."""
+    def layout(shapes):
+        offs, off = [], 0
+        for (r, c) in shapes:
+            offs.append(off)
+            off += (2 * r * c + 255) // 256 * 256
+        return offs, off
+
+    xo, xbytes = layout([(L["M"], L["K"]) for L in launches])
+    yo, ybytes = layout([(L["M"], L["N"]) for L in launches])
+    dev = launches[0]["x"].device
+    hx = torch.empty(xbytes, dtype=torch.uint8).pin_memory()
+    hy = torch.empty(ybytes, dtype=torch.uint8).pin_memory()
+    dx = torch.empty(xbytes, dtype=torch.uint8, device=dev)
+    dy = torch.empty(ybytes, dtype=torch.uint8, device=dev)
+    xs, ys = [], []
+    for L, ox, oy in zip(launches, xo, yo):
+        nx, ny = 2 * L["M"] * L["K"], 2 * L["M"] * L["N"]
+        hx[ox:ox + nx].copy_(L["x"].cpu().contiguous().view(torch.uint8).reshape(-1))
+        xs.append(dx[ox:ox + nx].view(act_torch()).view(L["M"], L["K"]))
+        ys.append(dy[oy:oy + ny].view(act_torch()).view(L["M"], L["N"]))
+    steps = max(3, min(args.steps, 200))
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        for L, x, y in zip(launches, xs, ys):
+            nv.gemm(x, L["w"], pre_quant_scale=L["pqs"], out=y, workspace=L["ws"])
+        hy.copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert torch.equal(hy, dy.cpu())
+    ms = e0.elapsed_time(e1) / steps
+    bytes_step = sum(algo_bytes(L["M"], L["N"], L["K"]) for L in launches)
+    flops_step = sum(flops(L["M"], L["N"], L["K"]) for L in launches)
+    v = bytes_step / (ms * 1e-3) / 1e9 if bw_unit else flops_step / (ms * 1e-3) / 1e12
+    return {"value": round(v, 2), "unit": "GB/s" if bw_unit else "TFLOP/s",
+            "h2d_bytes_per_step": hx.numel(), "d2h_bytes_per_step": hy.numel(),
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "path": "every step: pinned host X -> device (one copy), one nvfp4_w4a16_gemm call per GEMM "
+                    "through the Python binding (no graph capture), device Y -> pinned host (one copy)"}
+
+
 # ----------------------------------------------------------- CPU baseline --
 def _baseline_cases(base, rows_per_gemm):
     """The oracle's sample of the decode workload: every GEMM of a step
@@ -885,7 +962,7 @@ def attach_cpu_baselines(res, workload, world, skip, seconds=None):
     if workload == "decode":
         res["cpu_baseline"] = cpu_baseline(base=base, **kw)
         res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(base=base, **kw)
-    elif workload in ("prefill", "lmhead", "tails"):
+    elif workload in ("prefill", "lmhead", "tails", "toy"):
         res["cpu_baseline"] = cpu_baseline_dense(cases, base, workload != "prefill", **kw)
     elif workload == "moe":
         res["cpu_baseline"] = cpu_baseline_moe(*moe_host, **kw)
@@ -939,6 +1016,33 @@ def profile_case(args):
     print(json.dumps({"profile": [M, K, N], "awq": bool(args.awq), "ok": True}))
 
 
+def profile_moe_case(args):
+    """The MoE layer (128 experts, top-8, hidden 2048, intermediate 768) at T
+    tokens, 3 warm-up + 3 calls, for an ncu capture of its kernels."""
+    import w4a16_nvfp4_weight_gb300 as nv
+    from w4a16_nvfp4_weight_gb300 import synth
+    T = int(args.profile_moe)
+    fc1, fc2 = synth.moe_weights(MOE_E, MOE_H, MOE_I, synth.seed_for(3, 500))
+
+    def experts(ws, N, K):
+        size = nv.repack_size(N, K)
+        buf = torch.empty(len(ws) * size, dtype=torch.uint8, device="cuda")
+        for e, (p, sc, d) in enumerate(ws):
+            nv.repack(torch.from_numpy(p).cuda(), torch.from_numpy(sc).cuda(), float(d), N, K,
+                      out=buf[e * size:(e + 1) * size])
+        return buf
+
+    d1, d2 = experts(fc1, 2 * MOE_I, MOE_H), experts(fc2, MOE_H, MOE_I)
+    c = synth.moe_case(T, synth.seed_for(3, T), E=MOE_E, topk=MOE_TOPK, H=MOE_H, I=MOE_I, weights=(fc1, fc2))
+    x = bits_tensor(c.x_bits, "cuda")
+    lg = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
+    for _ in range(6):
+        nv.moe_grouped(x, lg, d1, d2, MOE_TOPK, MOE_I)
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    print(json.dumps({"profile_moe": T, "ok": True}))
+
+
 # ------------------------------------------------------------ distributed --
 def barrier(world):
     if world > 1:
@@ -959,18 +1063,24 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "lmhead", "tails", "moe", "mlp"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "lmhead", "tails", "toy", "moe", "mlp"])
     ap.add_argument("--awq", action="store_true")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="activation type: BF16 (default) or FP16 activations, weights and output")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, metavar="M,K,N",
                     help="run one GEMM shape 3 times after 3 warm-ups (for ncu captures); no timing")
+    ap.add_argument("--profile-moe", default=None, metavar="T",
+                    help="run the MoE layer at T tokens 3 times after 3 warm-ups (for ncu captures); no timing")
     args = ap.parse_args()
     global ACT
     ACT = args.dtype
     if args.profile:
         profile_case(args)
+        return
+    if args.profile_moe:
+        profile_moe_case(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -32,7 +32,7 @@ def test_attach_cpu_baselines_for_every_workload(monkeypatch):
     base = {(64, 48): (None,) + tuple(synth.weight_only(64, 48, 3))}
     cases = [(3, 64, 48, synth.normal_act(r, (3, 64), "bf16"), None),
              (5, 64, 48, synth.normal_act(r, (5, 64), "bf16"), synth.awq_scale_bits(r, 64))]
-    for wl, unit in (("prefill", "TFLOP/s"), ("lmhead", "GB/s"), ("tails", "GB/s")):
+    for wl, unit in (("prefill", "TFLOP/s"), ("lmhead", "GB/s"), ("tails", "GB/s"), ("toy", "GB/s")):
         res = {"value": 1.0, "_base": base, "_cases": cases}
         out = bench.attach_cpu_baselines(res, wl, 1, False, seconds=0.1)
         assert out["cpu_baseline"]["unit"] == unit and out["cpu_baseline"]["value"] > 0
@@ -56,3 +56,20 @@ def test_attach_cpu_baselines_for_every_workload(monkeypatch):
         res = {"value": 1.0, "_base": base, "_cases": cases}
         out = bench.attach_cpu_baselines(res, "prefill", world, skip)
         assert "cpu_baseline" not in out and "_cases" not in out
+
+
+def test_traffic_ratio_needs_a_matching_capture(tmp_path, monkeypatch):
+    """The roofline's traffic comes from a committed capture record only while
+    the kernel's sources still hash to the value the record holds."""
+    rec = tmp_path / "rec.json"
+    sha = bench.kernel_sources_sha(["common.cuh"])
+    rec.write_text(json.dumps({"traffic_ratio": 1.01, "kernel_sources_sha": sha}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "PROFILE_FOR", {"decode": ("rec.json", ["common.cuh"])})
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda srcs: sha)
+    assert bench.traffic_ratio("decode") == (1.01, "rec.json")
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda srcs: "different")
+    ratio, why = bench.traffic_ratio("decode")
+    assert ratio is None and "changed" in why
+    monkeypatch.setattr(bench, "PROFILE_FOR", {"decode": ("missing.json", ["common.cuh"])})
+    assert bench.traffic_ratio("decode")[0] is None
