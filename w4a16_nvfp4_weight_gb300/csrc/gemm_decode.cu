@@ -15,7 +15,9 @@
 // same permutation, so the dot products are unchanged.  K is split across the
 // CTAs of a thread-block cluster, which reduce their FP32 partials through
 // distributed shared memory in rank order: deterministic, and no global
-// workspace.  The AWQ pre-quant scale, when present, is applied to each ring
+// workspace.  The partials travel as asynchronous stores counted on the
+// receiving CTA's barrier, so no cluster-wide barrier closes the kernel: a CTA
+// leaves as soon as its own pushes are out and its own share has arrived.  The AWQ pre-quant scale, when present, is applied to each ring
 // stage's activation rows in shared memory, once, by the consumer warps
 // together (each loads its share of the scales a stage ahead): x' = RN(x * s)
 // in BF16 (or FP16), one packed multiply per pair, no extra pass and no
@@ -33,14 +35,12 @@
 #include <algorithm>
 #include <mutex>
 
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "gemm_decode.cuh"
 #include "ptx.cuh"
 #include "stream_mma.cuh"
 
-namespace cg = cooperative_groups;
 
 namespace nvfp4 {
 
@@ -78,7 +78,7 @@ using RingGeom = StreamRing<MT, Ring<MT, R, W>::kStages, Ring<MT, R, W>::kBlocks
 
 struct Smem {
     // offsets in bytes from the dynamic shared memory base
-    static constexpr size_t bars = 0;              // full[S], empty[S], lut_bar
+    static constexpr size_t bars = 0;              // full[S], empty[S], lut_bar, red_bar
     static constexpr size_t flag = 120;            // header accepted (written by the producer)
     static constexpr size_t lut = 128;
     static constexpr size_t ring = lut + kLutBytes;
@@ -102,12 +102,12 @@ decode_kernel(const DecodeParams p) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::bars);
     uint64_t* empty = full + kStages;
     uint64_t* lut_bar = empty + kStages;
+    uint64_t* red_bar = lut_bar + 1;       // this CTA's share of the split-K partials has landed
     volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + Smem::flag);
     uint4* lut = reinterpret_cast<uint4*>(smem + Smem::lut);
     uint8_t* ring = smem + Smem::ring;
     float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);
 
-    cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = blockIdx.x;
     const int split = blockIdx.y;
@@ -131,6 +131,7 @@ decode_kernel(const DecodeParams p) {
             mbar_init(&empty[s], kWarps);
         }
         mbar_init(lut_bar, 1);
+        mbar_init(red_bar, 1);
         fence_mbar_init();
     }
     // Zero every activation chunk once: token rows without data and the k tail
@@ -142,6 +143,10 @@ decode_kernel(const DecodeParams p) {
     }
     fence_proxy_async();      // these generic writes before later bulk copies into the same bytes
     __syncthreads();
+    // The split-K partials are pushed into other CTAs' shared memory at the end:
+    // their barriers must be initialised first.  Arrive now, wait just before
+    // the first push (by then every CTA of the cluster has long arrived).
+    cluster_arrive();
 
     float acc[MT][4];
     #pragma unroll
@@ -209,7 +214,7 @@ decode_kernel(const DecodeParams p) {
             }
         }
         __syncwarp();
-        __syncwarp();
+        cluster_wait();                   // the producer warp pairs its cluster arrival too
     } else {
         // ---------------- consumers
         const bool rows_valid = (int64_t)rg * kRowsPerCta + warp * kAtomRows < p.N;
@@ -262,10 +267,14 @@ decode_kernel(const DecodeParams p) {
 
         // Push each partial of a token row with data to the CTA that reduces it:
         // output e = token * rows + row belongs to rank e / share and lands in
-        // that rank's slot for this rank.  Token rows past M are never sent.
+        // that rank's slot for this rank, counted on that rank's red_bar.  Token
+        // rows past M are never sent.  No cluster-wide barrier follows: a CTA
+        // leaves once its pushes are out and its own share has arrived.
         const int c = lane & 3;
         const int total = kRowsPerCta * rows_x;
         const int share = (total + p.splits - 1) / p.splits;
+        const uint32_t part_s = smem_u32(part), bar_s = smem_u32(red_bar);
+        cluster_wait();
         #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             #pragma unroll
@@ -274,26 +283,31 @@ decode_kernel(const DecodeParams p) {
                 const int t = mt * 8 + 2 * c + (v & 1);
                 if (t < rows_x) {
                     const int e = t * kRowsPerCta + row;
-                    float* dst = cluster.map_shared_rank(part, e / share);
-                    dst[split * share + e % share] = acc[mt][v];
+                    const uint32_t owner = (uint32_t)(e / share);
+                    st_async_b32(map_rank(part_s + 4u * (uint32_t)(split * share + e % share), owner),
+                                 __float_as_uint(acc[mt][v]), map_rank(bar_s, owner));
                 }
             }
         }
     }
-    cluster.sync();     // all partials have landed in their reducing CTA
 
-    // Reduce this rank's share from local shared memory, ranks in order.
-    if (*hdr_flag != 0) {
-        const int total = kRowsPerCta * rows_x;
-        const int share = (total + p.splits - 1) / p.splits;
-        const int e0 = split * share, e1 = min(total, e0 + share);
-        for (int e = e0 + tid; e < e1; e += kThreads) {
-            float sum = 0.0f;
-            for (int r = 0; r < p.splits; ++r) sum += part[r * share + (e - e0)];
-            const int t = e / kRowsPerCta, row = e % kRowsPerCta;      // consecutive e -> consecutive n
-            const int64_t n = (int64_t)rg * kRowsPerCta + row;
-            const int64_t m = m0 + t;
-            if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_act_bits<F16>(sum);
+    // Reduce this rank's share from local shared memory, ranks in order, once
+    // every rank's partials for it have landed (4 bytes each).
+    const int total = kRowsPerCta * rows_x;
+    const int share = (total + p.splits - 1) / p.splits;
+    const int e0 = split * share, e1 = min(total, e0 + share);
+    if (e1 > e0) {
+        if (tid == 0) mbar_arrive_expect_tx(red_bar, (uint32_t)((e1 - e0) * p.splits * 4));
+        const bool got = mbar_wait_cluster(red_bar, 0, p.status);
+        if (got && *hdr_flag != 0) {
+            for (int e = e0 + tid; e < e1; e += kThreads) {
+                float sum = 0.0f;
+                for (int r = 0; r < p.splits; ++r) sum += part[r * share + (e - e0)];
+                const int t = e / kRowsPerCta, row = e % kRowsPerCta;      // consecutive e -> consecutive n
+                const int64_t n = (int64_t)rg * kRowsPerCta + row;
+                const int64_t m = m0 + t;
+                if (n < p.N && m < p.M) p.Y[m * p.N + n] = f32_to_act_bits<F16>(sum);
+            }
         }
     }
 }
