@@ -33,15 +33,12 @@
 // the GEMM; a zero-token chunk launches no kernel).
 #include <algorithm>
 #include <mutex>
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "gemm_decode.cuh"
 #include "gemm_tc.cuh"
 #include "ptx.cuh"
 #include "stream_mma.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace nvfp4 {
 namespace {
@@ -294,6 +291,7 @@ moe_linear_kernel(const MoeLinParams p) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kStages;
     uint64_t* lut_bar = empty + kStages;
+    uint64_t* red_bar = lut_bar + 1;          // this CTA's share of the split-K partials has landed
     volatile int* hdr_flag = reinterpret_cast<volatile int*>(smem + 120);
     // magnitude tables: one, or two with gate/up shards (gate first)
     const bool shards = GATED && p.half_stride != 0;
@@ -301,7 +299,6 @@ moe_linear_kernel(const MoeLinParams p) {
     uint8_t* ring = smem + kRingOffset + (shards ? 2 : 1) * kLutBytes;
     float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);
 
-    cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
     const int split = blockIdx.y;
@@ -340,6 +337,7 @@ moe_linear_kernel(const MoeLinParams p) {
             mbar_init(&empty[s], kWarps);
         }
         mbar_init(lut_bar, 1);
+        mbar_init(red_bar, 1);
         fence_mbar_init();
     }
     for (int s = 0; s < kStages; ++s) {
@@ -348,6 +346,7 @@ moe_linear_kernel(const MoeLinParams p) {
     }
     fence_proxy_async();
     __syncthreads();
+    cluster_arrive();                          // every CTA's red_bar is ready before any push
 
     float acc[MT][4];
     #pragma unroll
@@ -411,6 +410,7 @@ moe_linear_kernel(const MoeLinParams p) {
             }
         }
         __syncwarp();
+        cluster_wait();
     } else {
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
@@ -458,11 +458,14 @@ moe_linear_kernel(const MoeLinParams p) {
             if (lane == 0) mbar_arrive(&empty[s]);
             if (++s == kStages) { s = 0; phase ^= 1u; }
         }
-        // push partials to the reducing CTA
+        // push the partials of rows with data to the reducing CTA, as remote
+        // stores counted on its red_bar (no cluster-wide barrier afterwards)
         const int c = lane & 3;
+        const uint32_t part_s = smem_u32(part), bar_s = smem_u32(red_bar);
+        cluster_wait();
         if (GATED) {
             // pair (token t, column jj): gate partial from warps 0-3, up from warps 4-7
-            const int total = TOK * 64;
+            const int total = nrows * 64;
             const int share = (total + p.splits - 1) / p.splits;
             #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
@@ -472,11 +475,14 @@ moe_linear_kernel(const MoeLinParams p) {
                     const int t = mt * 8 + 2 * c + (v & 1);
                     const int jj = row & 63, half = row >> 6;
                     const int ei = t * 64 + jj;
-                    float* dst = cluster.map_shared_rank(part, ei / share);
-                    dst[(split * share + ei % share) * 2 + half] = acc[mt][v];
+                    if (t < nrows) {
+                        const uint32_t owner = (uint32_t)(ei / share);
+                        st_async_b32(map_rank(part_s + 4u * (uint32_t)((split * share + ei % share) * 2 + half), owner),
+                                     __float_as_uint(acc[mt][v]), map_rank(bar_s, owner));
+                    }
                 }
         } else {
-            const int total = TOK * 128;
+            const int total = nrows * 128;
             const int share = (total + p.splits - 1) / p.splits;
             #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
@@ -485,16 +491,29 @@ moe_linear_kernel(const MoeLinParams p) {
                     const int row = warp * 16 + g + (v >= 2 ? 8 : 0);
                     const int t = mt * 8 + 2 * c + (v & 1);
                     const int ei = t * 128 + row;
-                    float* dst = cluster.map_shared_rank(part, ei / share);
-                    dst[split * share + ei % share] = acc[mt][v];
+                    if (t < nrows) {
+                        const uint32_t owner = (uint32_t)(ei / share);
+                        st_async_b32(map_rank(part_s + 4u * (uint32_t)(split * share + ei % share), owner),
+                                     __float_as_uint(acc[mt][v]), map_rank(bar_s, owner));
+                    }
                 }
         }
     }
-    cluster.sync();
 
-    if (*hdr_flag != 0) {
+    // this rank's share: wait for every rank's partials (4 bytes each; two
+    // per output when gated), then reduce in rank order
+    const int per_e = GATED ? 2 : 1;
+    const int total_e = nrows * (GATED ? 64 : 128);
+    const int share_e = (total_e + p.splits - 1) / p.splits;
+    const int e0_own = split * share_e, e1_own = min(total_e, e0_own + share_e);
+    bool landed = true;
+    if (e1_own > e0_own) {
+        if (tid == 0) mbar_arrive_expect_tx(red_bar, (uint32_t)((e1_own - e0_own) * p.splits * per_e * 4));
+        landed = mbar_wait_cluster(red_bar, 0, p.status);
+    }
+    if (landed && *hdr_flag != 0) {
         if (GATED) {
-            const int total = TOK * 64;
+            const int total = nrows * 64;
             const int share = (total + p.splits - 1) / p.splits;
             const int e0 = split * share, e1 = min(total, e0 + share);
             for (int ei = e0 + tid; ei < e1; ei += kThreads) {
@@ -508,7 +527,7 @@ moe_linear_kernel(const MoeLinParams p) {
                     p.H[(int64_t)(r0 + t) * p.I + (int64_t)cgi * 64 + jj] = f32_to_act_bits<F16>(silu_f(gsum) * usum);
             }
         } else {
-            const int total = TOK * 128;
+            const int total = nrows * 128;
             const int share = (total + p.splits - 1) / p.splits;
             const int e0 = split * share, e1 = min(total, e0 + share);
             for (int ei = e0 + tid; ei < e1; ei += kThreads) {
