@@ -325,6 +325,23 @@ nvfp4_status nvfp4_w4a16_moe_grouped_ex(const void* X, const float* router_logit
                                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The kernels nvfp4_w4a16_moe_grouped* would run for a problem on the current
+ * device (host only, no launch).  activation as nvfp4_w4a16_moe_grouped_ex.
+ *  path_out           0 nothing (T == 0); 1 streaming kernels, one CTA per
+ *                     (work item, column group) with K split across a thread-
+ *                     block cluster; 2 streaming kernels, one persistent wave
+ *                     that walks the (work item, column group) units with K
+ *                     whole; 3 gathered rows on the tcgen05 tile kernels.
+ *  rows_per_item_out  routed rows per work item (8 or 16 streaming, 128 or
+ *                     256 on the tile kernels; 0 when T == 0).
+ * The choice depends on the routed rows per expert on average (T * topk / E)
+ * and, on the streaming path, on the expected units per SM.  Errors as the
+ * layer's argument checks (null output pointer, sizes outside its limits).
+ */
+nvfp4_status nvfp4_w4a16_moe_plan(int64_t T, int E, int topk, int64_t H, int64_t I, int activation,
+                                  int* path_out, int* rows_per_item_out);
+
+/*
  * The layer's FC1 activation scale from per-expert AWQ pre-quant scales (a
  * load-time step): out[k] = max over experts e of max(w3_e[k], w1_e[k])
  * ("[None][fix] Apply the NVFP4_AWQ pre-quant scale in MegaMoE CuteDSL",

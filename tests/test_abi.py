@@ -205,3 +205,29 @@ def test_gemm_plan_on_host(lib):
     assert lib.nvfp4_w4a16_gemm_plan(-1, 64, 64, 0, *refs) == 1
     assert lib.nvfp4_w4a16_gemm_plan(4, 64, 64, 2, *refs) == 1
     assert lib.nvfp4_w4a16_gemm_plan(4, 64, 64, 0, None, *refs[1:]) == 1
+
+
+def test_moe_plan_on_host(lib):
+    """The MoE path query: host only, the choice the layer makes from the
+    average routed rows per expert and the expected units per SM (the config
+    layer E=128, top-8, H=2048, I=768 at T = 1, 16, 256, 4096)."""
+    import w4a16_nvfp4_weight_gb300 as nv
+
+    E, k, H, I = 128, 8, 2048, 768
+    assert nv.moe_plan(0, E, k, H, I) == {"path": "none", "rows_per_item": 0}
+    assert nv.moe_plan(1, E, k, H, I) == {"path": "stream_split", "rows_per_item": 8}
+    assert nv.moe_plan(16, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 8}
+    assert nv.moe_plan(256, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 16}
+    assert nv.moe_plan(4096, E, k, H, I) == {"path": "tile", "rows_per_item": 256}
+    # non-gated experts have half the FC1 column groups
+    assert nv.moe_plan(16, E, k, H, I, "relu2")["path"] in ("stream_split", "stream_persistent")
+
+    path, rows = ctypes.c_int(0), ctypes.c_int(0)
+    refs = [ctypes.byref(path), ctypes.byref(rows)]
+    assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 64, 64, 0, *refs) == 0 and path.value == 1
+    assert lib.nvfp4_w4a16_moe_plan(-1, 8, 2, 64, 64, 0, *refs) == 1
+    assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 64, 64, 3, *refs) == 1
+    assert lib.nvfp4_w4a16_moe_plan(4, 0, 2, 64, 64, 0, *refs) == 2
+    assert lib.nvfp4_w4a16_moe_plan(4, 8, 9, 64, 64, 0, *refs) == 2
+    assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 96, 64, 0, *refs) == 2
+    assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 64, 64, 0, None, refs[1]) == 1

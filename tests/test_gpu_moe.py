@@ -212,3 +212,44 @@ def test_moe_route_ties_and_negative_zero():
     assert got["idx"][0].tolist() == [1, 4, 6]
     for k, v in (("idx", idx), ("perm", perm), ("inv", inv), ("offsets", offsets)):
         assert np.array_equal(got[k], v), k
+
+
+@pytest.mark.parametrize("T,E,topk", [(64, 256, 16), (65, 256, 16), (7, 40, 5), (100, 3, 3), (33, 1, 1)])
+def test_moe_route_tables_edge_shapes(T, E, topk):
+    """Both routing kernels at the edges of their limits: 256 experts with
+    top-16 at 64 tokens (the last fused size) and 65 (the first two-kernel
+    size), an expert count that is not a multiple of 32, top-k = E, and one
+    expert."""
+    c = synth.moe_case(T, synth.seed_for(3, T) + E, E=E, topk=topk, H=64, I=64, weights=None)
+    got = {k: v.cpu().numpy() for k, v in nv.moe_route(torch.from_numpy(np.ascontiguousarray(c.logits)).cuda(),
+                                                         topk).items()}
+    gu.check_device_status()
+    idx, p = omoe.route(c.logits, topk)
+    _, offsets, perm, inv = omoe.permute(idx, E)
+    for k, v in (("idx", idx), ("perm", perm), ("inv", inv), ("offsets", offsets)):
+        assert np.array_equal(got[k], v), k
+    assert np.allclose(got["p"], p, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T", [5, 70])
+def test_moe_route_nan_and_infinite_logits(T):
+    """NaN logits rank below every number (a sort that puts NaN last, ties to
+    the lower expert index) and infinities are ordinary extremes; fused
+    (T <= 64) and two-kernel routing."""
+    E, topk = 16, 4
+    r = synth.rng(T + 1)
+    logits = r.standard_normal((T, E)).astype(np.float32)
+    logits[:, 3] = np.nan
+    logits[::2, 9] = np.nan
+    logits[1, 12] = np.inf
+    logits[2, :] = -np.inf
+    logits[2, 5] = np.nan
+    logits[3, :] = np.nan                          # every logit NaN: experts 0..3
+    got = {k: v.cpu().numpy() for k, v in nv.moe_route(torch.from_numpy(logits).cuda(), topk).items()}
+    idx, p = omoe.route(logits, topk)
+    _, offsets, perm, inv = omoe.permute(idx, E)
+    for k, v in (("idx", idx), ("perm", perm), ("inv", inv), ("offsets", offsets)):
+        assert np.array_equal(got[k], v), k
+    assert got["idx"][3].tolist() == [0, 1, 2, 3]
+    finite = np.isfinite(p).all(axis=1)
+    assert np.allclose(got["p"][finite], p[finite], rtol=2e-6, atol=1e-7)

@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import Nvfp4Error
 
 __all__ = ["Nvfp4Error", "NVFP4Weight", "repack", "repack_size", "swizzled_scales_size", "dequant", "gemm",
-           "gemm_workspace_size", "gemm_plan", "moe_grouped", "moe_route", "moe_workspace_size",
+           "gemm_workspace_size", "gemm_plan", "moe_grouped", "moe_plan", "moe_route", "moe_workspace_size",
            "moe_finalize_pre_quant_scale",
            "mlp", "mlp_workspace_size",
            "device_status",
@@ -184,6 +184,20 @@ def moe_workspace_size(T, E, topk, H, I):
 
 
 MOE_ACTIVATIONS = {"swiglu": 0, "relu2": 1, "silu": 2}
+MOE_PATHS = {0: "none", 1: "stream_split", 2: "stream_persistent", 3: "tile"}
+
+
+def moe_plan(T, E, topk, H, I, activation="swiglu"):
+    """The kernels moe_grouped() would run on the current device: dict(path=
+    "stream_split" | "stream_persistent" | "tile" | "none", rows_per_item).
+    Host only."""
+    if activation not in MOE_ACTIVATIONS:
+        raise Nvfp4Error(1, f"activation must be one of {sorted(MOE_ACTIVATIONS)}")
+    h = _lib.load()
+    path, rows = ctypes.c_int(0), ctypes.c_int(0)
+    _lib.check(h.nvfp4_w4a16_moe_plan(T, E, topk, H, I, MOE_ACTIVATIONS[activation],
+                                      ctypes.byref(path), ctypes.byref(rows)))
+    return {"path": MOE_PATHS[path.value], "rows_per_item": rows.value}
 
 
 def moe_grouped(x, router_logits, fc1, fc2, topk, I, fc1_pre_quant_scale=None, out=None,

@@ -30,6 +30,7 @@ SIGNATURES = {
     "nvfp4_w4a16_gemm": (c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_gemm_f16": (c_int, [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_size, c_vp]),
     "nvfp4_w4a16_gemm_plan": (c_int, [c_i64, c_i64, c_i64, c_int, c_vp, c_vp, c_vp, c_vp]),
+    "nvfp4_w4a16_moe_plan": (c_int, [c_i64, c_int, c_int, c_i64, c_i64, c_int, c_vp, c_vp]),
     "nvfp4_moe_route": (c_int, [c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "nvfp4_w4a16_moe_workspace": (c_size, [c_i64, c_int, c_int, c_i64, c_i64]),
     "nvfp4_w4a16_moe_grouped": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_int, c_int, c_i64,

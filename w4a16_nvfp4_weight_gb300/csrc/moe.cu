@@ -47,50 +47,61 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 16;
 
 // ------------------------------------------------------------------- route --
+// Order-preserving 32-bit key of an FP32 logit for warp max-reductions: a
+// larger logit has a larger key, -0 the key of +0 (they tie), and NaN the
+// smallest key (picked after every number, as a sort that puts NaN last).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v != v) return 0u;
+    const uint32_t u = __float_as_uint(v + 0.0f);          // -0 + 0 = +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // One warp routes token t: top-k of its E logits (ties to the lower expert
-// index), softmax over the selected k.
+// index), softmax over the selected k.  Each round every lane offers its best
+// unused expert (largest key, then lowest index) and two warp reductions pick
+// the winner: the largest key, then the lowest expert index among its holders.
+// Lane j ends up holding selection j, written with one coalesced store.  With
+// `tok_mask` (tokens 0..63), bit t of expert e's 64-bit mask is set for each
+// selected expert e.
 __device__ void route_token(const float* __restrict__ logits, int64_t t, int E, int topk,
-                            int32_t* __restrict__ idx, float* __restrict__ wts, int lane) {
-    float l[kMaxExperts / 32];
+                            int32_t* __restrict__ idx, float* __restrict__ wts, int lane,
+                            uint32_t* tok_mask = nullptr) {
+    constexpr int kPer = kMaxExperts / 32;
+    float l[kPer];
+    uint32_t key[kPer];
     uint32_t used = 0;
     #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int i = 0; i < kPer; ++i) {
         const int e = lane + 32 * i;
         l[i] = e < E ? logits[t * E + e] : 0.0f;
+        key[i] = logit_key(l[i]);
         if (e >= E) used |= 1u << i;
     }
-    float sel_v[kMaxTopk];
-    int sel_e[kMaxTopk];
+    int my_e = 0;
+    float my_v = 0.0f, v0 = 0.0f;
     for (int j = 0; j < topk; ++j) {
-        bool found = false;
-        float v = 0.0f;
-        int b = 0x7fffffff;
+        uint32_t bk = 0u, be = 0xffffffffu;
+        float bv = 0.0f;
         #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            if (!((used >> i) & 1u) && (!found || l[i] > v || (l[i] == v && e < b))) {
-                v = l[i]; b = e; found = true;
+        for (int i = 0; i < kPer; ++i)             // ascending e: strict > keeps the lower index
+            if (!((used >> i) & 1u) && (be == 0xffffffffu || key[i] > bk)) {
+                bk = key[i]; be = (uint32_t)(lane + 32 * i); bv = l[i];
             }
-        }
-        #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-            const int ob = __shfl_xor_sync(0xffffffffu, b, off);
-            const bool of = __shfl_xor_sync(0xffffffffu, found ? 1 : 0, off) != 0;
-            if (of && (!found || ov > v || (ov == v && ob < b))) { v = ov; b = ob; found = true; }
-        }
-        if ((b & 31) == lane) used |= 1u << (b >> 5);
-        sel_v[j] = v;
-        sel_e[j] = b;
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const int e = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? be : 0xffffffffu);
+        const float v = __shfl_sync(0xffffffffu, bv, e & 31);     // the owner offered e
+        if ((e & 31) == lane) used |= 1u << (e >> 5);
+        if (j == lane) { my_e = e; my_v = v; }
+        if (j == 0) v0 = v;                         // the first selection is the largest
     }
-    if (lane == 0) {
-        // the first selected logit is the largest
-        float sum = 0.0f;
-        for (int j = 0; j < topk; ++j) sum += expf(sel_v[j] - sel_v[0]);
-        for (int j = 0; j < topk; ++j) {
-            idx[t * topk + j] = sel_e[j];
-            wts[t * topk + j] = expf(sel_v[j] - sel_v[0]) / sum;
-        }
+    // p_j = exp(v_j - v_0) / sum_j' exp(v_j' - v_0), the sum in selection order
+    const float w = expf(my_v - v0);
+    float sum = 0.0f;
+    for (int j = 0; j < topk; ++j) sum += __shfl_sync(0xffffffffu, w, j);
+    if (lane < topk) {
+        idx[t * topk + lane] = my_e;
+        wts[t * topk + lane] = w / sum;
+        if (tok_mask != nullptr) atomicOr(&tok_mask[2 * my_e + (int)(t >> 5)], 1u << (t & 31));
     }
 }
 
@@ -211,9 +222,12 @@ permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
     permute_block(idx, n, E, tok, offsets, perm, inv, items, n_items, perm_smem);
 }
 
-// Few tokens: one CTA routes every token (a warp per token) and then permutes,
-// saving a launch.  The block barrier orders the routing writes before the
-// permutation reads them.
+// Few tokens (T <= 64): one CTA routes every token (a warp per token) and
+// builds the tables from per-expert token masks instead of counting passes:
+// expert e's routed slots, in token order, are its mask's set bits, so its count
+// is the mask's population and the stable position of token t's slot is
+// offsets[e] + (set bits below t).  Routing, the tables and the permutation are
+// three phases between two block barriers.
 constexpr int64_t kFusedRouteMaxT = 64;
 
 __global__ void __launch_bounds__(kPermThreads)
@@ -221,13 +235,58 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
                      int32_t* __restrict__ idx, float* __restrict__ wts,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                      int4* __restrict__ items, int32_t* __restrict__ n_items) {
-    extern __shared__ int perm_smem[];
+    __shared__ uint32_t tok_mask[2 * kMaxExperts];      // bit t: token t chose the expert
+    __shared__ int32_t off_s[kMaxExperts];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     pdl_wait_previous();
     pdl_launch_dependents();
-    for (int64_t t = threadIdx.x / 32; t < T; t += kPermWarps)
-        route_token(logits, t, E, topk, idx, wts, threadIdx.x & 31);
+    for (int i = tid; i < 2 * E; i += kPermThreads) tok_mask[i] = 0u;
     __syncthreads();
-    permute_block(idx, T * topk, E, tok, offsets, perm, inv, items, n_items, perm_smem);
+    for (int64_t t = w; t < T; t += kPermWarps) route_token(logits, t, E, topk, idx, wts, lane, tok_mask);
+    __syncthreads();
+    if (w == 0) {
+        // counts, offsets and work items: lane l scans the experts [l * per, (l + 1) * per)
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int rows = 0, its = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int c = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
+            rows += c;
+            its += (c + tok - 1) / tok;
+        }
+        int rows_incl = rows, its_incl = its;
+        #pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
+            const int k = __shfl_up_sync(0xffffffffu, its_incl, off);
+            if (lane >= off) { rows_incl += r; its_incl += k; }
+        }
+        int run = rows_incl - rows, item = its_incl - its;
+        for (int e = e0; e < e1; ++e) {
+            const int c = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
+            offsets[e] = run;
+            off_s[e] = run;
+            if (items != nullptr)
+                for (int r = 0; r < c; r += tok) items[item++] = make_int4(e, run + r, min(tok, c - r), 0);
+            run += c;
+        }
+        if (lane == 31) {
+            offsets[E] = rows_incl;
+            if (n_items != nullptr) *n_items = its_incl;
+        }
+    }
+    __syncthreads();
+    // slot i = t * topk + j of expert e: after the earlier tokens of e
+    const int n = (int)T * topk;
+    for (int i = tid; i < n; i += kPermThreads) {
+        const int t = i / topk;
+        const int e = idx[i];                // written by this CTA before the barrier
+        const uint32_t lo = tok_mask[2 * e], hi = tok_mask[2 * e + 1];
+        const int below = t < 32 ? __popc(lo & ((1u << t) - 1u)) : __popc(lo) + __popc(hi & ((1u << (t - 32)) - 1u));
+        const int pos = off_s[e] + below;
+        perm[pos] = i;
+        inv[i] = pos;
+    }
 }
 
 size_t permute_smem_bytes(int E) { return ((size_t)kPermWarps * E + 2 * E) * sizeof(int); }
@@ -263,6 +322,8 @@ struct MoeLinParams {
     const float* wts;          // [T*k] routing weights
     const uint16_t* pqs;       // FC1: AWQ pre-quant scale [K] applied to the activation
                                //   fragments (x' = RN(x * s)); null = none
+    int early;                 // 1: the routing tables were written two launches back, so
+                               //   they and the weights may be read before the wait
     int* status;
 };
 
@@ -303,12 +364,19 @@ moe_linear_kernel(const MoeLinParams p) {
     const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
     const int split = blockIdx.y;
     const int item_id = blockIdx.z;
-    pdl_launch_dependents();
-    pdl_wait_previous();                       // items and activations come from earlier kernels
+    // Items and activations come from earlier kernels.  Dependents are released
+    // only after the wait: an FC2 reads the routing tables before its own wait
+    // (`early`), which is safe once the kernel that wrote them, two launches
+    // back, is known to be complete -- as it is when its successor has waited.
+    const bool early = p.early != 0 && p.items != nullptr;
+    if (!early) {
+        pdl_wait_previous();
+        pdl_launch_dependents();
+    }
     int4 item;                                 // the same for every CTA of the cluster
     if (p.items != nullptr) {
-        if (item_id >= *p.n_items) return;
-        item = p.items[item_id];
+        if (item_id >= (early ? __ldcg(p.n_items) : *p.n_items)) return;
+        item = early ? __ldcg(p.items + item_id) : p.items[item_id];
     } else {
         const int64_t first = (int64_t)item_id * TOK;
         if (first >= p.rows) return;
@@ -364,6 +432,10 @@ moe_linear_kernel(const MoeLinParams p) {
             if (!hdr_ok) {
                 record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
                 mbar_arrive(lut_bar);
+                if (early) {
+                    pdl_wait_previous();
+                    pdl_launch_dependents();
+                }
             } else {
                 mbar_arrive_expect_tx(lut_bar, (uint32_t)((shards ? 2 : 1) * kLutBytes));
                 bulk_g2s(lut, wexp + lut_offset<F16>(), (uint32_t)kLutBytes, lut_bar);
@@ -374,21 +446,19 @@ moe_linear_kernel(const MoeLinParams p) {
                 const uint16_t* xrow[TOK];
                 for (int t = 0; t < nrows; ++t) {
                     const int64_t r = r0 + t;
-                    const int64_t src_row = token_rows ? (int64_t)(p.perm[r] / p.topk) : r;
+                    const int64_t src_row = token_rows ? (int64_t)((early ? __ldcg(p.perm + r) : p.perm[r]) / p.topk) : r;
                     xrow[t] = p.X + src_row * p.K;
                 }
-                int issued = 0;
-                bool ok = true;
-                for (int i = 0; i < nst && ok; ++i) {
-                    const int s = i % kStages;
-                    if (i >= kStages) ok = mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.status);
-                    if (!ok) break;
+                auto stage_xk = [&](int i) {
                     const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
-                    const int64_t kx = (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
-                    const int64_t kx_left = p.K - kx;
-                    const int xk = (int)(kx_left < nb * kBlockK ? kx_left : nb * kBlockK);
+                    const int64_t kx_left = p.K - (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
+                    return (int)(kx_left < nb * kBlockK ? kx_left : nb * kBlockK);
+                };
+                auto issue_weights = [&](int i) {
+                    const int s = i % kStages;
+                    const int nb = min(kBlocksPerStage, nkb - i * kBlocksPerStage);
                     uint8_t* st = ring + s * kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * kBlockBytes + (size_t)nrows * xk * 2));
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * kBlockBytes + (size_t)nrows * stage_xk(i) * 2));
                     for (int b = 0; b < nb; ++b) {
                         const int kb = kb0 + i * kBlocksPerStage + b;
                         if (GATED) {
@@ -399,19 +469,49 @@ moe_linear_kernel(const MoeLinParams p) {
                             bulk_g2s(st + b * kBlockBytes, atom_src(wexp, row_a, kb), kBlockBytes, &full[s]);
                         }
                     }
-                    uint16_t* xsb = reinterpret_cast<uint16_t*>(st + kWeightStageBytes);
+                };
+                auto issue_x = [&](int i) {
+                    const int s = i % kStages, xk = stage_xk(i);
+                    const int64_t kx = (int64_t)(kb0 + i * kBlocksPerStage) * kBlockK;
+                    uint16_t* xsb = reinterpret_cast<uint16_t*>(ring + s * kStageBytes + kWeightStageBytes);
                     for (int t = 0; t < nrows; ++t)
                         bulk_g2s(xsb + t * kXRowElems, xrow[t] + kx, (uint32_t)xk * 2, &full[s]);
+                };
+                int issued = 0;
+                bool ok = true;
+                if (early) {
+                    // the first stages' weights (and the table, above) before the
+                    // wait, their activations after it
+                    const int first = min(nst, kStages);
+                    for (int i = 0; i < first; ++i) issue_weights(i);
+                    pdl_wait_previous();
+                    pdl_launch_dependents();
+                    for (int i = 0; i < first; ++i) issue_x(i);
+                    issued = first;
+                }
+                for (int i = issued; i < nst && ok; ++i) {
+                    const int s = i % kStages;
+                    if (i >= kStages) ok = mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.status);
+                    if (!ok) break;
+                    issue_weights(i);
+                    issue_x(i);
                     ++issued;
                 }
                 mbar_wait(lut_bar, 0, p.status);
                 for (int i = max(0, issued - kStages); i < issued; ++i)
                     mbar_wait(&full[i % kStages], (i / kStages) & 1, p.status);
             }
+        } else if (early) {
+            pdl_wait_previous();
+            pdl_launch_dependents();
         }
         __syncwarp();
         cluster_wait();
     } else {
+        if (early) {
+            pdl_wait_previous();
+            pdl_launch_dependents();
+        }
         const int g = lane >> 2, q = lane & 3;
         bool ok = mbar_wait(lut_bar, 0, p.status) && *hdr_flag != 0;
         // the AWQ stages synchronise the consumer warps: they must all run the loop
@@ -548,6 +648,313 @@ moe_linear_kernel(const MoeLinParams p) {
     }
 }
 
+// ----------------------------------------- persistent grouped streaming --
+// With many work items the layer runs one wave of CTAs instead of one CTA per
+// (item, column group): CTA b walks the units u = b, b + G, ... (G CTAs; u =
+// item * ncg + column group, K whole), and its producer warp keeps the ring
+// streaming across unit boundaries, so no unit pays for a launch, barrier
+// set-up, ring fill or drain.  Each unit's magnitude table (its expert's
+// global) goes through one of two table slots, so the next unit's table lands
+// while the current one is still read.  No split: the gated experts' up rows
+// meet their gate rows through shared memory, the others write from
+// registers.  When the routing tables were written two launches back (FC2 after
+// FC1), the producer reads its first unit and streams that unit's first weight
+// stages and table before the programmatic-launch wait; only the activation
+// copies wait for the preceding kernel.
+// Stages of two 64-k blocks: with three CTAs per SM a ring of two large
+// stages keeps about one stage per CTA in flight while the other is read,
+// which left the consumers waiting on data at a third of the HBM rate; five
+// (four) small stages keep three to four in flight in the same shared memory.
+template <int MT> struct PersistRing;
+template <> struct PersistRing<1> { using G = StreamRing<1, 5, 2>; };
+template <> struct PersistRing<2> { using G = StreamRing<2, 4, 2>; };
+
+struct PersistSmem {
+    static constexpr size_t flags = 112;       // int[2]: the unit in table slot i passed its header check
+    static constexpr size_t lut = 128;         // 2 slots x (1, or 2 with gate/up shards) tables
+};
+
+size_t persist_smem(int MT, bool gated, bool shards) {
+    const int tok = 8 * MT;
+    const size_t ring = MT == 1 ? PersistRing<1>::G::kStages * PersistRing<1>::G::kStageBytes
+                                : PersistRing<2>::G::kStages * PersistRing<2>::G::kStageBytes;
+    const size_t part = gated ? (size_t)tok * 64 * 4 : 0;
+    return PersistSmem::lut + 2 * (shards ? 2 : 1) * kLutBytes + ring + part;
+}
+
+template <int MT, bool GATED, bool F16, bool AWQ>
+__global__ void __launch_bounds__(kThreads, 3)
+moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    using G = typename PersistRing<MT>::G;
+    constexpr int TOK = G::kTok;
+    constexpr int kStages = G::kStages;
+    constexpr int kBlocksPerStage = G::kBlocksPerStage;
+    constexpr uint32_t kWeightStageBytes = G::kWeightStageBytes;
+    constexpr int kXRowElems = G::kXRowElems;
+    constexpr size_t kStageBytes = G::kStageBytes;
+    static_assert((2 * kStages + 4) * 8 <= PersistSmem::flags, "barriers overlap the unit flags");
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kStages;
+    uint64_t* lut_full = empty + kStages;     // table slot i holds the current unit's table(s)
+    uint64_t* lut_empty = lut_full + 2;       // every consumer warp is done with table slot i
+    volatile int* unit_ok = reinterpret_cast<volatile int*>(smem + PersistSmem::flags);
+    const bool shards = GATED && p.half_stride != 0;
+    const int ntab = shards ? 2 : 1;
+    uint4* lut = reinterpret_cast<uint4*>(smem + PersistSmem::lut);
+    uint8_t* ring = smem + PersistSmem::lut + 2 * ntab * kLutBytes;
+    float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);   // gated: up values [64][TOK]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nst = (int)((p.KB + kBlocksPerStage - 1) / kBlocksPerStage);
+    const int64_t stride = gridDim.x;
+    // K is a multiple of 64 here: every k of a stage's blocks holds data
+    auto stage_nb = [&](int i) { return (int)min((int64_t)kBlocksPerStage, p.KB - (int64_t)i * kBlocksPerStage); };
+    auto stage_kx = [&](int i) { return (int64_t)i * kBlocksPerStage * kBlockK; };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&lut_full[i], 1);
+            mbar_init(&lut_empty[i], kWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ---------------- producer: the whole warp issues each stage's copies
+        // (lane b a weight block or half-block, lane t activation row t) after
+        // lane 0 has armed the stage's barrier; lane 0 alone waits on barriers
+        // and the warp follows its verdict.
+        const unsigned all = 0xffffffffu;
+        bool waited = early == 0;
+        if (waited) {
+            pdl_wait_previous();
+            pdl_launch_dependents();
+        }
+        const int64_t units = (int64_t)__ldcg(p.n_items) * ncg;
+        const bool token_rows = GATED || p.act != 0;
+        int gs = 0;                    // stages issued so far
+        int j = 0;                     // units taken so far
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units && ok; u += stride, ++j) {
+            const int4 item = __ldcg(p.items + u / ncg);
+            const int cgi = (int)(u % ncg);
+            const int e = item.x, r0 = item.y, nrows = item.z;
+            const uint8_t* wexp = p.w + (size_t)e * p.w_stride;
+            const uint8_t* wup = shards ? wexp + p.half_stride : wexp;
+            const int slot = j & 1;
+            int hdr_ok = 0;
+            if (lane == 0) {
+                const Header* hdr = reinterpret_cast<const Header*>(wexp);
+                const Header* hdr_up = reinterpret_cast<const Header*>(wup);
+                hdr_ok = hdr->magic == kMagic && hdr->N == p.N && hdr->K == p.K &&
+                         (!shards || (hdr_up->magic == kMagic && hdr_up->N == p.N && hdr_up->K == p.K));
+                if (j >= 2) ok = mbar_wait(&lut_empty[slot], ((j >> 1) - 1) & 1, p.status);
+                if (ok) {
+                    unit_ok[slot] = hdr_ok;
+                    if (!hdr_ok) {
+                        record_status(p.status, NVFP4_ERR_BAD_WEIGHT);
+                        mbar_arrive(&lut_full[slot]);          // the consumers skip this unit
+                    } else {
+                        uint4* ls = lut + slot * ntab * 256;
+                        mbar_arrive_expect_tx(&lut_full[slot], (uint32_t)(ntab * kLutBytes));
+                        bulk_g2s(ls, wexp + lut_offset<F16>(), (uint32_t)kLutBytes, &lut_full[slot]);
+                        if (shards) bulk_g2s(ls + 256, wup + lut_offset<F16>(), (uint32_t)kLutBytes, &lut_full[slot]);
+                    }
+                }
+            }
+            ok = __shfl_sync(all, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;                            // unit j was not taken: j units were
+            if (!__shfl_sync(all, hdr_ok, 0)) continue;
+            // this lane's copies: weight block (or gate / up half-block) `lane`
+            // of each stage, and activation row `lane`
+            const int64_t row_a = GATED ? (int64_t)cgi * 64 : (int64_t)cgi * 128;
+            const int64_t row_b = GATED ? (shards ? 0 : p.I) + (int64_t)cgi * 64 : 0;
+            constexpr int kCopiesPerBlock = GATED ? 2 : 1;
+            const int wb = lane / kCopiesPerBlock;                        // block within the stage
+            const bool up_half = GATED && (lane & 1);
+            const int64_t rbg = (up_half ? row_b : row_a) / kAtomRows;
+            const uint8_t* wsrc = (up_half ? wup : wexp) + kTilesOffset +
+                                  atom_offset(rbg / kAtomsPerTileK, 0, rbg % kAtomsPerTileK, p.KB);
+            constexpr uint32_t kCopyBytes = kBlockBytes / kCopiesPerBlock;
+            const size_t kb_stride = (size_t)kAtomsPerTileK * kAtomBytes;
+            const uint16_t* xsrc = p.X;
+            if (lane < nrows) {
+                const int64_t r = r0 + lane;
+                xsrc = p.X + (token_rows ? (int64_t)(__ldcg(p.perm + r) / p.topk) : r) * p.K;
+            }
+            auto issue_weights = [&](int i, int s) {
+                const int nb = stage_nb(i);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * kBlockBytes + (size_t)nrows * nb * kBlockK * 2));
+                __syncwarp();
+                if (wb < nb)
+                    bulk_g2s(ring + s * kStageBytes + lane * kCopyBytes,
+                             wsrc + (size_t)(i * kBlocksPerStage + wb) * kb_stride, kCopyBytes, &full[s]);
+            };
+            auto issue_x = [&](int i, int s) {
+                if (lane < nrows)
+                    bulk_g2s(ring + s * kStageBytes + kWeightStageBytes + lane * kXRowElems * 2,
+                             xsrc + stage_kx(i), (uint32_t)(stage_nb(i) * kBlockK * 2), &full[s]);
+            };
+            int i = 0;
+            if (!waited) {
+                // weights (and the table, above) before the wait, activations
+                // after it; no stage has been issued yet (gs == 0)
+                const int pre = min(nst, kStages);
+                for (; i < pre; ++i) issue_weights(i, i);
+                pdl_wait_previous();
+                pdl_launch_dependents();
+                waited = true;
+                for (int k = 0; k < pre; ++k) issue_x(k, k);
+                gs = pre;
+            }
+            for (; i < nst; ++i, ++gs) {
+                const int s = gs % kStages;
+                if (gs >= kStages) {
+                    bool got = true;
+                    if (lane == 0) got = mbar_wait(&empty[s], ((gs / kStages) - 1) & 1, p.status);
+                    if (!(ok = __shfl_sync(all, got ? 1 : 0, 0) != 0)) break;
+                }
+                issue_weights(i, s);
+                issue_x(i, s);
+            }
+        }
+        if (!waited) {
+            pdl_wait_previous();
+            pdl_launch_dependents();
+        }
+        // never leave a copy in flight into this CTA's shared memory
+        if (lane == 0) {
+            for (int k = max(0, j - 2); k < j; ++k) mbar_wait(&lut_full[k & 1], (k >> 1) & 1, p.status);
+            for (int k = max(0, gs - kStages); k < gs; ++k) mbar_wait(&full[k % kStages], (k / kStages) & 1, p.status);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers
+        pdl_wait_previous();
+        pdl_launch_dependents();
+        const int g = lane >> 2, q = lane & 3, c = lane & 3;
+        const int64_t units = (int64_t)(*p.n_items) * ncg;
+        const uint8_t* const a0 = ring + warp * kAtomBytes;
+        const uint16_t* const x0 = reinterpret_cast<const uint16_t*>(ring + kWeightStageBytes) +
+                                   g * kXRowElems + q * 16;
+        using AwqStagesT = AwqStages<F16, kXRowElems, TOK, kBlocksPerStage, kWarps * 32>;
+        AwqStagesT awq;
+        // every unit walks the same k stages: the scales of stage i are unit-independent
+        if constexpr (AWQ) awq.prefetch(p.pqs, TOK, stage_nb(0) * kBlockK, tid);
+        int s = 0;
+        uint32_t phase = 0;
+        int j = 0;
+        int4 item = (int64_t)blockIdx.x < units ? p.items[blockIdx.x / ncg] : make_int4(0, 0, 0, 0);
+        for (int64_t u = blockIdx.x; u < units; u += stride, ++j) {
+            const int slot = j & 1;
+            const int cgi = (int)(u % ncg);
+            const int r0 = item.y, nrows = item.z;
+            // the next unit's item, and this unit's routing slots and weights
+            // (FC2 epilogue), load while the stages stream
+            if (u + stride < units) item = p.items[(u + stride) / ncg];
+            int32_t sl[MT][2];
+            float pw[MT][2];
+            if constexpr (!GATED) {
+                #pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+                    #pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = mt * 8 + 2 * c + h;
+                        sl[mt][h] = (p.act == 0 && t < nrows) ? p.perm[r0 + t] : 0;
+                        pw[mt][h] = (p.act == 0 && t < nrows) ? p.wts[sl[mt][h]] : 0.0f;
+                    }
+            }
+            // every consumer warp leaves together when one could not go on
+            if (!named_bar_red_and(1, kWarps * 32, mbar_wait(&lut_full[slot], (j >> 1) & 1, p.status))) break;
+            const bool valid = unit_ok[slot] != 0;
+            const int64_t row_a = GATED ? (int64_t)cgi * 64 : (int64_t)cgi * 128;
+            const bool rows_valid = GATED || row_a + warp * kAtomRows < p.N;
+            const uint32_t lut_s = smem_u32(lut + slot * ntab * 256 + ((shards && warp >= 4) ? 256 : 0));
+            float acc[MT][4];
+            #pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                #pragma unroll
+                for (int v = 0; v < 4; ++v) acc[mt][v] = 0.0f;
+            bool ok = true;
+            if (valid) {
+                for (int i = 0; i < nst; ++i) {
+                    const bool got = mbar_wait(&full[s], phase, p.status);
+                    if constexpr (!AWQ) {
+                        if (!got) { ok = false; break; }
+                    } else {
+                        AwqStagesT nxt = awq;
+                        const int in = i + 1 < nst ? i + 1 : 0;
+                        nxt.prefetch(p.pqs + stage_kx(in), TOK, stage_nb(in) * kBlockK, tid);
+                        if (got)
+                            awq.apply(reinterpret_cast<uint16_t*>(ring + s * kStageBytes + kWeightStageBytes), nrows,
+                                      stage_nb(i) * kBlockK, tid);
+                        awq = nxt;
+                        if (!named_bar_red_and(1, kWarps * 32, got)) { ok = false; break; }
+                    }
+                    if (rows_valid)
+                        stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
+                            a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), stage_nb(i), acc);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    if (++s == kStages) { s = 0; phase ^= 1u; }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&lut_empty[slot]);
+            if (!named_bar_red_and(1, kWarps * 32, ok)) break;
+            if (!valid) continue;
+            if constexpr (GATED) {
+                // up rows (warps 4-7) hand their values to the gate rows (warps 0-3)
+                if (warp >= 4) {
+                    #pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+                        #pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int jj = (warp - 4) * 16 + g + (v >= 2 ? 8 : 0);
+                            part[jj * TOK + mt * 8 + 2 * c + (v & 1)] = acc[mt][v];
+                        }
+                }
+                named_bar_sync(2, kWarps * 32);
+                if (warp < 4) {
+                    #pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+                        #pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int jj = warp * 16 + g + (v >= 2 ? 8 : 0);
+                            const int t = mt * 8 + 2 * c + (v & 1);
+                            if (t < nrows)
+                                p.H[(int64_t)(r0 + t) * p.I + (int64_t)cgi * 64 + jj] =
+                                    f32_to_act_bits<F16>(silu_f(acc[mt][v]) * part[jj * TOK + t]);
+                        }
+                }
+                named_bar_sync(2, kWarps * 32);
+            } else {
+                #pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+                    #pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int t = mt * 8 + 2 * c + (v & 1);
+                        const int64_t n = row_a + warp * 16 + g + (v >= 2 ? 8 : 0);
+                        if (t < nrows && n < p.N) {
+                            if (p.act != 0)
+                                p.H[(int64_t)(r0 + t) * p.N + n] = f32_to_act_bits<F16>(plain_act(acc[mt][v], p.act));
+                            else
+                                p.Yp[(int64_t)sl[mt][v & 1] * p.N + n] = pw[mt][v & 1] * acc[mt][v];
+                        }
+                    }
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------- combine --
 template <bool F16>
 __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk, int64_t H,
@@ -644,6 +1051,48 @@ nvfp4_status launch_moe_linear_typed(const MoeLinParams& p, unsigned gx, unsigne
     return check_cuda(e, GATED ? "MoE FC1: launch" : "MoE FC2: launch");
 }
 
+// Resident CTAs per SM of a persistent instance (registers, shared memory and
+// threads), looked up once per instance.
+template <int MT, bool GATED, bool F16, bool AWQ>
+int persist_ctas_per_sm(size_t smem) {
+    static int cache[2] = {0, 0};
+    static std::once_flag once[2];
+    const int k = smem > persist_smem(MT, GATED, false) ? 1 : 0;      // with gate/up shards
+    std::call_once(once[k], [&] {
+        int n = 0;
+        if (cudaFuncSetAttribute(moe_persist_kernel<MT, GATED, F16, AWQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe_persist_kernel<MT, GATED, F16, AWQ>, kThreads,
+                                                          smem) == cudaSuccess)
+            cache[k] = n;
+    });
+    return cache[k];
+}
+
+template <int MT, bool GATED, bool F16, bool AWQ>
+nvfp4_status launch_moe_persist_typed(const MoeLinParams& p, int ncg, int64_t max_units, bool early, cudaStream_t s) {
+    const size_t smem = persist_smem(MT, GATED, GATED && p.half_stride != 0);
+    cudaError_t e = cudaFuncSetAttribute(moe_persist_kernel<MT, GATED, F16, AWQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return check_cuda(e, "MoE persistent linear: shared memory attribute");
+    const int per_sm = std::max(1, persist_ctas_per_sm<MT, GATED, F16, AWQ>(smem));
+    const int64_t grid = std::min<int64_t>(max_units, (int64_t)per_sm * sm_count());
+    return launch_chained(moe_persist_kernel<MT, GATED, F16, AWQ>, dim3((unsigned)std::max<int64_t>(grid, 1)),
+                          dim3(kThreads), smem, s, GATED ? "MoE FC1 (persistent): launch" : "MoE FC2 (persistent): launch",
+                          p, ncg, early ? 1 : 0);
+}
+
+// The persistent instance for the activation type and AWQ choice.
+template <int MT, bool GATED>
+nvfp4_status launch_moe_persist(const MoeLinParams& p, int ncg, int64_t max_units, bool early, bool f16,
+                                cudaStream_t s) {
+    if (p.pqs != nullptr)
+        return f16 ? launch_moe_persist_typed<MT, GATED, true, true>(p, ncg, max_units, early, s)
+                   : launch_moe_persist_typed<MT, GATED, false, true>(p, ncg, max_units, early, s);
+    return f16 ? launch_moe_persist_typed<MT, GATED, true, false>(p, ncg, max_units, early, s)
+               : launch_moe_persist_typed<MT, GATED, false, false>(p, ncg, max_units, early, s);
+}
+
 template <int MT, bool GATED>
 nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_items, bool f16, cudaStream_t s) {
     // AWQ instances: FC1 with a pre-quant scale on its input
@@ -700,13 +1149,9 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
                             int32_t* n_items, cudaStream_t s) {
     nvfp4_status st;
     const size_t psmem = permute_smem_bytes(E);
-    if (T <= kFusedRouteMaxT) {
-        cudaError_t ce = cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)psmem);
-        if ((st = check_cuda(ce, "MoE route+permute: shared memory attribute")) != NVFP4_OK) return st;
-        return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE route+permute: launch",
+    if (T <= kFusedRouteMaxT)
+        return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), 0, s, "MoE route+permute: launch",
                               router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items);
-    }
     st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
                         router_logits, T, E, topk, idx, wts);
     if (st != NVFP4_OK) return st;
@@ -715,6 +1160,16 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
     return launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
                           (const int32_t*)idx, T * topk, E, tok, offsets, perm, inv, items, n_items);
 }
+
+// Work items expected in flight, for the split-K and persistent choices of the
+// streaming path (the exact count is known only on the device).
+int64_t moe_est_items(const MoeLayout& L, int64_t n, int E) {
+    return std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
+}
+
+// Units (item x column group) for several waves: one persistent wave walks
+// them without splitting K; fewer: a CTA per unit, K split across a cluster.
+bool moe_use_persist(int64_t fc1_groups, int64_t est_items) { return fc1_groups * est_items >= 4LL * sm_count(); }
 
 int moe_splits(int64_t base_ctas, int64_t KB, int kbs_min) {
     int64_t splits = std::max<int64_t>(1, ceil_div(2LL * sm_count(), std::max<int64_t>(base_ctas, 1)));
@@ -743,6 +1198,29 @@ extern "C" nvfp4_status nvfp4_moe_route(const float* router_logits, int64_t T, i
         return fail(NVFP4_ERR_ALIGNMENT, "%s: every pointer must be 4-byte aligned", fn);
     return launch_routing(router_logits, T, E, topk, 1, topk_idx_out, topk_weight_out, offsets_out, perm_out,
                           inv_out, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" nvfp4_status nvfp4_w4a16_moe_plan(int64_t T, int E, int topk, int64_t H, int64_t I, int activation,
+                                             int* path_out, int* rows_per_item_out) {
+    const char* fn = "nvfp4_w4a16_moe_plan";
+    if (!path_out || !rows_per_item_out) return fail(NVFP4_ERR_INVALID_ARG, "%s: null output pointer", fn);
+    if (activation < NVFP4_MOE_SWIGLU || activation > NVFP4_MOE_SILU)
+        return fail(NVFP4_ERR_INVALID_ARG, "%s: activation=%d is not one of SWIGLU, RELU2, SILU", fn, activation);
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: T=%lld is negative", fn, (long long)T);
+    if (E < 1 || E > kMaxExperts) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: E=%d outside [1, %d]", fn, E, kMaxExperts);
+    if (topk < 1 || topk > kMaxTopk || topk > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: topk=%d outside [1, min(E, %d)]", fn, topk, kMaxTopk);
+    if (H <= 0 || I <= 0 || H % 64 != 0 || I % 64 != 0)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: H=%lld and I=%lld must be positive multiples of 64", fn, (long long)H, (long long)I);
+    if (T == 0) {
+        *path_out = 0;
+        *rows_per_item_out = 0;
+        return NVFP4_OK;
+    }
+    const MoeLayout L = moe_layout(T, E, topk, H, I);
+    const int64_t fc1_groups = activation == NVFP4_MOE_SWIGLU ? I / 64 : ceil_div(I, 128);
+    *path_out = L.tile ? 3 : moe_use_persist(fc1_groups, moe_est_items(L, T * topk, E)) ? 2 : 1;
+    *rows_per_item_out = L.tok;
+    return NVFP4_OK;
 }
 
 extern "C" size_t nvfp4_w4a16_moe_workspace(int64_t T, int E, int topk, int64_t H, int64_t I) {
@@ -831,20 +1309,27 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         t2.N = H; t2.K = I; t2.Yp = yp; t2.H = nullptr;
         if ((st = launch_tc_moe(t2, s)) != NVFP4_OK) return st;
     } else {
-        // expected work items in flight, for the split-K choice
-        const int64_t est_items = std::min<int64_t>(L.max_items, std::max<int64_t>(ceil_div(n, L.tok), std::min<int64_t>(E, n)));
+        const int64_t est_items = moe_est_items(L, n, E);
         MoeLinParams p1{};
         p1.w = (const uint8_t*)fc1; p1.w_stride = fc1_stride; p1.half_stride = half_stride;
         p1.N = fc1_rows; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
         const int64_t fc1_groups = gated ? I / 64 : ceil_div(I, 128);     // CTAs per item along the rows
-        p1.splits = moe_splits(fc1_groups * est_items, p1.KB, 4);
+        const bool persist = moe_use_persist(fc1_groups, est_items);
+        p1.splits = persist ? 1 : moe_splits(fc1_groups * est_items, p1.KB, 4);
         p1.kbs = (int)ceil_div(p1.KB, p1.splits);
         p1.splits = (int)ceil_div(p1.KB, p1.kbs);
         p1.X = (const uint16_t*)X; p1.perm = perm; p1.topk = topk; p1.items = items; p1.n_items = n_items;
         p1.I = I; p1.H = hbuf; p1.wts = wts; p1.status = status;
         p1.pqs = (const uint16_t*)fc1_pre_quant_scale;
         p1.act = gated ? 0 : activation;
-        if (gated)
+        const int64_t fc1_max_units = fc1_groups * L.max_items;
+        if (persist && gated)
+            st = L.mt == 1 ? launch_moe_persist<1, true>(p1, (int)fc1_groups, fc1_max_units, false, f16, s)
+                           : launch_moe_persist<2, true>(p1, (int)fc1_groups, fc1_max_units, false, f16, s);
+        else if (persist)
+            st = L.mt == 1 ? launch_moe_persist<1, false>(p1, (int)fc1_groups, fc1_max_units, false, f16, s)
+                           : launch_moe_persist<2, false>(p1, (int)fc1_groups, fc1_max_units, false, f16, s);
+        else if (gated)
             st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
                            : launch_moe_linear<2, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
         else
@@ -855,13 +1340,20 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         MoeLinParams p2{};
         p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
         p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
-        p2.splits = moe_splits(ceil_div(H, 128) * est_items, p2.KB, 4);
+        p2.splits = persist ? 1 : moe_splits(ceil_div(H, 128) * est_items, p2.KB, 4);
         p2.kbs = (int)ceil_div(p2.KB, p2.splits);
         p2.splits = (int)ceil_div(p2.KB, p2.kbs);
         p2.X = hbuf; p2.perm = perm; p2.topk = topk; p2.items = items; p2.n_items = n_items;
         p2.I = I; p2.Yp = yp; p2.wts = wts; p2.status = status;
-        st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s)
-                       : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s);
+        p2.early = 1;          // FC1 released it after its own wait: routing is complete
+        // the routing tables were written two launches back: the persistent FC2
+        // streams its first weights before waiting for FC1
+        if (persist)
+            st = L.mt == 1 ? launch_moe_persist<1, false>(p2, (int)ceil_div(H, 128), ceil_div(H, 128) * L.max_items, true, f16, s)
+                           : launch_moe_persist<2, false>(p2, (int)ceil_div(H, 128), ceil_div(H, 128) * L.max_items, true, f16, s);
+        else
+            st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s)
+                           : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
     }
 
