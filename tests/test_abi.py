@@ -217,7 +217,8 @@ def test_moe_plan_on_host(lib):
     assert nv.moe_plan(0, E, k, H, I) == {"path": "none", "rows_per_item": 0}
     assert nv.moe_plan(1, E, k, H, I) == {"path": "stream_split", "rows_per_item": 8}
     assert nv.moe_plan(16, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 8}
-    assert nv.moe_plan(256, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 16}
+    assert nv.moe_plan(256, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 32}
+    assert nv.moe_plan(160, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 16}
     assert nv.moe_plan(4096, E, k, H, I) == {"path": "tile", "rows_per_item": 256}
     # non-gated experts have half the FC1 column groups
     assert nv.moe_plan(16, E, k, H, I, "relu2")["path"] in ("stream_split", "stream_persistent")

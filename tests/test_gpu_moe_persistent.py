@@ -3,8 +3,8 @@
 With many (work item, column group) units the streaming path runs one wave of
 CTAs that walk the units with K whole (moe_plan path "stream_persistent").
 These cases are sized so that the plan takes that path on a GB300 (and on any
-GPU with up to 256 SMs), at oracle sizes: gated SwiGLU experts with 8- and
-16-row items, AWQ with its dropped-scale control, FP16 activations, non-gated
+GPU with up to 256 SMs), at oracle sizes: gated SwiGLU experts with 8-, 16- and
+32-row items, AWQ with its dropped-scale control, FP16 activations, non-gated
 relu2 / silu experts, gate/up shards with their own globals, and run-to-run
 bitwise determinism.  The bar is the GEMM parity bar against the oracle's
 output; the routing tables are compared bit for bit.
@@ -66,9 +66,10 @@ def _oracle_plain(c, fc1, fc2, act="bf16", activation="swiglu", awq=False):
                           pqs_bits=c.pqs_bits if awq else None)
 
 
-# (64, 64, 8, 256, 1024): 8 rows per expert -> 8-row items;
-# (128, 64, 8, 128, 1024): 16 rows per expert -> 16-row items
-@pytest.mark.parametrize("T,E,topk,H,I,rows", [(64, 64, 8, 256, 1024, 8), (128, 64, 8, 128, 1024, 16)])
+# routed rows per expert on average: 8 -> 8-row items, 10 -> 16-row items,
+# 16 -> 32-row items
+@pytest.mark.parametrize("T,E,topk,H,I,rows", [(64, 64, 8, 256, 1024, 8), (80, 64, 8, 128, 1024, 16),
+                                               (128, 64, 8, 128, 1024, 32)])
 def test_persistent_gated_full_compare(T, E, topk, H, I, rows):
     _assert_persistent(T, E, topk, H, I, rows)
     c, fc1, fc2 = _case(T, E, topk, H, I, seed=T + E + I)
@@ -95,7 +96,7 @@ def test_persistent_awq_and_dropped_scale_control():
 
 def test_persistent_f16_activations():
     T, E, topk, H, I = 128, 64, 8, 128, 1024
-    _assert_persistent(T, E, topk, H, I, 16)
+    _assert_persistent(T, E, topk, H, I, 32)
     c, fc1, fc2 = _case(T, E, topk, H, I, seed=43, act="f16", awq=True)
     out, _ = _run(c, _stack(fc1, 2 * I, H), _stack(fc2, H, I), act="f16", awq=True)
     ref = _oracle_plain(c, fc1, fc2, act="f16", awq=True)

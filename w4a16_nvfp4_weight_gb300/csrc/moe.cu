@@ -300,6 +300,7 @@ constexpr uint32_t kBlockBytes = kStreamBlockBytes;            // 4608 per 64-k 
 template <int MT> struct MoeRing;
 template <> struct MoeRing<1> { using G = StreamRing<1, 3, 4>; };
 template <> struct MoeRing<2> { using G = StreamRing<2, 2, 4>; };
+template <> struct MoeRing<4> { using G = StreamRing<4, 2, 4>; };
 constexpr size_t kRingOffset = 128;
 
 struct MoeLinParams {
@@ -668,6 +669,7 @@ moe_linear_kernel(const MoeLinParams p) {
 template <int MT> struct PersistRing;
 template <> struct PersistRing<1> { using G = StreamRing<1, 5, 2>; };
 template <> struct PersistRing<2> { using G = StreamRing<2, 4, 2>; };
+template <> struct PersistRing<4> { using G = StreamRing<4, 3, 2>; };
 
 struct PersistSmem {
     static constexpr size_t flags = 112;       // int[2]: the unit in table slot i passed its header check
@@ -676,10 +678,12 @@ struct PersistSmem {
 
 size_t persist_smem(int MT, bool gated, bool shards) {
     const int tok = 8 * MT;
-    const size_t ring = MT == 1 ? PersistRing<1>::G::kStages * PersistRing<1>::G::kStageBytes
-                                : PersistRing<2>::G::kStages * PersistRing<2>::G::kStageBytes;
+    const size_t ring = MT == 1   ? PersistRing<1>::G::kStages * PersistRing<1>::G::kStageBytes
+                        : MT == 2 ? PersistRing<2>::G::kStages * PersistRing<2>::G::kStageBytes
+                                  : PersistRing<4>::G::kStages * PersistRing<4>::G::kStageBytes;
     const size_t part = gated ? (size_t)tok * 64 * 4 : 0;
-    return PersistSmem::lut + 2 * (shards ? 2 : 1) * kLutBytes + ring + part;
+    const size_t epi = (size_t)2 * tok * 8;        // FC2: routing slot and weight per row, per table slot
+    return PersistSmem::lut + 2 * (shards ? 2 : 1) * kLutBytes + ring + part + epi;
 }
 
 template <int MT, bool GATED, bool F16, bool AWQ>
@@ -704,6 +708,10 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
     uint4* lut = reinterpret_cast<uint4*>(smem + PersistSmem::lut);
     uint8_t* ring = smem + PersistSmem::lut + 2 * ntab * kLutBytes;
     float* part = reinterpret_cast<float*>(ring + kStages * kStageBytes);   // gated: up values [64][TOK]
+    // FC2 epilogue operands of the unit in table slot i: routing slot and
+    // routing weight of each row, written by the producer with the unit's table
+    int32_t* ep_slot = reinterpret_cast<int32_t*>(part + (GATED ? 64 * TOK : 0));   // [2][TOK]
+    float* ep_w = reinterpret_cast<float*>(ep_slot + 2 * TOK);                      // [2][TOK]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nst = (int)((p.KB + kBlocksPerStage - 1) / kBlocksPerStage);
@@ -787,7 +795,13 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
             if (lane < nrows) {
                 const int64_t r = r0 + lane;
                 xsrc = p.X + (token_rows ? (int64_t)(__ldcg(p.perm + r) / p.topk) : r) * p.K;
+                if (!token_rows) {
+                    const int32_t sl = __ldcg(p.perm + r);
+                    ep_slot[slot * TOK + lane] = sl;
+                    ep_w[slot * TOK + lane] = __ldcg(p.wts + sl);
+                }
             }
+            __syncwarp();          // those writes before lane 0 arms the unit's first stage
             auto issue_weights = [&](int i, int s) {
                 const int nb = stage_nb(i);
                 if (lane == 0)
@@ -856,21 +870,8 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
             const int slot = j & 1;
             const int cgi = (int)(u % ncg);
             const int r0 = item.y, nrows = item.z;
-            // the next unit's item, and this unit's routing slots and weights
-            // (FC2 epilogue), load while the stages stream
+            // the next unit's item loads while this unit's stages stream
             if (u + stride < units) item = p.items[(u + stride) / ncg];
-            int32_t sl[MT][2];
-            float pw[MT][2];
-            if constexpr (!GATED) {
-                #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int t = mt * 8 + 2 * c + h;
-                        sl[mt][h] = (p.act == 0 && t < nrows) ? p.perm[r0 + t] : 0;
-                        pw[mt][h] = (p.act == 0 && t < nrows) ? p.wts[sl[mt][h]] : 0.0f;
-                    }
-            }
             // every consumer warp leaves together when one could not go on
             if (!named_bar_red_and(1, kWarps * 32, mbar_wait(&lut_full[slot], (j >> 1) & 1, p.status))) break;
             const bool valid = unit_ok[slot] != 0;
@@ -907,10 +908,8 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
                     if (++s == kStages) { s = 0; phase ^= 1u; }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&lut_empty[slot]);
             if (!named_bar_red_and(1, kWarps * 32, ok)) break;
-            if (!valid) continue;
+            if (valid) {
             if constexpr (GATED) {
                 // up rows (warps 4-7) hand their values to the gate rows (warps 0-3)
                 if (warp >= 4) {
@@ -947,10 +946,14 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
                             if (p.act != 0)
                                 p.H[(int64_t)(r0 + t) * p.N + n] = f32_to_act_bits<F16>(plain_act(acc[mt][v], p.act));
                             else
-                                p.Yp[(int64_t)sl[mt][v & 1] * p.N + n] = pw[mt][v & 1] * acc[mt][v];
+                                p.Yp[(int64_t)ep_slot[slot * TOK + t] * p.N + n] = ep_w[slot * TOK + t] * acc[mt][v];
                         }
                     }
             }
+            }
+            // the table slot (and its epilogue operands) may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&lut_empty[slot]);
         }
     }
 }
@@ -1022,8 +1025,9 @@ nvfp4_status launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, si
 size_t moe_lin_smem(int MT, bool gated, bool shards) {
     const int tok = 8 * MT;
     const size_t part = gated ? ((size_t)tok * 64 + 8) * 2 : (size_t)tok * 128 + 8;
-    const size_t ring = MT == 1 ? MoeRing<1>::G::kStages * MoeRing<1>::G::kStageBytes
-                                : MoeRing<2>::G::kStages * MoeRing<2>::G::kStageBytes;
+    const size_t ring = MT == 1   ? MoeRing<1>::G::kStages * MoeRing<1>::G::kStageBytes
+                        : MT == 2 ? MoeRing<2>::G::kStages * MoeRing<2>::G::kStageBytes
+                                  : MoeRing<4>::G::kStages * MoeRing<4>::G::kStageBytes;
     return kRingOffset + (shards ? 2 : 1) * kLutBytes + ring + part * 4;
 }
 
@@ -1103,6 +1107,23 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
                : launch_moe_linear_typed<MT, GATED, false, false>(p, gx, max_items, s);
 }
 
+// The instances for 8, 16 or 32 routed rows per work item.
+template <bool GATED>
+nvfp4_status launch_moe_linear_mt(int mt, const MoeLinParams& p, unsigned gx, unsigned max_items, bool f16,
+                                  cudaStream_t s) {
+    return mt == 1   ? launch_moe_linear<1, GATED>(p, gx, max_items, f16, s)
+           : mt == 2 ? launch_moe_linear<2, GATED>(p, gx, max_items, f16, s)
+                     : launch_moe_linear<4, GATED>(p, gx, max_items, f16, s);
+}
+
+template <bool GATED>
+nvfp4_status launch_moe_persist_mt(int mt, const MoeLinParams& p, int ncg, int64_t max_units, bool early, bool f16,
+                                   cudaStream_t s) {
+    return mt == 1   ? launch_moe_persist<1, GATED>(p, ncg, max_units, early, f16, s)
+           : mt == 2 ? launch_moe_persist<2, GATED>(p, ncg, max_units, early, f16, s)
+                     : launch_moe_persist<4, GATED>(p, ncg, max_units, early, f16, s);
+}
+
 struct MoeLayout {
     size_t idx, wts, offsets, perm, inv, items, n_items, xp, h, yp, total;
     bool tile;              // tensor-core tile path (many rows per expert) or the streaming path
@@ -1121,7 +1142,10 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
     // twice when its rows need two items.
     L.tile = per_expert >= 32 && I % 128 == 0;
     L.subm = per_expert >= 192 ? 2 : 1;
-    L.mt = per_expert > 8 ? 2 : 1;
+    // rows per streaming item: 8, 16 or 32 -- at 13 or more rows per expert on
+    // average 32-row items hold most experts whole, so that their weights are
+    // expanded once instead of once per 16 rows
+    L.mt = per_expert > 12 ? 4 : per_expert > 8 ? 2 : 1;
     L.tok = L.tile ? 128 * L.subm : 8 * L.mt;
     L.max_items = ceil_div(n, L.tok) + std::min<int64_t>(E, n);
     size_t off = 0;
@@ -1323,18 +1347,12 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         p1.pqs = (const uint16_t*)fc1_pre_quant_scale;
         p1.act = gated ? 0 : activation;
         const int64_t fc1_max_units = fc1_groups * L.max_items;
-        if (persist && gated)
-            st = L.mt == 1 ? launch_moe_persist<1, true>(p1, (int)fc1_groups, fc1_max_units, false, f16, s)
-                           : launch_moe_persist<2, true>(p1, (int)fc1_groups, fc1_max_units, false, f16, s);
-        else if (persist)
-            st = L.mt == 1 ? launch_moe_persist<1, false>(p1, (int)fc1_groups, fc1_max_units, false, f16, s)
-                           : launch_moe_persist<2, false>(p1, (int)fc1_groups, fc1_max_units, false, f16, s);
-        else if (gated)
-            st = L.mt == 1 ? launch_moe_linear<1, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
-                           : launch_moe_linear<2, true>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
+        if (persist)
+            st = gated ? launch_moe_persist_mt<true>(L.mt, p1, (int)fc1_groups, fc1_max_units, false, f16, s)
+                       : launch_moe_persist_mt<false>(L.mt, p1, (int)fc1_groups, fc1_max_units, false, f16, s);
         else
-            st = L.mt == 1 ? launch_moe_linear<1, false>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
-                           : launch_moe_linear<2, false>(p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
+            st = gated ? launch_moe_linear_mt<true>(L.mt, p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s)
+                       : launch_moe_linear_mt<false>(L.mt, p1, (unsigned)fc1_groups, (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
 
         MoeLinParams p2{};
@@ -1348,12 +1366,9 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         p2.early = 1;          // FC1 released it after its own wait: routing is complete
         // the routing tables were written two launches back: the persistent FC2
         // streams its first weights before waiting for FC1
-        if (persist)
-            st = L.mt == 1 ? launch_moe_persist<1, false>(p2, (int)ceil_div(H, 128), ceil_div(H, 128) * L.max_items, true, f16, s)
-                           : launch_moe_persist<2, false>(p2, (int)ceil_div(H, 128), ceil_div(H, 128) * L.max_items, true, f16, s);
-        else
-            st = L.mt == 1 ? launch_moe_linear<1, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s)
-                           : launch_moe_linear<2, false>(p2, (unsigned)ceil_div(H, 128), (unsigned)L.max_items, f16, s);
+        const unsigned fc2_groups = (unsigned)ceil_div(H, 128);
+        st = persist ? launch_moe_persist_mt<false>(L.mt, p2, (int)fc2_groups, fc2_groups * L.max_items, true, f16, s)
+                     : launch_moe_linear_mt<false>(L.mt, p2, fc2_groups, (unsigned)L.max_items, f16, s);
         if (st != NVFP4_OK) return st;
     }
 
