@@ -3,15 +3,19 @@
 //   route    -- one warp per token: top-k of the FP32 router logits (ties to
 //               the lower expert index, slots in descending-logit order) and
 //               p = softmax over the k selected logits.
-//   permute  -- one CTA: per-expert counts, offsets (exclusive scan), a stable
-//               counting sort of the routing slots t*k+j by expert (so by
-//               expert, then token, then slot), its inverse, and a list of
-//               work items (expert, first permuted row, rows <= TOK).
+//   permute  -- one CTA: per-expert counts, offsets (exclusive scan), the
+//               stable sort of the routing slots t*k+j by expert (so by expert,
+//               then token, then slot) from per-expert token bitmasks (a
+//               slot's place is its expert's offset plus the set bits below
+//               its token), its inverse, and a list of work items (expert,
+//               first permuted row, rows <= TOK).  Up to 64 tokens one CTA
+//               routes and permutes.
 //   fc1      -- per work item and 64 intermediate columns: the gate rows and
 //               the matching up rows of the expert's FC1 weight, streamed like
-//               the dense decode kernel (bulk-copy ring, split-K across a
-//               cluster, push-based reduction); the epilogue applies
-//               h = RN(silu(g) * u) and writes H in permuted row order.
+//               the dense decode kernel (bulk-copy ring; with few units, split-K
+//               across a cluster and a push-based reduction; with many, one
+//               persistent wave walking the units with K whole); the epilogue
+//               applies h = RN(silu(g) * u) and writes H in permuted row order.
 //               Non-gated experts (relu2 / silu): 128 rows of [I, H] per CTA,
 //               h = RN(act(v)).  With many rows per expert the tcgen05 tile
 //               kernel (gemm_tc.cu) runs FC1 and FC2 instead.
@@ -120,106 +124,127 @@ __global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E,
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
-// Warp w owns the contiguous slot range [w*seg, (w+1)*seg).  Pass 1 counts each
-// warp's slots per expert (warp-private counters, 32 slots at a time with
-// __match_any_sync); a scan over experts and warps gives every (warp, expert)
-// its first position; pass 2 walks the same slots again and places them.
-// Slots of one expert therefore keep their flat order t*k+j: stable.
-__device__ void permute_block(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
-                              int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                              int4* __restrict__ items, int32_t* __restrict__ n_items, int* perm_smem) {
-    int* wcnt = perm_smem;                                  // [kPermWarps][E], then positions
-    int* cnt = perm_smem + kPermWarps * E;                  // [E]
-    int* item_base = cnt + E;                               // [E]
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int64_t seg = (n + kPermWarps - 1) / kPermWarps;
-    const int64_t s0 = n < (int64_t)w * seg ? n : (int64_t)w * seg;
-    const int64_t s1 = n < s0 + seg ? n : s0 + seg;
-    for (int k = tid; k < kPermWarps * E; k += kPermThreads) wcnt[k] = 0;
-    __syncthreads();
-    int* my = wcnt + w * E;
-    for (int64_t c0 = s0; c0 < s1; c0 += 32) {
-        const int64_t i = c0 + lane;
-        const int e = i < s1 ? idx[i] : -1;
-        const uint32_t mask = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && __popc(mask & ((1u << lane) - 1u)) == 0) my[e] += __popc(mask);
-        __syncwarp();
+// Offsets and work items from the per-expert counts cnt[0..E) in shared
+// memory, by one warp: lane l scans the experts [l * per, (l + 1) * per).
+// Writes offsets[0..E], off_s[e] = offsets[e], the items (expert, first
+// permuted row, rows <= tok) when `items` is not null, and their count.
+__device__ void expert_tables(const int32_t* cnt, int E, int tok, int32_t* __restrict__ offsets, int32_t* off_s,
+                              int4* __restrict__ items, int32_t* __restrict__ n_items, int lane) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int rows = 0, its = 0;
+    for (int e = e0; e < e1; ++e) {
+        rows += cnt[e];
+        its += (cnt[e] + tok - 1) / tok;
     }
-    __syncthreads();
-    // per expert: total, then each warp's first position (exclusive scan over warps)
-    for (int e = tid; e < E; e += kPermThreads) {
-        int run = 0;
-        for (int ww = 0; ww < kPermWarps; ++ww) {
-            const int c = wcnt[ww * E + e];
-            wcnt[ww * E + e] = run;
-            run += c;
-        }
-        cnt[e] = run;
+    int rows_incl = rows, its_incl = its;
+    #pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
+        const int k = __shfl_up_sync(0xffffffffu, its_incl, off);
+        if (lane >= off) { rows_incl += r; its_incl += k; }
     }
-    __syncthreads();
-    if (w == 0) {
-        // exclusive scans over experts of the row counts and the work items:
-        // lane l takes the consecutive experts [l * per, (l + 1) * per)
-        const int per = (E + 31) / 32;
-        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-        int rows = 0, its = 0;
-        for (int e = e0; e < e1; ++e) {
-            rows += cnt[e];
-            its += (cnt[e] + tok - 1) / tok;
-        }
-        int rows_incl = rows, its_incl = its;
-        #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
-            const int m = __shfl_up_sync(0xffffffffu, its_incl, off);
-            if (lane >= off) { rows_incl += r; its_incl += m; }
-        }
-        int run = rows_incl - rows, items_run = its_incl - its;
-        for (int e = e0; e < e1; ++e) {
-            const int c = cnt[e];
-            offsets[e] = run;
-            item_base[e] = items_run;
-            cnt[e] = run;                                    // now the expert's offset
-            run += c;
-            items_run += (c + tok - 1) / tok;
-        }
-        if (lane == 31) {
-            offsets[E] = rows_incl;
-            if (n_items != nullptr) *n_items = its_incl;
-        }
+    int run = rows_incl - rows, item = its_incl - its;
+    for (int e = e0; e < e1; ++e) {
+        const int c = cnt[e];
+        offsets[e] = run;
+        off_s[e] = run;
+        if (items != nullptr)
+            for (int r = 0; r < c; r += tok) items[item++] = make_int4(e, run + r, min(tok, c - r), 0);
+        run += c;
     }
-    __syncthreads();
-    if (items != nullptr) {                                  // null: routing tables only
-        for (int e = tid; e < E; e += kPermThreads) {
-            const int off = cnt[e], c = offsets[e + 1] - off;
-            for (int r = 0, k = 0; r < c; r += tok, ++k)
-                items[item_base[e] + k] = make_int4(e, off + r, min(tok, c - r), 0);
-        }
-    }
-    for (int64_t c0 = s0; c0 < s1; c0 += 32) {
-        const int64_t i = c0 + lane;
-        const int e = i < s1 ? idx[i] : -1;
-        const uint32_t mask = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(mask & ((1u << lane) - 1u));
-        if (e >= 0) {
-            const int pos = cnt[e] + my[e] + rank;
-            perm[pos] = (int32_t)i;
-            inv[i] = pos;
-        }
-        __syncwarp();
-        if (e >= 0 && rank == 0) my[e] += __popc(mask);
-        __syncwarp();
+    if (lane == 31) {
+        offsets[E] = rows_incl;
+        if (n_items != nullptr) *n_items = its_incl;
     }
 }
 
+// Many tokens: one CTA.  The counts come from shared-memory atomics.  The
+// stable order (by expert, then token -- a token's k slots hold distinct
+// experts) comes from per-expert token bitmasks, one chunk of tokens at a
+// time: for each expert the running number of its slots in earlier 32-token
+// words (pre), so that token t's slot of expert e lands at offsets[e] +
+// pre[e][t / 32] + (set bits of its word below t).  A thread holds up to
+// kPermSlots of a chunk's slots in registers, read with independent loads (a
+// single-CTA loop that waited on each load in turn spent its time in memory
+// latency).
+constexpr int kPermSlots = 16;
+
 __global__ void __launch_bounds__(kPermThreads)
-permute_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int tok,
+permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E, int tok, int wc,
                int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                int4* __restrict__ items, int32_t* __restrict__ n_items) {
-    extern __shared__ int perm_smem[];
+    extern __shared__ uint32_t psm[];
+    // rows of ws >= wc words, ws odd: the experts of one token's slots, which
+    // touch the same word column, fall on different banks
+    const int ws = wc | 1;
+    uint32_t* mask = psm;                                            // [E][ws]
+    int32_t* pre = reinterpret_cast<int32_t*>(mask + (size_t)E * ws);  // [E][ws]
+    int32_t* cnt = pre + (size_t)E * ws;                             // [E]: counts, then the running base
+    int32_t* off_s = cnt + E;                                        // [E]
+    const int tid = threadIdx.x;
     pdl_wait_previous();
     pdl_launch_dependents();
-    permute_block(idx, n, E, tok, offsets, perm, inv, items, n_items, perm_smem);
+    const int64_t n = T * topk;
+    constexpr int64_t kBatch = (int64_t)kPermSlots * kPermThreads;
+    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int64_t b0 = 0; b0 < n; b0 += kBatch) {
+        int ev[kPermSlots];
+        #pragma unroll
+        for (int u = 0; u < kPermSlots; ++u) {
+            const int64_t i = b0 + (int64_t)u * kPermThreads + tid;
+            ev[u] = i < n ? idx[i] : -1;
+        }
+        #pragma unroll
+        for (int u = 0; u < kPermSlots; ++u)
+            if (ev[u] >= 0) atomicAdd(&cnt[ev[u]], 1);
+    }
+    __syncthreads();
+    if (tid < 32) expert_tables(cnt, E, tok, offsets, off_s, items, n_items, tid);
+    __syncthreads();
+    for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
+    // a chunk: at most wc words of tokens and at most kBatch slots
+    const int64_t ct = min((int64_t)wc * 32, kBatch / topk);
+    // (the host sizes wc so that both bounds agree for the usual top-k)
+    for (int64_t t0 = 0; t0 < T; t0 += ct) {
+        for (int k = tid; k < E * ws; k += kPermThreads) mask[k] = 0u;
+        const int64_t i0 = t0 * topk, i1 = min(T, t0 + ct) * topk;
+        int ev[kPermSlots];
+        #pragma unroll
+        for (int u = 0; u < kPermSlots; ++u) {
+            const int64_t i = i0 + (int64_t)u * kPermThreads + tid;
+            ev[u] = i < i1 ? idx[i] : -1;
+        }
+        __syncthreads();
+        #pragma unroll
+        for (int u = 0; u < kPermSlots; ++u)
+            if (ev[u] >= 0) {
+                const int t = (int)(i0 + (int64_t)u * kPermThreads + tid) / topk - (int)t0;   // slots < 2^31
+                atomicOr(&mask[ev[u] * ws + (t >> 5)], 1u << (t & 31));
+            }
+        __syncthreads();
+        for (int e = tid; e < E; e += kPermThreads) {
+            int run = cnt[e];
+            for (int w = 0; w < wc; ++w) {
+                pre[e * ws + w] = run;
+                run += __popc(mask[e * ws + w]);
+            }
+            cnt[e] = run;
+        }
+        __syncthreads();
+        #pragma unroll
+        for (int u = 0; u < kPermSlots; ++u)
+            if (ev[u] >= 0) {
+                const int64_t i = i0 + (int64_t)u * kPermThreads + tid;
+                const int t = (int)i / topk - (int)t0, e = ev[u];
+                const int pos = off_s[e] + pre[e * ws + (t >> 5)] +
+                                __popc(mask[e * ws + (t >> 5)] & ((1u << (t & 31)) - 1u));
+                perm[pos] = (int32_t)i;
+                inv[i] = pos;
+            }
+        __syncthreads();
+    }
 }
 
 // Few tokens (T <= 64): one CTA routes every token (a warp per token) and
@@ -236,6 +261,7 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                      int4* __restrict__ items, int32_t* __restrict__ n_items) {
     __shared__ uint32_t tok_mask[2 * kMaxExperts];      // bit t: token t chose the expert
+    __shared__ int32_t cnt_s[kMaxExperts];
     __shared__ int32_t off_s[kMaxExperts];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     pdl_wait_previous();
@@ -245,35 +271,9 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
     for (int64_t t = w; t < T; t += kPermWarps) route_token(logits, t, E, topk, idx, wts, lane, tok_mask);
     __syncthreads();
     if (w == 0) {
-        // counts, offsets and work items: lane l scans the experts [l * per, (l + 1) * per)
-        const int per = (E + 31) / 32;
-        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-        int rows = 0, its = 0;
-        for (int e = e0; e < e1; ++e) {
-            const int c = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
-            rows += c;
-            its += (c + tok - 1) / tok;
-        }
-        int rows_incl = rows, its_incl = its;
-        #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
-            const int k = __shfl_up_sync(0xffffffffu, its_incl, off);
-            if (lane >= off) { rows_incl += r; its_incl += k; }
-        }
-        int run = rows_incl - rows, item = its_incl - its;
-        for (int e = e0; e < e1; ++e) {
-            const int c = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
-            offsets[e] = run;
-            off_s[e] = run;
-            if (items != nullptr)
-                for (int r = 0; r < c; r += tok) items[item++] = make_int4(e, run + r, min(tok, c - r), 0);
-            run += c;
-        }
-        if (lane == 31) {
-            offsets[E] = rows_incl;
-            if (n_items != nullptr) *n_items = its_incl;
-        }
+        for (int e = lane; e < E; e += 32) cnt_s[e] = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
+        __syncwarp();
+        expert_tables(cnt_s, E, tok, offsets, off_s, items, n_items, lane);
     }
     __syncthreads();
     // slot i = t * topk + j of expert e: after the earlier tokens of e
@@ -289,7 +289,15 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
     }
 }
 
-size_t permute_smem_bytes(int E) { return ((size_t)kPermWarps * E + 2 * E) * sizeof(int); }
+// Token words per permutation chunk: a chunk holds at most kPermSlots slots
+// per thread, and its masks and prefixes take about E * wc * 8 bytes of at
+// most 160 KB of shared memory.
+int permute_words(int64_t T, int E, int topk) {
+    const int64_t cap = std::max<int64_t>(1, (160 * 1024) / (8LL * E));
+    const int64_t by_slots = std::max<int64_t>(1, (int64_t)kPermSlots * kPermThreads / topk / 32);
+    return (int)std::min<int64_t>(std::min<int64_t>(ceil_div(T, 32), cap), by_slots);
+}
+size_t permute_smem_bytes(int E, int wc) { return ((size_t)2 * E * (wc | 1) + 2 * E) * sizeof(int); }
 
 // ------------------------------------------------- grouped streaming linear --
 constexpr int kWarps = 8;                      // 8 x 16 = 128 weight rows per CTA
@@ -1172,7 +1180,8 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
                             float* wts, int32_t* offsets, int32_t* perm, int32_t* inv, int4* items,
                             int32_t* n_items, cudaStream_t s) {
     nvfp4_status st;
-    const size_t psmem = permute_smem_bytes(E);
+    const int wc = permute_words(T, E, topk);
+    const size_t psmem = permute_smem_bytes(E, wc);
     if (T <= kFusedRouteMaxT)
         return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), 0, s, "MoE route+permute: launch",
                               router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items);
@@ -1182,7 +1191,7 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
     cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
     return launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
-                          (const int32_t*)idx, T * topk, E, tok, offsets, perm, inv, items, n_items);
+                          (const int32_t*)idx, T, topk, E, tok, wc, offsets, perm, inv, items, n_items);
 }
 
 // Work items expected in flight, for the split-K and persistent choices of the
