@@ -196,8 +196,12 @@ def test_gemm_plan_on_host(lib):
         # (M, N, K): tensor-memory-A tiles, shared-memory tiles, and a K split with its reduction pass
         assert nv.gemm_plan(2048, 5120, 13824) == {"kernel": "tile_tmem", "tokens": 192, "splits": 1, "launches": 1}
         assert nv.gemm_plan(2048, 13824, 5120) == {"kernel": "tile_smem", "tokens": 256, "splits": 1, "launches": 1}
+        # the tile kernels take the AWQ-scaled activations from one pass before
+        # them (its buffer in the workspace); the K split adds its reduction pass
         p = nv.gemm_plan(512, 5120, 13824, has_pre_quant_scale=True)
         assert p["kernel"] == "tile_smem" and p["splits"] > 1 and p["launches"] == 3
+        assert nv.gemm_workspace_size(512, 5120, 13824, True) == \
+            nv.gemm_workspace_size(512, 5120, 13824, False) + 512 * 13824 * 2
 
     out = [ctypes.c_int(0) for _ in range(4)]
     refs = [ctypes.byref(o) for o in out]

@@ -269,6 +269,33 @@ def test_gemm_tile_kernels_sampled(M, K, N):
     assert np.all(np.isfinite(formats.bf16_to_float(yb)))
 
 
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+@pytest.mark.parametrize("M,K,N", [(100, 1024, 20480), (300, 1040, 20480), (1000, 1024, 20480), (520, 4096, 2560)])
+def test_gemm_tile_kernels_awq(M, K, N, act):
+    """The AWQ pre-quant scale on both tile kernels (x' = RN(x * s) by one pass
+    before them): the tensor-memory-A kernel with 128- and 192-token tiles (K
+    tail at K=1040), the shared-memory-operand kernel (M=1000) and a 5-way K
+    split; BF16 and FP16; dropping the scale must fail the bar."""
+    r = synth.rng(synth.seed_for(7, M + K + N) + (act == "f16"))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(7, M * 3 + K * 7 + N))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = np.unique(np.concatenate([_sampled_rows(N, r, n=32), np.arange(0, N, 64), [N - 1]]))
+    x_bits = synth.normal_act(r, (M, K), act)
+    pqs = synth.awq_scale_bits(r, K, act)
+    plan = nv.gemm_plan(M, N, K, has_pre_quant_scale=True)
+    assert plan["kernel"] in ("tile_smem", "tile_tmem")
+    assert plan["launches"] == (3 if plan["splits"] > 1 else 2)
+    x = gu.bits_to_tensor(x_bits, act)
+    y = nv.gemm(x, w, pre_quant_scale=gu.bits_to_tensor(pqs, act))
+    gu.check_device_status()
+    yb = gu.tensor_to_bits(y)
+    _, ref = dense.linear(x_bits, packed, scales, d, True, pqs_bits=pqs, rows=rows, act=act)
+    gu.compare(yb[:, rows], ref, f"tile AWQ M={M} K={K} N={N} {act}", act=act)
+    plain = gu.tensor_to_bits(nv.gemm(x, w))
+    with pytest.raises(AssertionError):
+        gu.compare(plain[:, rows], ref, "tile dropped AWQ", act=act)
+
+
 def test_lm_head_full_size_sampled():
     K, N = 4096, 151936
     r = synth.rng(synth.seed_for(4, 0))

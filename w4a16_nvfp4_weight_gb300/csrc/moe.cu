@@ -1517,6 +1517,8 @@ nvfp4_status mlp_impl(const void* X, const void* fc1, const void* fc2, const voi
     const bool fc1_tile = mlp_fc1_tile(T, I);
     if (fc1_pre_quant_scale && fc1_tile) {
         // the tile FC1 reads X through TMA: scale it into the workspace first
+        // (scaling the tiles in the kernel measured slower: it doubles the
+        // shared-memory traffic of a kernel bound by its shared-memory pipe)
         st = launch_awq_scale((const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale, (uint16_t*)(ws + L.xs), T, H,
                               f16, s);
         if (st != NVFP4_OK) return st;
