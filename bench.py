@@ -525,7 +525,7 @@ def run_moe(args, rank, world, device, nv, synth):
         "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(value / pk["hbm"], 4), "traffic": None, "peak_source": pk["source"],
                      "kernel": "nvfp4::tc_gemm_kernel (MoE FC1 tile mode at T=4096, the largest share of a "
-                               "step); T <= 256 run nvfp4::moe_linear_kernel",
+                               "step); T=16 and 256 run nvfp4::moe_persist_kernel, T=1 nvfp4::moe_linear_kernel",
                      "per_call": per},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
