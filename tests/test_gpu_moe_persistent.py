@@ -132,3 +132,27 @@ def test_persistent_deterministic():
     a, _ = _run(c, fc1_dev, fc2_dev)
     b, _ = _run(c, fc1_dev, fc2_dev)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("T,E,topk,H,I,path", [(1, 8, 2, 128, 256, "stream_split"),
+                                               (64, 64, 8, 128, 1024, "stream_persistent"),
+                                               (300, 8, 2, 256, 256, "tile")])
+def test_corrupt_expert_header_is_reported_not_trapped(T, E, topk, H, I, path):
+    """An expert whose repacked header does not match (its magic overwritten)
+    on each MoE path: the kernels skip that expert's work, record status 7 in
+    the device status word and finish; the next call with intact weights
+    matches the oracle again."""
+    assert nv.moe_plan(T, E, topk, H, I)["path"] == path
+    c, fc1, fc2 = _case(T, E, topk, H, I, seed=61 + T)
+    fc1_dev, fc2_dev = _stack(fc1, 2 * I, H), _stack(fc2, H, I)
+    size = nv.repack_size(2 * I, H)
+    routed = int(np.argmax(np.bincount(omoe.route(c.logits, topk)[0].ravel(), minlength=E)))
+    saved = fc1_dev[routed * size:routed * size + 4].clone()
+    fc1_dev[routed * size:routed * size + 4] = 0
+    x = gu.bits_to_tensor(c.x_bits, "bf16")
+    logits = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
+    nv.moe_grouped(x, logits, fc1_dev, fc2_dev, topk, I)
+    assert nv.device_status(clear=True) == 7
+    fc1_dev[routed * size:routed * size + 4] = saved
+    out, _ = _run(c, fc1_dev, fc2_dev)
+    gu.compare(out, _oracle_plain(c, fc1, fc2)["out_bits"], f"after a corrupt header ({path})")
