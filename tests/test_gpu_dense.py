@@ -296,6 +296,27 @@ def test_gemm_tile_kernels_awq(M, K, N, act):
         gu.compare(plain[:, rows], ref, "tile dropped AWQ", act=act)
 
 
+@pytest.mark.parametrize("M,K,N", [(64, 4096, 4096), (128, 14336, 4096), (256, 4096, 8192), (32, 4096, 4096)])
+def test_gemm_mid_m_path_choice(M, K, N):
+    """Between 17 and 511 tokens the path comes from a cost model (the
+    streaming kernel expands the weights once per 16 tokens; the tile kernels
+    once per tile, with a K split when the tiles alone leave SMs idle): these
+    take the tile kernels with a K split, except M=32, which streams.  Sampled
+    output rows against the oracle."""
+    plan = nv.gemm_plan(M, N, K)
+    assert plan["kernel"] == ("decode" if M == 32 else "tile_tmem" if M < 256 else plan["kernel"])
+    r = synth.rng(synth.seed_for(8, M + K + N))
+    packed, scales, d = synth.weight_only(K, N, synth.seed_for(8, M * 3 + K * 7 + N))
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    rows = _sampled_rows(N, r, n=32)
+    x_bits = synth.normal_bf16(r, (M, K))
+    y = nv.gemm(gu.bits_to_bf16_tensor(x_bits), w)
+    gu.check_device_status()
+    yb = gu.tensor_to_bits(y)
+    _, ref = dense.linear(x_bits, packed, scales, d, True, rows=rows)
+    gu.compare(yb[:, rows], ref, f"mid M={M} K={K} N={N} ({plan['kernel']})")
+
+
 def test_lm_head_full_size_sampled():
     K, N = 4096, 151936
     r = synth.rng(synth.seed_for(4, 0))

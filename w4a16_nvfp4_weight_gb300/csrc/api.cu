@@ -151,7 +151,7 @@ extern "C" nvfp4_status nvfp4_device_status(int* code_out, int clear, void* stre
 
 extern "C" size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_quant_scale) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kGroup != 0) return 0;
-    if (use_tc_path(M, N)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
+    if (use_tc_path(M, N, K)) return tc_workspace_bytes(M, N, K, has_pre_quant_scale != 0);
     return 0;               // the decode kernel applies AWQ to its activation fragments
 }
 
@@ -174,7 +174,7 @@ nvfp4_status nvfp4::run_dense_gemm(const void* X, const void* repacked, const vo
     int* status = device_status_ptr();
     if (!status) return fail(NVFP4_ERR_CUDA, "%s: no CUDA device", fn);
     cudaStream_t s = (cudaStream_t)stream;
-    if (use_tc_path(M, N)) {
+    if (use_tc_path(M, N, K)) {
         TcParams tp{};
         tp.X = (const uint16_t*)X; tp.pqs = (const uint16_t*)pre_quant_scale;
         tp.rp = (const uint8_t*)repacked; tp.Y = (uint16_t*)Y;
@@ -213,7 +213,7 @@ extern "C" nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, i
         *kernel_out = -1; *tokens_out = 0; *splits_out = 0; *launches_out = 0;
         return NVFP4_OK;
     }
-    if (use_tc_path(M, N)) {
+    if (use_tc_path(M, N, K)) {
         bool wa = false;
         int tok = 0, sp = 1;
         tc_plan_info(M, N, K, &wa, &tok, &sp);

@@ -743,7 +743,7 @@ struct TcPlan {
     int splits, kbs;
 };
 
-TcPlan plan_tc(int64_t M, int64_t N, int64_t K) {
+TcPlan plan_tc(int64_t M, int64_t N, int64_t K, double* predicted_us = nullptr) {
     const int64_t KB = round_up(K, kBlockK) / kBlockK;
     const int64_t sms = sm_count();
     auto split_plan = [&](TcPlan pl, double t_blk, double* cost_out) {
@@ -773,6 +773,7 @@ TcPlan plan_tc(int64_t M, int64_t N, int64_t K) {
     const TcPlan sm = split_plan(TcPlan{false, 128 * sub, 1, 1}, sub == 1 ? 0.74 : 0.82, &t_sm);
     const int nt = ceil_div(M, 192) < ceil_div(M, 128) ? 192 : 128;
     const TcPlan wa = split_plan(TcPlan{true, nt, 1, 1}, 0.64, &t_wa);
+    if (predicted_us) *predicted_us = t_wa < t_sm ? t_wa : t_sm;
     return t_wa < t_sm ? wa : sm;
 }
 
@@ -785,10 +786,26 @@ void tc_plan_info(int64_t M, int64_t N, int64_t K, bool* wa, int* tokens, int* s
     *splits = pl.splits;
 }
 
-bool use_tc_path(int64_t M, int64_t N) {
+// Streaming kernel or tile kernels for M > 16: whichever a cost model predicts
+// faster.  The streaming kernel expands every weight once per 16 tokens (its
+// token chunks run as separate CTAs): about 4 us plus one 16-token pass over
+// the weights at 4.8 T weights/s on GB300 (M = 32..300, N = 1000..14336,
+// K = 720..14336, within 15 %); the tile kernels' time is their plan's
+// (wave-quantized blocks plus the K split's reduction pass).  From M = 512 the
+// tiles always win.
+bool tc_tiles_fill(int64_t M, int64_t N) {
     if (M <= 16) return false;
     const int64_t tiles = ceil_div(N, kBN) * (M <= 128 ? ceil_div(M, 128) : ceil_div(M, 256));
     return tiles >= sm_count() / 2 || M >= 512;
+}
+
+bool use_tc_path(int64_t M, int64_t N, int64_t K) {
+    if (M <= 16) return false;
+    if (M >= 512) return true;
+    double t_tile = 0.0;
+    plan_tc(M, N, K, &t_tile);
+    const double t_stream = 4.0 + (double)ceil_div(M, 16) * (double)N * (double)K / 4.8e6;
+    return t_tile < t_stream;
 }
 
 size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K, bool has_pqs) {

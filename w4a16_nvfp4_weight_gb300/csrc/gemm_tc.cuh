@@ -41,9 +41,12 @@ struct TcMoeParams {
 };
 nvfp4_status launch_tc_moe(const TcMoeParams& p, cudaStream_t stream);
 
-// Shape rule between the streaming (decode) kernel and the tile kernels: tiles
-// for M > 16 unless the tile grid would leave most SMs idle at M < 512.
-bool use_tc_path(int64_t M, int64_t N);
+// Shape rule between the streaming (decode) kernel and the tile kernels for
+// M > 16: the one a cost model predicts faster (always tiles from M = 512).
+bool use_tc_path(int64_t M, int64_t N, int64_t K);
+// Whether the tile grid alone (no K split) fills at least half of the SMs, or
+// M >= 512: the rule of the callers whose tile modes do not split K.
+bool tc_tiles_fill(int64_t M, int64_t N);
 // The dense tile plan of an M x N x K GEMM: the tensor-memory-A kernel (wa) or
 // the shared-memory-operand one, its tokens per tile and its K splits.
 void tc_plan_info(int64_t M, int64_t N, int64_t K, bool* wa, int* tokens, int* splits);

@@ -1486,7 +1486,7 @@ MlpLayout mlp_layout(int64_t T, int64_t H, int64_t I) {
 
 // FC1 on the tile kernel when the dense shape rule picks tiles for [T, 2I]
 // and the gate/up halves are whole 128-row tiles; else the streaming kernel.
-bool mlp_fc1_tile(int64_t T, int64_t I) { return I % 128 == 0 && use_tc_path(T, 2 * I); }
+bool mlp_fc1_tile(int64_t T, int64_t I) { return I % 128 == 0 && tc_tiles_fill(T, 2 * I); }
 
 nvfp4_status mlp_impl(const void* X, const void* fc1, const void* fc2, const void* fc1_pre_quant_scale, int64_t T,
                       int64_t H, int64_t I, void* out, void* workspace, size_t workspace_bytes, bool f16,
