@@ -331,7 +331,11 @@ nvfp4_status nvfp4_w4a16_moe_grouped_ex(const void* X, const float* router_logit
  *                     (work item, column group) with K split across a thread-
  *                     block cluster; 2 streaming kernels, one persistent wave
  *                     that walks the (work item, column group) units with K
- *                     whole; 3 gathered rows on the tcgen05 tile kernels.
+ *                     whole; 3 gathered rows on the tcgen05 tile kernels;
+ *                     4 one token with topk <= 8: two kernels in all (every
+ *                     CTA routes the token itself; FC2 sums the slots'
+ *                     weighted outputs inside a cluster, so no routing or
+ *                     combine kernel runs).
  *  rows_per_item_out  routed rows per work item (8 or 16 streaming, 128 or
  *                     256 on the tile kernels; 0 when T == 0).
  * The choice depends on the routed rows per expert on average (T * topk / E)

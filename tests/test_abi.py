@@ -219,7 +219,9 @@ def test_moe_plan_on_host(lib):
 
     E, k, H, I = 128, 8, 2048, 768
     assert nv.moe_plan(0, E, k, H, I) == {"path": "none", "rows_per_item": 0}
-    assert nv.moe_plan(1, E, k, H, I) == {"path": "stream_split", "rows_per_item": 8}
+    assert nv.moe_plan(1, E, k, H, I) == {"path": "single_token", "rows_per_item": 8}
+    assert nv.moe_plan(2, E, k, H, I) == {"path": "stream_split", "rows_per_item": 8}
+    assert nv.moe_plan(1, 32, 16, H, I)["path"] == "stream_split"      # top-16: beyond one portable cluster
     assert nv.moe_plan(16, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 8}
     assert nv.moe_plan(256, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 32}
     assert nv.moe_plan(160, E, k, H, I) == {"path": "stream_persistent", "rows_per_item": 16}
@@ -230,6 +232,7 @@ def test_moe_plan_on_host(lib):
     path, rows = ctypes.c_int(0), ctypes.c_int(0)
     refs = [ctypes.byref(path), ctypes.byref(rows)]
     assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 64, 64, 0, *refs) == 0 and path.value == 1
+    assert lib.nvfp4_w4a16_moe_plan(1, 8, 2, 64, 64, 0, *refs) == 0 and path.value == 4
     assert lib.nvfp4_w4a16_moe_plan(-1, 8, 2, 64, 64, 0, *refs) == 1
     assert lib.nvfp4_w4a16_moe_plan(4, 8, 2, 64, 64, 3, *refs) == 1
     assert lib.nvfp4_w4a16_moe_plan(4, 0, 2, 64, 64, 0, *refs) == 2

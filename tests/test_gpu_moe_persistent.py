@@ -134,7 +134,7 @@ def test_persistent_deterministic():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("T,E,topk,H,I,path", [(1, 8, 2, 128, 256, "stream_split"),
+@pytest.mark.parametrize("T,E,topk,H,I,path", [(1, 8, 2, 128, 256, "single_token"), (3, 8, 2, 128, 256, "stream_split"),
                                                (64, 64, 8, 128, 1024, "stream_persistent"),
                                                (300, 8, 2, 256, 256, "tile")])
 def test_corrupt_expert_header_is_reported_not_trapped(T, E, topk, H, I, path):
@@ -156,3 +156,46 @@ def test_corrupt_expert_header_is_reported_not_trapped(T, E, topk, H, I, path):
     fc1_dev[routed * size:routed * size + 4] = saved
     out, _ = _run(c, fc1_dev, fc2_dev)
     gu.compare(out, _oracle_plain(c, fc1, fc2)["out_bits"], f"after a corrupt header ({path})")
+
+
+@pytest.mark.parametrize("E,topk,H,I,act,activation,awq", [(8, 2, 128, 256, "bf16", "swiglu", False),
+                                                           (64, 8, 256, 512, "bf16", "swiglu", True),
+                                                           (256, 8, 128, 128, "f16", "swiglu", True),
+                                                           (16, 1, 192, 320, "bf16", "relu2", False),
+                                                           (40, 5, 128, 192, "f16", "silu", False)])
+def test_single_token_layer(E, topk, H, I, act, activation, awq):
+    """One token (the moe_plan path "single_token"): two kernels, each routing
+    the token itself -- FC1 writes h_j per routing slot, FC2 sums p_j * y_j in
+    slot order inside a cluster of the slots.  Output against the oracle, the
+    routing outputs bit for bit, AWQ with its dropped-scale control, FP16,
+    non-gated experts, run-to-run bitwise equality."""
+    assert nv.moe_plan(1, E, topk, H, I, activation)["path"] == "single_token"
+    kind = "gated" if activation == "swiglu" else "plain"
+    c, fc1, fc2 = _case(1, E, topk, H, I, seed=E + topk + H, kind=kind, act=act, awq=awq)
+    fc1_dev = _stack(fc1, 2 * I if kind == "gated" else I, H)
+    fc2_dev = _stack(fc2, H, I)
+    out, routing = _run(c, fc1_dev, fc2_dev, act=act, activation=activation, awq=awq)
+    ref = _oracle_plain(c, fc1, fc2, act=act, activation=activation, awq=awq)
+    assert np.array_equal(routing["idx"].reshape(1, topk), ref["idx"])
+    assert np.array_equal(routing["perm"], ref["perm"])
+    assert np.array_equal(routing["offsets"], ref["offsets"])
+    assert np.allclose(routing["p"].reshape(1, topk), ref["p"], rtol=2e-6, atol=1e-7)
+    gu.compare(out, ref["out_bits"], f"single token E={E} k={topk} {act} {activation}", act=act)
+    again, _ = _run(c, fc1_dev, fc2_dev, act=act, activation=activation, awq=awq)
+    assert np.array_equal(out, again)
+    if awq:
+        plain, _ = _run(c, fc1_dev, fc2_dev, act=act, activation=activation, awq=False)
+        with pytest.raises(AssertionError):
+            gu.compare(plain, ref["out_bits"], "single token dropped AWQ", act=act)
+
+
+def test_single_token_gate_up_shards():
+    E, topk, H, I = 16, 4, 128, 256
+    assert nv.moe_plan(1, E, topk, H, I)["path"] == "single_token"
+    c, fc1, fc2 = _case(1, E, topk, H, I, seed=71, kind="split")
+    shards = [w for pair in fc1 for w in pair]
+    out, _ = _run(c, _stack(shards, I, H), _stack(fc2, H, I), split=True)
+    ref = omoe.moe_layer(c.x_bits, c.logits,
+                         [((gp, gs, gd, True), (up, us, ud, True)) for (gp, gs, gd), (up, us, ud) in fc1],
+                         [(p, s, d, True) for p, s, d in fc2], topk, fc1_split=True)
+    gu.compare(out, ref["out_bits"], "single token shards")

@@ -184,12 +184,13 @@ def moe_workspace_size(T, E, topk, H, I):
 
 
 MOE_ACTIVATIONS = {"swiglu": 0, "relu2": 1, "silu": 2}
-MOE_PATHS = {0: "none", 1: "stream_split", 2: "stream_persistent", 3: "tile"}
+MOE_PATHS = {0: "none", 1: "stream_split", 2: "stream_persistent", 3: "tile", 4: "single_token"}
 
 
 def moe_plan(T, E, topk, H, I, activation="swiglu"):
     """The kernels moe_grouped() would run on the current device: dict(path=
-    "stream_split" | "stream_persistent" | "tile" | "none", rows_per_item).
+    "single_token" | "stream_split" | "stream_persistent" | "tile" | "none",
+    rows_per_item).
     Host only."""
     if activation not in MOE_ACTIVATIONS:
         raise Nvfp4Error(1, f"activation must be one of {sorted(MOE_ACTIVATIONS)}")

@@ -333,6 +333,15 @@ struct MoeLinParams {
                                //   fragments (x' = RN(x * s)); null = none
     int early;                 // 1: the routing tables were written two launches back, so
                                //   they and the weights may be read before the wait
+    // single token (ONE kernels): every CTA routes the token from its logits
+    const float* logits;       // [E] FP32
+    int E;
+    uint16_t* out;             // FC2 + combine: the layer output [N]
+    int32_t* r_idx;            // FC1: the routing tables, written by CTA (0, 0, 0) when
+    float* r_wts;              //   not null -- top-k experts and weights [topk], the
+    int32_t* r_perm;           //   permutation and its inverse [topk], the expert
+    int32_t* r_inv;            //   offsets [E + 1]
+    int32_t* r_offsets;
     int* status;
 };
 
@@ -347,9 +356,18 @@ __device__ __forceinline__ float plain_act(float v, int act) {
     return silu_f(v);
 }
 
-template <int MT, bool GATED, bool F16, bool AWQ>
+// ONE = 1: FC1 of a single token, ONE = 2: its FC2 with the combine.  The
+// token's routing is computed by every CTA from the logits (the same top-k
+// everywhere), so no routing kernel runs: grid z is the routing slot j, whose
+// expert is the j-th selection.  FC1 writes h_j to row j of H.  FC2 gives each
+// CTA the whole K of one slot and clusters the topk slots of a row group: the
+// push reduction then sums p_j * y_j over the slots in slot order and writes
+// the output row, so no combine kernel runs either.
+template <int MT, bool GATED, bool F16, bool AWQ, int ONE = 0>
 __global__ void __launch_bounds__(kThreads)
 moe_linear_kernel(const MoeLinParams p) {
+    __shared__ int32_t one_e[kMaxTopk];        // single token: its experts and weights
+    __shared__ float one_p[kMaxTopk];
     extern __shared__ __align__(128) uint8_t smem[];
     using G = typename MoeRing<MT>::G;
     constexpr int TOK = G::kTok;
@@ -373,17 +391,42 @@ moe_linear_kernel(const MoeLinParams p) {
     const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
     const int split = blockIdx.y;
     const int item_id = blockIdx.z;
+    // the cluster's reduction ranks: the K splits, or (single-token FC2) the slots
+    const int rank = ONE == 2 ? item_id : split;
+    const int nranks = ONE == 2 ? p.topk : p.splits;
     // Items and activations come from earlier kernels.  Dependents are released
     // only after the wait: an FC2 reads the routing tables before its own wait
     // (`early`), which is safe once the kernel that wrote them, two launches
     // back, is known to be complete -- as it is when its successor has waited.
-    const bool early = p.early != 0 && p.items != nullptr;
+    const bool early = (p.early != 0 && p.items != nullptr) || ONE == 2;
     if (!early) {
         pdl_wait_previous();
         pdl_launch_dependents();
     }
     int4 item;                                 // the same for every CTA of the cluster
-    if (p.items != nullptr) {
+    if constexpr (ONE != 0) {
+        // FC1 has waited for the logits' producer; FC2 starts only after FC1
+        // has waited too, so it may route before its own wait
+        if (warp == 0) route_token(p.logits, 0, p.E, p.topk, one_e, one_p, lane);
+        __syncthreads();
+        if (ONE == 1 && warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && p.r_idx != nullptr) {
+            // the layer's routing outputs: slots sorted by expert (distinct)
+            if (lane < p.topk) {
+                int pos = 0;
+                for (int j = 0; j < p.topk; ++j) pos += one_e[j] < one_e[lane];
+                p.r_idx[lane] = one_e[lane];
+                p.r_wts[lane] = one_p[lane];
+                p.r_perm[pos] = lane;
+                p.r_inv[lane] = pos;
+            }
+            for (int ex = lane; ex <= p.E; ex += 32) {
+                int c = 0;
+                for (int j = 0; j < p.topk; ++j) c += one_e[j] < ex;
+                p.r_offsets[ex] = c;
+            }
+        }
+        item = make_int4(one_e[item_id], item_id, 1, 0);
+    } else if (p.items != nullptr) {
         if (item_id >= (early ? __ldcg(p.n_items) : *p.n_items)) return;
         item = early ? __ldcg(p.items + item_id) : p.items[item_id];
     } else {
@@ -455,7 +498,8 @@ moe_linear_kernel(const MoeLinParams p) {
                 const uint16_t* xrow[TOK];
                 for (int t = 0; t < nrows; ++t) {
                     const int64_t r = r0 + t;
-                    const int64_t src_row = token_rows ? (int64_t)((early ? __ldcg(p.perm + r) : p.perm[r]) / p.topk) : r;
+                    const int64_t src_row = ONE == 1 ? 0    // the single token; FC2: H row j = r
+                                            : token_rows ? (int64_t)((early ? __ldcg(p.perm + r) : p.perm[r]) / p.topk) : r;
                     xrow[t] = p.X + src_row * p.K;
                 }
                 auto stage_xk = [&](int i) {
@@ -571,11 +615,13 @@ moe_linear_kernel(const MoeLinParams p) {
         // stores counted on its red_bar (no cluster-wide barrier afterwards)
         const int c = lane & 3;
         const uint32_t part_s = smem_u32(part), bar_s = smem_u32(red_bar);
+        // single-token FC2: the partials are p_j * y_j of this CTA's slot j
+        const float scale = ONE == 2 ? one_p[item_id] : 1.0f;
         cluster_wait();
         if (GATED) {
             // pair (token t, column jj): gate partial from warps 0-3, up from warps 4-7
             const int total = nrows * 64;
-            const int share = (total + p.splits - 1) / p.splits;
+            const int share = (total + nranks - 1) / nranks;
             #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
                 #pragma unroll
@@ -586,13 +632,13 @@ moe_linear_kernel(const MoeLinParams p) {
                     const int ei = t * 64 + jj;
                     if (t < nrows) {
                         const uint32_t owner = (uint32_t)(ei / share);
-                        st_async_b32(map_rank(part_s + 4u * (uint32_t)((split * share + ei % share) * 2 + half), owner),
+                        st_async_b32(map_rank(part_s + 4u * (uint32_t)((rank * share + ei % share) * 2 + half), owner),
                                      __float_as_uint(acc[mt][v]), map_rank(bar_s, owner));
                     }
                 }
         } else {
             const int total = nrows * 128;
-            const int share = (total + p.splits - 1) / p.splits;
+            const int share = (total + nranks - 1) / nranks;
             #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
                 #pragma unroll
@@ -602,8 +648,8 @@ moe_linear_kernel(const MoeLinParams p) {
                     const int ei = t * 128 + row;
                     if (t < nrows) {
                         const uint32_t owner = (uint32_t)(ei / share);
-                        st_async_b32(map_rank(part_s + 4u * (uint32_t)(split * share + ei % share), owner),
-                                     __float_as_uint(acc[mt][v]), map_rank(bar_s, owner));
+                        st_async_b32(map_rank(part_s + 4u * (uint32_t)(rank * share + ei % share), owner),
+                                     __float_as_uint(scale * acc[mt][v]), map_rank(bar_s, owner));
                     }
                 }
         }
@@ -613,21 +659,21 @@ moe_linear_kernel(const MoeLinParams p) {
     // per output when gated), then reduce in rank order
     const int per_e = GATED ? 2 : 1;
     const int total_e = nrows * (GATED ? 64 : 128);
-    const int share_e = (total_e + p.splits - 1) / p.splits;
-    const int e0_own = split * share_e, e1_own = min(total_e, e0_own + share_e);
+    const int share_e = (total_e + nranks - 1) / nranks;
+    const int e0_own = rank * share_e, e1_own = min(total_e, e0_own + share_e);
     bool landed = true;
     if (e1_own > e0_own) {
-        if (tid == 0) mbar_arrive_expect_tx(red_bar, (uint32_t)((e1_own - e0_own) * p.splits * per_e * 4));
+        if (tid == 0) mbar_arrive_expect_tx(red_bar, (uint32_t)((e1_own - e0_own) * nranks * per_e * 4));
         landed = mbar_wait_cluster(red_bar, 0, p.status);
     }
     if (landed && *hdr_flag != 0) {
         if (GATED) {
             const int total = nrows * 64;
-            const int share = (total + p.splits - 1) / p.splits;
-            const int e0 = split * share, e1 = min(total, e0 + share);
+            const int share = (total + nranks - 1) / nranks;
+            const int e0 = rank * share, e1 = min(total, e0 + share);
             for (int ei = e0 + tid; ei < e1; ei += kThreads) {
                 float gsum = 0.0f, usum = 0.0f;
-                for (int r = 0; r < p.splits; ++r) {
+                for (int r = 0; r < nranks; ++r) {
                     gsum += part[(r * share + (ei - e0)) * 2 + 0];
                     usum += part[(r * share + (ei - e0)) * 2 + 1];
                 }
@@ -637,15 +683,17 @@ moe_linear_kernel(const MoeLinParams p) {
             }
         } else {
             const int total = nrows * 128;
-            const int share = (total + p.splits - 1) / p.splits;
-            const int e0 = split * share, e1 = min(total, e0 + share);
+            const int share = (total + nranks - 1) / nranks;
+            const int e0 = rank * share, e1 = min(total, e0 + share);
             for (int ei = e0 + tid; ei < e1; ei += kThreads) {
                 float sum = 0.0f;
-                for (int r = 0; r < p.splits; ++r) sum += part[r * share + (ei - e0)];
+                for (int r = 0; r < nranks; ++r) sum += part[r * share + (ei - e0)];
                 const int t = ei / 128, row = ei % 128;
                 const int64_t n = row_a + row;
                 if (t < nrows && n < p.N) {
-                    if (p.act != 0) {        // non-gated FC1: h = RN(act(v)) in permuted row order
+                    if (ONE == 2) {          // the layer output: sum over the slots of p_j * y_j
+                        p.out[n] = f32_to_act_bits<F16>(sum);
+                    } else if (p.act != 0) {        // non-gated FC1: h = RN(act(v)) in permuted row order
                         p.H[(int64_t)(r0 + t) * p.N + n] = f32_to_act_bits<F16>(plain_act(sum, p.act));
                     } else {
                         const int32_t slot = p.perm[r0 + t];
@@ -1115,6 +1163,34 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
                : launch_moe_linear_typed<MT, GATED, false, false>(p, gx, max_items, s);
 }
 
+// Single-token kernels: FC1 (ONE = 1; K split across a cluster of `splits`)
+// and FC2 with the combine (ONE = 2; one cluster per row group over the topk
+// slots), both with grid z = the routing slot.
+template <bool GATED, bool F16, bool AWQ, int ONE>
+nvfp4_status launch_moe_one_typed(const MoeLinParams& p, unsigned gx, cudaStream_t s) {
+    const size_t smem = moe_lin_smem(1, GATED, GATED && p.half_stride != 0);
+    cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<1, GATED, F16, AWQ, ONE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return check_cuda(e, "MoE single token: shared memory attribute");
+    const unsigned ys = ONE == 1 ? (unsigned)p.splits : 1u;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, ys, (unsigned)p.topk);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = ys;
+    attr[0].val.clusterDim.z = ONE == 2 ? (unsigned)p.topk : 1u;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, moe_linear_kernel<1, GATED, F16, AWQ, ONE>, p);
+    return check_cuda(e, ONE == 1 ? "MoE single-token FC1: launch" : "MoE single-token FC2: launch");
+}
+
 // The instances for 8, 16 or 32 routed rows per work item.
 template <bool GATED>
 nvfp4_status launch_moe_linear_mt(int mt, const MoeLinParams& p, unsigned gx, unsigned max_items, bool f16,
@@ -1204,6 +1280,9 @@ int64_t moe_est_items(const MoeLayout& L, int64_t n, int E) {
 // them without splitting K; fewer: a CTA per unit, K split across a cluster.
 bool moe_use_persist(int64_t fc1_groups, int64_t est_items) { return fc1_groups * est_items >= 4LL * sm_count(); }
 
+// One token whose top-k fits one portable cluster: the two single-token kernels.
+bool moe_single_token(int64_t T, int topk) { return T == 1 && topk <= 8; }
+
 int moe_splits(int64_t base_ctas, int64_t KB, int kbs_min) {
     int64_t splits = std::max<int64_t>(1, ceil_div(2LL * sm_count(), std::max<int64_t>(base_ctas, 1)));
     splits = std::min<int64_t>(splits, std::min<int64_t>(8, std::max<int64_t>(1, KB / kbs_min)));
@@ -1251,7 +1330,8 @@ extern "C" nvfp4_status nvfp4_w4a16_moe_plan(int64_t T, int E, int topk, int64_t
     }
     const MoeLayout L = moe_layout(T, E, topk, H, I);
     const int64_t fc1_groups = activation == NVFP4_MOE_SWIGLU ? I / 64 : ceil_div(I, 128);
-    *path_out = L.tile ? 3 : moe_use_persist(fc1_groups, moe_est_items(L, T * topk, E)) ? 2 : 1;
+    *path_out = moe_single_token(T, topk) ? 4
+              : L.tile ? 3 : moe_use_persist(fc1_groups, moe_est_items(L, T * topk, E)) ? 2 : 1;
     *rows_per_item_out = L.tok;
     return NVFP4_OK;
 }
@@ -1315,6 +1395,44 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
     const size_t fc1_stride = !gated ? shard_bytes : fc1_split ? 2 * shard_bytes : nvfp4_repack_size(2 * I, H);
     const size_t half_stride = fc1_split ? shard_bytes : 0;
     const int64_t fc1_rows = (gated && !fc1_split) ? 2 * I : I;          // rows of one repacked FC1 buffer
+
+    if (moe_single_token(T, topk)) {
+        // One token: two kernels.  Every CTA routes the token itself; FC1 writes
+        // h_j per slot, FC2 sums p_j * y_j over a cluster of the slots.
+        MoeLinParams p1{};
+        p1.w = (const uint8_t*)fc1; p1.w_stride = fc1_stride; p1.half_stride = half_stride;
+        p1.N = fc1_rows; p1.K = H; p1.KB = round_up(H, kBlockK) / kBlockK;
+        const int64_t fc1_groups = gated ? I / 64 : ceil_div(I, 128);
+        p1.splits = moe_splits(fc1_groups * topk, p1.KB, 4);
+        p1.kbs = (int)ceil_div(p1.KB, p1.splits);
+        p1.splits = (int)ceil_div(p1.KB, p1.kbs);
+        p1.X = (const uint16_t*)X; p1.topk = topk; p1.I = I; p1.H = hbuf; p1.status = status;
+        p1.pqs = (const uint16_t*)fc1_pre_quant_scale;
+        p1.act = gated ? 0 : activation;
+        p1.logits = router_logits; p1.E = E;
+        p1.r_idx = idx; p1.r_wts = wts; p1.r_perm = perm; p1.r_inv = inv; p1.r_offsets = offsets;
+        const bool awq = fc1_pre_quant_scale != nullptr;
+        if (gated)
+            st = f16 ? (awq ? launch_moe_one_typed<true, true, true, 1>(p1, (unsigned)fc1_groups, s)
+                            : launch_moe_one_typed<true, true, false, 1>(p1, (unsigned)fc1_groups, s))
+                     : (awq ? launch_moe_one_typed<true, false, true, 1>(p1, (unsigned)fc1_groups, s)
+                            : launch_moe_one_typed<true, false, false, 1>(p1, (unsigned)fc1_groups, s));
+        else
+            st = f16 ? (awq ? launch_moe_one_typed<false, true, true, 1>(p1, (unsigned)fc1_groups, s)
+                            : launch_moe_one_typed<false, true, false, 1>(p1, (unsigned)fc1_groups, s))
+                     : (awq ? launch_moe_one_typed<false, false, true, 1>(p1, (unsigned)fc1_groups, s)
+                            : launch_moe_one_typed<false, false, false, 1>(p1, (unsigned)fc1_groups, s));
+        if (st != NVFP4_OK) return st;
+        MoeLinParams p2{};
+        p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
+        p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
+        p2.splits = 1; p2.kbs = (int)p2.KB;
+        p2.X = hbuf; p2.topk = topk; p2.I = I; p2.status = status;
+        p2.logits = router_logits; p2.E = E; p2.out = (uint16_t*)out;
+        const unsigned fc2_groups = (unsigned)ceil_div(H, 128);
+        return f16 ? launch_moe_one_typed<false, true, false, 2>(p2, fc2_groups, s)
+                   : launch_moe_one_typed<false, false, false, 2>(p2, fc2_groups, s);
+    }
 
     // AWQ: the tile path scales the rows while gathering them, the streaming
     // path the activation fragments inside FC1; no separate pass either way
