@@ -181,11 +181,11 @@ def test_moe_full_size_sampled(full_experts, T):
 
 @pytest.mark.parametrize("T", [1, 16, 64, 65, 256, 4096])
 def test_moe_route_tables_bit_exact(T):
-    """The standalone routing call (the same kernels the layer runs first: the
-    fused single-CTA kernel up to 64 tokens, two kernels above) against the
-    oracle: top-k indices, the stable permutation, its inverse and the expert
-    offsets bit for bit, the routing weights to float32 rounding; and the layer
-    reports the same tables."""
+    """The standalone routing call (the fused single-CTA kernel up to 64
+    tokens; above, a routing kernel and a single-CTA permutation, since the
+    call has no workspace for the layer's chunked kernels) against the oracle:
+    top-k indices, the stable permutation, its inverse and the expert offsets
+    bit for bit, the routing weights to float32 rounding."""
     E, topk = 128, 8
     c = synth.moe_case(T, synth.seed_for(3, T) + 7, E=E, topk=topk, H=64, I=64, weights=None)
     logits = torch.from_numpy(np.ascontiguousarray(c.logits)).cuda()
@@ -229,6 +229,28 @@ def test_moe_route_tables_edge_shapes(T, E, topk):
     for k, v in (("idx", idx), ("perm", perm), ("inv", inv), ("offsets", offsets)):
         assert np.array_equal(got[k], v), k
     assert np.allclose(got["p"], p, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,E,topk", [(513, 256, 16), (530, 40, 5), (600, 3, 3), (803, 1, 1), (4097, 128, 8),
+                                       (65, 256, 16), (130, 40, 5)])
+def test_moe_layer_chunked_routing_tables(T, E, topk):
+    """From 513 tokens the layer routes and permutes in chunks of 8 tokens (a
+    CTA per chunk: routing + per-expert counts; a scan of each expert's counts
+    over the chunks; each chunk's positions after the earlier chunks'); from
+    65 to 512 a routing kernel and a single-CTA permutation: 256 experts with
+    top-16, an expert count that is not a multiple of 32, top-k = E, one
+    expert and ragged last chunks -- indices, the stable permutation and the
+    offsets bit for bit against the oracle, and the layer output on a few
+    tokens."""
+    H = I = 64
+    c = _small_case(T, E, topk, H, I, seed=T + E)
+    out, routing = _run(c)
+    tokens = sorted(set([0, 1, T // 2, T - 1]))
+    ref = _oracle(c, tokens=tokens)
+    _check_routing(routing, ref, T, topk, E)
+    _, offsets, perm, inv = omoe.permute(ref["idx"], E)
+    assert np.array_equal(routing["perm"], perm)
+    gu.compare(out[tokens], ref["out_bits"], f"MoE T={T} E={E} top-{topk}")
 
 
 @pytest.mark.parametrize("T", [5, 70])

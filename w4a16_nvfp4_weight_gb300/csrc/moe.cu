@@ -65,11 +65,11 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
 // unused expert (largest key, then lowest index) and two warp reductions pick
 // the winner: the largest key, then the lowest expert index among its holders.
 // Lane j ends up holding selection j, written with one coalesced store.  With
-// `tok_mask` (tokens 0..63), bit t of expert e's 64-bit mask is set for each
-// selected expert e.
+// `tok_mask` (tokens mask_t0 .. mask_t0 + 63), bit t - mask_t0 of expert e's
+// 64-bit mask is set for each selected expert e.
 __device__ void route_token(const float* __restrict__ logits, int64_t t, int E, int topk,
                             int32_t* __restrict__ idx, float* __restrict__ wts, int lane,
-                            uint32_t* tok_mask = nullptr) {
+                            uint32_t* tok_mask = nullptr, int64_t mask_t0 = 0) {
     constexpr int kPer = kMaxExperts / 32;
     float l[kPer];
     uint32_t key[kPer];
@@ -105,7 +105,10 @@ __device__ void route_token(const float* __restrict__ logits, int64_t t, int E, 
     if (lane < topk) {
         idx[t * topk + lane] = my_e;
         wts[t * topk + lane] = w / sum;
-        if (tok_mask != nullptr) atomicOr(&tok_mask[2 * my_e + (int)(t >> 5)], 1u << (t & 31));
+        if (tok_mask != nullptr) {
+            const int tb = (int)(t - mask_t0);
+            atomicOr(&tok_mask[2 * my_e + (tb >> 5)], 1u << (tb & 31));
+        }
     }
 }
 
@@ -126,8 +129,9 @@ constexpr int kPermWarps = kPermThreads / 32;
 
 // Offsets and work items from the per-expert counts cnt[0..E) in shared
 // memory, by one warp: lane l scans the experts [l * per, (l + 1) * per).
-// Writes offsets[0..E], off_s[e] = offsets[e], the items (expert, first
-// permuted row, rows <= tok) when `items` is not null, and their count.
+// Writes off_s[e] = offsets[e], offsets[0..E] when `offsets` is not null, the
+// items (expert, first permuted row, rows <= tok) when `items` is not null, and
+// their count.
 __device__ void expert_tables(const int32_t* cnt, int E, int tok, int32_t* __restrict__ offsets, int32_t* off_s,
                               int4* __restrict__ items, int32_t* __restrict__ n_items, int lane) {
     const int per = (E + 31) / 32;
@@ -147,14 +151,14 @@ __device__ void expert_tables(const int32_t* cnt, int E, int tok, int32_t* __res
     int run = rows_incl - rows, item = its_incl - its;
     for (int e = e0; e < e1; ++e) {
         const int c = cnt[e];
-        offsets[e] = run;
+        if (offsets != nullptr) offsets[e] = run;
         off_s[e] = run;
         if (items != nullptr)
             for (int r = 0; r < c; r += tok) items[item++] = make_int4(e, run + r, min(tok, c - r), 0);
         run += c;
     }
     if (lane == 31) {
-        offsets[E] = rows_incl;
+        if (offsets != nullptr) offsets[E] = rows_incl;
         if (n_items != nullptr) *n_items = its_incl;
     }
 }
@@ -289,6 +293,103 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
     }
 }
 
+// Many tokens with a workspace: the permutation in chunks of 8 tokens, in three
+// short kernels that each spread over many SMs (the single-CTA permutation
+// grows by ~7.5 us per 1000 tokens: 37 us at 4096 tokens, against ~19 us for
+// the three kernels, route included).  route_count_kernel routes a chunk's tokens
+// (a warp per token, as route_kernel) and counts each expert's slots in it
+// from per-expert token masks; chunk_scan_kernel turns each expert's counts
+// over the chunks into exclusive prefixes and a total (a warp per expert);
+// chunk_permute_kernel gives chunk c's slots of expert e the positions after
+// the earlier chunks' slots of e, in token order -- the same stable order as
+// the single-CTA kernel.
+constexpr int kChunkTokens = 8;
+// From this many tokens: below, the routing kernel and the single-CTA
+// permutation (two launches) measured as fast as the three chunked ones.
+constexpr int64_t kChunkedRouteMinT = 513;
+constexpr int kChunkThreads = kChunkTokens * 32;      // a warp per token
+constexpr int kScanWarps = 8;
+
+__global__ void __launch_bounds__(kChunkThreads)
+route_count_kernel(const float* __restrict__ logits, int64_t T, int E, int topk, int32_t* __restrict__ idx,
+                   float* __restrict__ wts, int32_t* __restrict__ counts, int C) {
+    __shared__ uint32_t tok_mask[2 * kMaxExperts];      // bit t: token t0 + t chose the expert
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int c = blockIdx.x;
+    const int64_t t0 = (int64_t)c * kChunkTokens;
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    for (int i = tid; i < 2 * E; i += kChunkThreads) tok_mask[i] = 0u;
+    __syncthreads();
+    if (t0 + w < T) route_token(logits, t0 + w, E, topk, idx, wts, lane, tok_mask, t0);
+    __syncthreads();
+    // expert-major, so that one warp scans an expert's counts over the chunks coalesced
+    for (int e = tid; e < E; e += kChunkThreads) counts[(int64_t)e * C + c] = __popc(tok_mask[2 * e]);
+}
+
+__global__ void __launch_bounds__(kScanWarps * 32)
+chunk_scan_kernel(int32_t* __restrict__ counts, int C, int E, int32_t* __restrict__ totals) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    if (e >= E) return;
+    int32_t* row = counts + (int64_t)e * C;
+    int run = 0;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        const int v = c0 + lane < C ? row[c0 + lane] : 0;
+        int incl = v;
+        #pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        if (c0 + lane < C) row[c0 + lane] = run + incl - v;      // earlier chunks' slots of e
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) totals[e] = run;
+}
+
+__global__ void __launch_bounds__(kChunkTokens * kMaxTopk)
+chunk_permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E, int tok,
+                     const int32_t* __restrict__ base, const int32_t* __restrict__ totals, int C,
+                     int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                     int4* __restrict__ items, int32_t* __restrict__ n_items) {
+    constexpr int kThreads = kChunkTokens * kMaxTopk;
+    __shared__ uint32_t tok_mask[kMaxExperts];
+    __shared__ int32_t tot_s[kMaxExperts];
+    __shared__ int32_t base_s[kMaxExperts];
+    __shared__ int32_t off_s[kMaxExperts];
+    const int tid = threadIdx.x;
+    const int c = blockIdx.x;
+    const int64_t t0 = (int64_t)c * kChunkTokens;
+    const int nslots = (int)(min(T - t0, (int64_t)kChunkTokens) * topk);
+    pdl_wait_previous();
+    pdl_launch_dependents();
+    for (int e = tid; e < E; e += kThreads) {
+        tok_mask[e] = 0u;
+        tot_s[e] = totals[e];
+        base_s[e] = base[(int64_t)e * C + c];
+    }
+    const int e_mine = tid < nslots ? idx[t0 * topk + tid] : -1;
+    __syncthreads();
+    const int t = tid / topk;                            // token of this thread's slot, within the chunk
+    if (e_mine >= 0) atomicOr(&tok_mask[e_mine], 1u << t);
+    if (tid < 32)
+        expert_tables(tot_s, E, tok, c == 0 ? offsets : nullptr, off_s, c == 0 ? items : nullptr,
+                      c == 0 ? n_items : nullptr, tid);
+    __syncthreads();
+    if (e_mine >= 0) {
+        const int pos = off_s[e_mine] + base_s[e_mine] + __popc(tok_mask[e_mine] & ((1u << t) - 1u));
+        const int64_t i = t0 * topk + tid;
+        perm[pos] = (int32_t)i;
+        inv[i] = pos;
+    }
+}
+
+// Chunks of the chunked permutation.
+int64_t route_chunks(int64_t T) { return ceil_div(T, (int64_t)kChunkTokens); }
+
 // Token words per permutation chunk: a chunk holds at most kPermSlots slots
 // per thread, and its masks and prefixes take about E * wc * 8 bytes of at
 // most 160 KB of shared memory.
@@ -359,10 +460,11 @@ __device__ __forceinline__ float plain_act(float v, int act) {
 // ONE = 1: FC1 of a single token, ONE = 2: its FC2 with the combine.  The
 // token's routing is computed by every CTA from the logits (the same top-k
 // everywhere), so no routing kernel runs: grid z is the routing slot j, whose
-// expert is the j-th selection.  FC1 writes h_j to row j of H.  FC2 gives each
-// CTA the whole K of one slot and clusters the topk slots of a row group: the
-// push reduction then sums p_j * y_j over the slots in slot order and writes
-// the output row, so no combine kernel runs either.
+// expert is the j-th selection.  FC1 writes h_j to row j of H.  FC2 clusters
+// the topk slots of a row group, each slot's K split over `splits` CTAs: the
+// push reduction then sums p_j * y_j over the slots in slot order (each
+// slot's splits in order) and writes the output row, so no combine kernel
+// runs either.
 template <int MT, bool GATED, bool F16, bool AWQ, int ONE = 0>
 __global__ void __launch_bounds__(kThreads)
 moe_linear_kernel(const MoeLinParams p) {
@@ -391,9 +493,10 @@ moe_linear_kernel(const MoeLinParams p) {
     const int cgi = blockIdx.x;                // column group: 64 (gated) or 128 output features
     const int split = blockIdx.y;
     const int item_id = blockIdx.z;
-    // the cluster's reduction ranks: the K splits, or (single-token FC2) the slots
-    const int rank = ONE == 2 ? item_id : split;
-    const int nranks = ONE == 2 ? p.topk : p.splits;
+    // the cluster's reduction ranks: the K splits, or (single-token FC2) the
+    // slots, each with its K splits (slot-major, so the sum runs slot by slot)
+    const int rank = ONE == 2 ? item_id * p.splits + split : split;
+    const int nranks = ONE == 2 ? p.topk * p.splits : p.splits;
     // Items and activations come from earlier kernels.  Dependents are released
     // only after the wait: an FC2 reads the routing tables before its own wait
     // (`early`), which is safe once the kernel that wrote them, two launches
@@ -605,7 +708,8 @@ moe_linear_kernel(const MoeLinParams p) {
             }
             if (rows_valid)
                 stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
-                    a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc);
+                    a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), nkb - i * kBlocksPerStage, acc,
+                    MT == 1 ? 1 : (nrows + 7) >> 3);
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -957,7 +1061,8 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
                     }
                     if (rows_valid)
                         stage_mma<MT, kXRowElems, F16, kBlocksPerStage, kBlockBytes>(
-                            a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), stage_nb(i), acc);
+                            a0 + s * kStageBytes, lane, lut_s, x0 + s * (kStageBytes / 2), stage_nb(i), acc,
+                            MT == 1 ? 1 : (nrows + 7) >> 3);
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
@@ -1034,31 +1139,47 @@ __global__ void combine_kernel(const float* __restrict__ Yp, int64_t T, int topk
 }
 
 // Rows of X in permuted (expert-contiguous) order, for the tile path:
-// Xp[r] = X[perm[r] / topk], times the AWQ pre-quant scale when given.
+// Xp[r] = X[perm[r] / topk], times the AWQ pre-quant scale when given.  A
+// thread moves kGatherChunks 16-byte chunks, blockDim chunks apart, with all
+// their row-index loads and then all their data loads in flight at once.
+constexpr int kGatherChunks = 4;
+
 template <bool F16>
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ pqs,
                                    const int32_t* __restrict__ perm, int topk, int64_t n, int64_t H,
                                    uint16_t* __restrict__ Xp) {
     pdl_wait_previous();
     pdl_launch_dependents();
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (i >= n * H) return;
-    const int64_t r = i / H, k = i % H;
-    const int64_t t = perm[r] / topk;
-    uint4 v = *reinterpret_cast<const uint4*>(X + t * H + k);
-    if (pqs != nullptr) {
-        const uint4 sv4 = *reinterpret_cast<const uint4*>(pqs + k);
-        uint32_t xv[4] = {v.x, v.y, v.z, v.w};
-        const uint32_t sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
-        #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint16_t lo = awq_mul<F16>((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
-            const uint16_t hi = awq_mul<F16>((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
-            xv[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-        }
-        v = make_uint4(xv[0], xv[1], xv[2], xv[3]);
+    const int64_t chunks = n * H / 8;
+    const int64_t c0 = (int64_t)blockIdx.x * blockDim.x * kGatherChunks + threadIdx.x;
+    int64_t src[kGatherChunks];
+    #pragma unroll
+    for (int u = 0; u < kGatherChunks; ++u) {
+        const int64_t i = (c0 + (int64_t)u * blockDim.x) * 8;
+        src[u] = i < n * H ? (int64_t)(perm[i / H] / topk) * H + i % H : -1;
     }
-    *reinterpret_cast<uint4*>(Xp + i) = v;
+    uint4 v[kGatherChunks];
+    #pragma unroll
+    for (int u = 0; u < kGatherChunks; ++u)
+        if (src[u] >= 0) v[u] = *reinterpret_cast<const uint4*>(X + src[u]);
+    #pragma unroll
+    for (int u = 0; u < kGatherChunks; ++u) {
+        const int64_t c = c0 + (int64_t)u * blockDim.x;
+        if (c >= chunks) continue;
+        if (pqs != nullptr) {
+            const uint4 sv4 = *reinterpret_cast<const uint4*>(pqs + (c * 8) % H);
+            uint32_t xv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            const uint32_t sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint16_t lo = awq_mul<F16>((uint16_t)(xv[e] & 0xFFFF), (uint16_t)(sv[e] & 0xFFFF));
+                const uint16_t hi = awq_mul<F16>((uint16_t)(xv[e] >> 16), (uint16_t)(sv[e] >> 16));
+                xv[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            v[u] = make_uint4(xv[0], xv[1], xv[2], xv[3]);
+        }
+        *reinterpret_cast<uint4*>(Xp + c * 8) = v[u];
+    }
 }
 
 // Launch with programmatic dependent launch enabled (see route_kernel).
@@ -1165,14 +1286,20 @@ nvfp4_status launch_moe_linear(const MoeLinParams& p, unsigned gx, unsigned max_
 
 // Single-token kernels: FC1 (ONE = 1; K split across a cluster of `splits`)
 // and FC2 with the combine (ONE = 2; one cluster per row group over the topk
-// slots), both with grid z = the routing slot.
+// slots and their `splits` K splits), both with grid z = the routing slot.
 template <bool GATED, bool F16, bool AWQ, int ONE>
 nvfp4_status launch_moe_one_typed(const MoeLinParams& p, unsigned gx, cudaStream_t s) {
     const size_t smem = moe_lin_smem(1, GATED, GATED && p.half_stride != 0);
     cudaError_t e = cudaFuncSetAttribute(moe_linear_kernel<1, GATED, F16, AWQ, ONE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return check_cuda(e, "MoE single token: shared memory attribute");
-    const unsigned ys = ONE == 1 ? (unsigned)p.splits : 1u;
+    const unsigned ys = (unsigned)p.splits;
+    const unsigned zs = ONE == 2 ? (unsigned)p.topk : 1u;
+    if (ys * zs > 8) {             // clusters of up to 16 CTAs are not portable: opt in
+        e = cudaFuncSetAttribute(moe_linear_kernel<1, GATED, F16, AWQ, ONE>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return check_cuda(e, "MoE single token: cluster size attribute");
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, ys, (unsigned)p.topk);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1182,7 +1309,7 @@ nvfp4_status launch_moe_one_typed(const MoeLinParams& p, unsigned gx, cudaStream
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = ys;
-    attr[0].val.clusterDim.z = ONE == 2 ? (unsigned)p.topk : 1u;
+    attr[0].val.clusterDim.z = zs;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
@@ -1209,7 +1336,7 @@ nvfp4_status launch_moe_persist_mt(int mt, const MoeLinParams& p, int ncg, int64
 }
 
 struct MoeLayout {
-    size_t idx, wts, offsets, perm, inv, items, n_items, xp, h, yp, total;
+    size_t idx, wts, offsets, perm, inv, items, n_items, counts, xp, h, yp, total;
     bool tile;              // tensor-core tile path (many rows per expert) or the streaming path
     int tok, mt, subm;
     int64_t max_items;
@@ -1241,6 +1368,7 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
     L.inv = take(n * 4);
     L.items = take(L.max_items * 16);
     L.n_items = take(4);
+    L.counts = T >= kChunkedRouteMinT ? take((size_t)E * (route_chunks(T) + 1) * 4) : 0;
     L.xp = L.tile ? take(n * H * 2) : 0;
     L.h = take(n * I * 2);
     L.yp = take(n * H * 4);
@@ -1251,16 +1379,31 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
 // Route (top-k + softmax over the selected logits) and permute (counts,
 // offsets, stable permutation, its inverse, and -- when `items` is not null --
 // the work list of `tok`-row items): one fused single-CTA kernel for few
-// tokens, else a routing kernel and a permutation kernel.
+// tokens; else, with `counts` scratch (E x (ceil(T / 8) + 1) ints), the three
+// chunked kernels; without it a routing kernel and a single-CTA permutation.
 nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int topk, int tok, int32_t* idx,
                             float* wts, int32_t* offsets, int32_t* perm, int32_t* inv, int4* items,
-                            int32_t* n_items, cudaStream_t s) {
+                            int32_t* n_items, cudaStream_t s, int32_t* counts = nullptr) {
     nvfp4_status st;
     const int wc = permute_words(T, E, topk);
     const size_t psmem = permute_smem_bytes(E, wc);
     if (T <= kFusedRouteMaxT)
         return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), 0, s, "MoE route+permute: launch",
                               router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items);
+    if (counts != nullptr) {
+        const int C = (int)route_chunks(T);
+        int32_t* totals = counts + (int64_t)E * C;
+        st = launch_chained(route_count_kernel, dim3((unsigned)C), dim3(kChunkThreads), 0, s,
+                            "MoE route+count: launch", router_logits, T, E, topk, idx, wts, counts, C);
+        if (st != NVFP4_OK) return st;
+        st = launch_chained(chunk_scan_kernel, dim3((unsigned)ceil_div(E, kScanWarps)), dim3(kScanWarps * 32), 0, s,
+                            "MoE chunk scan: launch", counts, C, E, totals);
+        if (st != NVFP4_OK) return st;
+        return launch_chained(chunk_permute_kernel, dim3((unsigned)C), dim3(kChunkTokens * kMaxTopk), 0, s,
+                              "MoE chunk permute: launch", (const int32_t*)idx, T, topk, E, tok,
+                              (const int32_t*)counts, (const int32_t*)totals, C, offsets, perm, inv, items,
+                              n_items);
+    }
     st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
                         router_logits, T, E, topk, idx, wts);
     if (st != NVFP4_OK) return st;
@@ -1426,7 +1569,11 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         MoeLinParams p2{};
         p2.w = (const uint8_t*)fc2; p2.w_stride = nvfp4_repack_size(H, I);
         p2.N = H; p2.K = I; p2.KB = round_up(I, kBlockK) / kBlockK;
-        p2.splits = 1; p2.kbs = (int)p2.KB;
+        // K split in two when the slots' cluster stays within 16 CTAs: twice
+        // the CTAs for FC2's small grid (one per row group and slot)
+        const int64_t sp2 = (2 * topk <= 16 && p2.KB >= 4) ? 2 : 1;
+        p2.kbs = (int)ceil_div(p2.KB, sp2);
+        p2.splits = (int)ceil_div(p2.KB, (int64_t)p2.kbs);
         p2.X = hbuf; p2.topk = topk; p2.I = I; p2.status = status;
         p2.logits = router_logits; p2.E = E; p2.out = (uint16_t*)out;
         const unsigned fc2_groups = (unsigned)ceil_div(H, 128);
@@ -1436,14 +1583,15 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
 
     // AWQ: the tile path scales the rows while gathering them, the streaming
     // path the activation fragments inside FC1; no separate pass either way
-    st = launch_routing(router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items, s);
+    st = launch_routing(router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items, s,
+                        T >= kChunkedRouteMinT ? (int32_t*)(ws + L.counts) : nullptr);
     if (st != NVFP4_OK) return st;
 
     if (L.tile) {
         // gather the routed rows into expert-contiguous order, then two tile GEMMs
         uint16_t* xp = (uint16_t*)(ws + L.xp);
         st = launch_chained(f16 ? gather_rows_kernel<true> : gather_rows_kernel<false>,
-                            dim3((unsigned)ceil_div(n * H / 8, 256)), dim3(256), 0, s,
+                            dim3((unsigned)ceil_div(n * H / 8, 256 * kGatherChunks)), dim3(256), 0, s,
                             "MoE gather: launch", (const uint16_t*)X, (const uint16_t*)fc1_pre_quant_scale,
                             (const int32_t*)perm, topk, n, H, xp);
         if (st != NVFP4_OK) return st;

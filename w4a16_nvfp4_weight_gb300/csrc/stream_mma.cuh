@@ -127,10 +127,12 @@ struct AwqStages {
 // token row g, group q of the activation chunk (row stride XS elements,
 // 16-byte aligned).  Within the group the MMA's k order is permuted -- MMA j
 // consumes k = 4j..4j+3 of every lane's group -- and the activation fragments
-// use the same permutation.
+// use the same permutation.  Only the first `mt_used` 8-token tiles hold
+// tokens (warp-uniform): the MMAs and activation loads of the others are
+// skipped, their accumulators stay zero.
 template <int MT, int XS, bool F16>
 __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc0, uint32_t sc1, uint32_t lut_s,
-                                         const uint16_t* xrow, float acc[MT][4]) {
+                                         const uint16_t* xrow, float acc[MT][4], int mt_used = MT) {
     const Lut t0 = lut_entry(lut_s, sc0);
     const Lut t1 = lut_entry(lut_s, sc1);
     uint32_t ra[8], rb[8];
@@ -140,6 +142,7 @@ __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc0, uint32
     expand8(codes.w, t1, rb + 4);
     #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
+        if (mt >= mt_used) break;
         const uint4 b01 = *reinterpret_cast<const uint4*>(xrow + mt * 8 * XS);
         const uint4 b23 = *reinterpret_cast<const uint4*>(xrow + mt * 8 * XS + 8);
         const uint32_t a0[4] = {ra[0], rb[0], ra[1], rb[1]};
@@ -154,12 +157,12 @@ __device__ __forceinline__ void atom_mma(const uint4 codes, uint32_t sc0, uint32
 }
 
 // One ring stage of B 64-k blocks (block stride BLK bytes; this warp's atom at
-// `a`, its activation chunk at `xrow`), nb of them holding data.  Full stages
-// take a loop without per-block bounds checks; only the last stage of a K
-// slice can be partial.
+// `a`, its activation chunk at `xrow`), nb of them holding data, the first
+// `mt_used` 8-token tiles holding tokens.  Full stages take a loop without
+// per-block bounds checks; only the last stage of a K slice can be partial.
 template <int MT, int XS, bool F16, int B, uint32_t BLK>
 __device__ __forceinline__ void stage_mma(const uint8_t* a, int lane, uint32_t lut_s, const uint16_t* xrow,
-                                          int nb, float acc[MT][4]) {
+                                          int nb, float acc[MT][4], int mt_used = MT) {
     uint4 codes[B];
     uint32_t s0[B], s1[B];
     const uint32_t sa = smem_u32(a) + kAtomCodeBytes + 2 * lane;
@@ -171,11 +174,12 @@ __device__ __forceinline__ void stage_mma(const uint8_t* a, int lane, uint32_t l
     }
     if (nb >= B) {
         #pragma unroll
-        for (int b = 0; b < B; ++b) atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc);
+        for (int b = 0; b < B; ++b)
+            atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc, mt_used);
     } else {
         #pragma unroll
         for (int b = 0; b < B; ++b)
-            if (b < nb) atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc);
+            if (b < nb) atom_mma<MT, XS, F16>(codes[b], s0[b], s1[b], lut_s, xrow + b * kBlockK, acc, mt_used);
     }
 }
 
