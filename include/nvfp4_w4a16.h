@@ -231,10 +231,12 @@ nvfp4_status nvfp4_w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int has_pre_
 /* ------------------------------------------------------------------------ */
 
 /*
- * The MoE layer's routing step on its own (the same kernels the layer runs
- * first): per token the top-k of its FP32 router logits (ties to the lower
- * expert index, slots in descending-logit order) and p = softmax over the k
- * selected logits; then the routing slots s = t*topk + j sorted by expert,
+ * The MoE layer's routing step on its own (the same results as the layer's
+ * own routing; the kernels are the layer's up to 512 tokens, above which the
+ * layer uses chunked kernels that need its workspace while this call keeps
+ * a single-CTA permutation): per token the top-k of its FP32 router logits
+ * (ties to the lower expert index, slots in descending-logit order) and
+ * p = softmax over the k selected logits; then the routing slots s = t*topk + j sorted by expert,
  * then token, then slot (stable).  "[TRTLLM-12288][feat] Support Nemotron-H
  * nvfp4 ckpt on Hopper", Changes table (MoE: only the routed, active experts'
  * weights are dequantized -- the permutation groups each expert's rows).
