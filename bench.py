@@ -548,14 +548,16 @@ def launch_count(nv, L):
 
 
 def moe_launches(T, E, topk, I):
-    """Kernels of one MoE call: route + permute (one fused kernel for T <= 64),
-    FC1 and FC2 (plus the row gather on the tile path), combine; one token:
-    two kernels."""
+    """Kernels of one MoE call: routing + permutation (one fused kernel up to 64
+    tokens, two up to 512, three chunked ones above), FC1 and FC2 (on the tile
+    path plus the row gather and the two streaming waves of the experts'
+    tails), combine; one token: two kernels."""
     if T == 1 and topk <= 8:
         return 2                      # single token: FC1 and FC2 (+ combine), each routing itself
     per_expert = T * topk // E
     tile = per_expert >= 32 and I % 128 == 0
-    return (1 if T <= 64 else 2) + (3 if tile else 2) + 1
+    routing = 1 if T <= 64 else 2 if T <= 512 else 3
+    return routing + (5 if tile else 2) + 1
 
 
 def mlp_launches(T, H, I):

@@ -72,6 +72,27 @@ def test_moe_small_full_compare(T, E, topk, H, I):
     gu.compare(out, ref["out_bits"], f"MoE T={T} E={E} k={topk}")
 
 
+@pytest.mark.parametrize("awq", [False, True])
+def test_moe_tile_path_expert_tails(awq):
+    """Tile path (about 150 rows per expert: 128-row items): expert 0 gets 135
+    rows (a 7-row tail past its full tile, run as a streaming item), expert 1
+    165 rows (a 37-row tail, more than the 32 a streaming tail takes, so a
+    second tile item).  Every output row against the oracle, and with AWQ the
+    tail rows are scaled inside the streaming kernel, the others while
+    gathering."""
+    T, E, topk, H, I = 300, 2, 1, 256, 128
+    c = _small_case(T, E, topk, H, I, seed=91, awq=awq)
+    logits = np.zeros((T, E), dtype=np.float32)
+    logits[:135, 0] = 1.0
+    logits[135:, 1] = 1.0
+    c.logits = logits
+    out, routing = _run(c, awq=awq)
+    ref = _oracle(c, awq=awq)
+    _check_routing(routing, ref, T, topk, E)
+    assert routing["offsets"].tolist() == [0, 135, 300]
+    gu.compare(out, ref["out_bits"], f"MoE tile tails awq={awq}")
+
+
 def test_moe_awq_and_dropped_scale_control():
     c = _small_case(10, 8, 2, 128, 64, seed=5, awq=True)
     out, routing = _run(c, awq=True)

@@ -131,35 +131,50 @@ constexpr int kPermWarps = kPermThreads / 32;
 // memory, by one warp: lane l scans the experts [l * per, (l + 1) * per).
 // Writes off_s[e] = offsets[e], offsets[0..E] when `offsets` is not null, the
 // items (expert, first permuted row, rows <= tok) when `items` is not null, and
-// their count.
+// their count.  With tail_rows > 0 (tile path), an expert with more than tok
+// rows whose last item would hold at most tail_rows rows gets that tail as an
+// item of a second list, items[tail_base..] with its count in n_items[1], for
+// the streaming kernels, which do not pay a whole tile for a few rows.
 __device__ void expert_tables(const int32_t* cnt, int E, int tok, int32_t* __restrict__ offsets, int32_t* off_s,
-                              int4* __restrict__ items, int32_t* __restrict__ n_items, int lane) {
+                              int4* __restrict__ items, int32_t* __restrict__ n_items, int lane,
+                              int tail_rows = 0, int tail_base = 0) {
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int rows = 0, its = 0;
+    auto is_tail = [&](int c) { return tail_rows > 0 && c > tok && c % tok != 0 && c % tok <= tail_rows; };
+    int rows = 0, its = 0, tails = 0;
     for (int e = e0; e < e1; ++e) {
-        rows += cnt[e];
-        its += (cnt[e] + tok - 1) / tok;
+        const int c = cnt[e];
+        rows += c;
+        if (is_tail(c)) { its += c / tok; ++tails; }
+        else its += (c + tok - 1) / tok;
     }
-    int rows_incl = rows, its_incl = its;
+    int rows_incl = rows, its_incl = its, tails_incl = tails;
     #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int r = __shfl_up_sync(0xffffffffu, rows_incl, off);
         const int k = __shfl_up_sync(0xffffffffu, its_incl, off);
-        if (lane >= off) { rows_incl += r; its_incl += k; }
+        const int q = __shfl_up_sync(0xffffffffu, tails_incl, off);
+        if (lane >= off) { rows_incl += r; its_incl += k; tails_incl += q; }
     }
-    int run = rows_incl - rows, item = its_incl - its;
+    int run = rows_incl - rows, item = its_incl - its, tail = tails_incl - tails;
     for (int e = e0; e < e1; ++e) {
         const int c = cnt[e];
         if (offsets != nullptr) offsets[e] = run;
         off_s[e] = run;
-        if (items != nullptr)
-            for (int r = 0; r < c; r += tok) items[item++] = make_int4(e, run + r, min(tok, c - r), 0);
+        if (items != nullptr) {
+            const bool t = is_tail(c);
+            const int main_rows = t ? c - c % tok : c;
+            for (int r = 0; r < main_rows; r += tok) items[item++] = make_int4(e, run + r, min(tok, main_rows - r), 0);
+            if (t) items[tail_base + tail++] = make_int4(e, run + main_rows, c % tok, 0);
+        }
         run += c;
     }
     if (lane == 31) {
         if (offsets != nullptr) offsets[E] = rows_incl;
-        if (n_items != nullptr) *n_items = its_incl;
+        if (n_items != nullptr) {
+            n_items[0] = its_incl;
+            if (tail_rows > 0) n_items[1] = tails_incl;
+        }
     }
 }
 
@@ -177,7 +192,7 @@ constexpr int kPermSlots = 16;
 __global__ void __launch_bounds__(kPermThreads)
 permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E, int tok, int wc,
                int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-               int4* __restrict__ items, int32_t* __restrict__ n_items) {
+               int4* __restrict__ items, int32_t* __restrict__ n_items, int tail_rows, int tail_base) {
     extern __shared__ uint32_t psm[];
     // rows of ws >= wc words, ws odd: the experts of one token's slots, which
     // touch the same word column, fall on different banks
@@ -205,7 +220,7 @@ permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E, int 
             if (ev[u] >= 0) atomicAdd(&cnt[ev[u]], 1);
     }
     __syncthreads();
-    if (tid < 32) expert_tables(cnt, E, tok, offsets, off_s, items, n_items, tid);
+    if (tid < 32) expert_tables(cnt, E, tok, offsets, off_s, items, n_items, tid, tail_rows, tail_base);
     __syncthreads();
     for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
     // a chunk: at most wc words of tokens and at most kBatch slots
@@ -263,7 +278,7 @@ __global__ void __launch_bounds__(kPermThreads)
 route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int topk, int tok,
                      int32_t* __restrict__ idx, float* __restrict__ wts,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                     int4* __restrict__ items, int32_t* __restrict__ n_items) {
+                     int4* __restrict__ items, int32_t* __restrict__ n_items, int tail_rows, int tail_base) {
     __shared__ uint32_t tok_mask[2 * kMaxExperts];      // bit t: token t chose the expert
     __shared__ int32_t cnt_s[kMaxExperts];
     __shared__ int32_t off_s[kMaxExperts];
@@ -277,7 +292,7 @@ route_permute_kernel(const float* __restrict__ logits, int64_t T, int E, int top
     if (w == 0) {
         for (int e = lane; e < E; e += 32) cnt_s[e] = __popc(tok_mask[2 * e]) + __popc(tok_mask[2 * e + 1]);
         __syncwarp();
-        expert_tables(cnt_s, E, tok, offsets, off_s, items, n_items, lane);
+        expert_tables(cnt_s, E, tok, offsets, off_s, items, n_items, lane, tail_rows, tail_base);
     }
     __syncthreads();
     // slot i = t * topk + j of expert e: after the earlier tokens of e
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(kChunkTokens * kMaxTopk)
 chunk_permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E, int tok,
                      const int32_t* __restrict__ base, const int32_t* __restrict__ totals, int C,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                     int4* __restrict__ items, int32_t* __restrict__ n_items) {
+                     int4* __restrict__ items, int32_t* __restrict__ n_items, int tail_rows, int tail_base) {
     constexpr int kThreads = kChunkTokens * kMaxTopk;
     __shared__ uint32_t tok_mask[kMaxExperts];
     __shared__ int32_t tot_s[kMaxExperts];
@@ -377,7 +392,7 @@ chunk_permute_kernel(const int32_t* __restrict__ idx, int64_t T, int topk, int E
     if (e_mine >= 0) atomicOr(&tok_mask[e_mine], 1u << t);
     if (tid < 32)
         expert_tables(tot_s, E, tok, c == 0 ? offsets : nullptr, off_s, c == 0 ? items : nullptr,
-                      c == 0 ? n_items : nullptr, tid);
+                      c == 0 ? n_items : nullptr, tid, tail_rows, tail_base);
     __syncthreads();
     if (e_mine >= 0) {
         const int pos = off_s[e_mine] + base_s[e_mine] + __popc(tok_mask[e_mine] & ((1u << t) - 1u));
@@ -1335,10 +1350,15 @@ nvfp4_status launch_moe_persist_mt(int mt, const MoeLinParams& p, int ncg, int64
                      : launch_moe_persist<4, GATED>(p, ncg, max_units, early, f16, s);
 }
 
+// Tile path: an expert's last few rows past its full tiles (at most this many)
+// run as one 32-row item of the streaming kernels instead of a whole tile.
+constexpr int kTileTailRows = 32;
+
 struct MoeLayout {
     size_t idx, wts, offsets, perm, inv, items, n_items, counts, xp, h, yp, total;
     bool tile;              // tensor-core tile path (many rows per expert) or the streaming path
     int tok, mt, subm;
+    int tail_rows;          // tile path: kTileTailRows (tail items follow the max_items main ones)
     int64_t max_items;
 };
 
@@ -1366,8 +1386,9 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
     L.offsets = take((E + 1) * 4);
     L.perm = take(n * 4);
     L.inv = take(n * 4);
-    L.items = take(L.max_items * 16);
-    L.n_items = take(4);
+    L.tail_rows = L.tile ? kTileTailRows : 0;
+    L.items = take((L.max_items + (L.tile ? E : 0)) * 16);
+    L.n_items = take(8);
     L.counts = T >= kChunkedRouteMinT ? take((size_t)E * (route_chunks(T) + 1) * 4) : 0;
     L.xp = L.tile ? take(n * H * 2) : 0;
     L.h = take(n * I * 2);
@@ -1383,13 +1404,15 @@ MoeLayout moe_layout(int64_t T, int E, int topk, int64_t H, int64_t I) {
 // chunked kernels; without it a routing kernel and a single-CTA permutation.
 nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int topk, int tok, int32_t* idx,
                             float* wts, int32_t* offsets, int32_t* perm, int32_t* inv, int4* items,
-                            int32_t* n_items, cudaStream_t s, int32_t* counts = nullptr) {
+                            int32_t* n_items, cudaStream_t s, int32_t* counts = nullptr, int tail_rows = 0,
+                            int tail_base = 0) {
     nvfp4_status st;
     const int wc = permute_words(T, E, topk);
     const size_t psmem = permute_smem_bytes(E, wc);
     if (T <= kFusedRouteMaxT)
         return launch_chained(route_permute_kernel, dim3(1), dim3(kPermThreads), 0, s, "MoE route+permute: launch",
-                              router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items);
+                              router_logits, T, E, topk, tok, idx, wts, offsets, perm, inv, items, n_items,
+                              tail_rows, tail_base);
     if (counts != nullptr) {
         const int C = (int)route_chunks(T);
         int32_t* totals = counts + (int64_t)E * C;
@@ -1402,7 +1425,7 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
         return launch_chained(chunk_permute_kernel, dim3((unsigned)C), dim3(kChunkTokens * kMaxTopk), 0, s,
                               "MoE chunk permute: launch", (const int32_t*)idx, T, topk, E, tok,
                               (const int32_t*)counts, (const int32_t*)totals, C, offsets, perm, inv, items,
-                              n_items);
+                              n_items, tail_rows, tail_base);
     }
     st = launch_chained(route_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, "MoE route: launch",
                         router_logits, T, E, topk, idx, wts);
@@ -1410,7 +1433,8 @@ nvfp4_status launch_routing(const float* router_logits, int64_t T, int E, int to
     cudaError_t ce = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if ((st = check_cuda(ce, "MoE permute: shared memory attribute")) != NVFP4_OK) return st;
     return launch_chained(permute_kernel, dim3(1), dim3(kPermThreads), psmem, s, "MoE permute: launch",
-                          (const int32_t*)idx, T, topk, E, tok, wc, offsets, perm, inv, items, n_items);
+                          (const int32_t*)idx, T, topk, E, tok, wc, offsets, perm, inv, items, n_items, tail_rows,
+                          tail_base);
 }
 
 // Work items expected in flight, for the split-K and persistent choices of the
@@ -1584,7 +1608,8 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
     // AWQ: the tile path scales the rows while gathering them, the streaming
     // path the activation fragments inside FC1; no separate pass either way
     st = launch_routing(router_logits, T, E, topk, L.tok, idx, wts, offsets, perm, inv, items, n_items, s,
-                        T >= kChunkedRouteMinT ? (int32_t*)(ws + L.counts) : nullptr);
+                        T >= kChunkedRouteMinT ? (int32_t*)(ws + L.counts) : nullptr, L.tail_rows,
+                        (int)L.max_items);
     if (st != NVFP4_OK) return st;
 
     if (L.tile) {
@@ -1602,11 +1627,38 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         t1.N = fc1_rows; t1.K = H; t1.I = I; t1.items = items; t1.n_items = n_items; t1.max_items = L.max_items;
         t1.perm = perm; t1.wts = wts; t1.H = hbuf; t1.status = status;
         if ((st = launch_tc_moe(t1, s)) != NVFP4_OK) return st;
+        // the experts' tails (<= 32 rows past their last full tile): one wave of
+        // the streaming kernel over the second item list, writing the same H rows
+        int4* tails = items + L.max_items;
+        int32_t* n_tails = n_items + 1;
+        MoeLinParams q1{};
+        q1.w = (const uint8_t*)fc1; q1.w_stride = fc1_stride; q1.half_stride = half_stride;
+        q1.N = fc1_rows; q1.K = H; q1.KB = round_up(H, kBlockK) / kBlockK;
+        q1.splits = 1; q1.kbs = (int)q1.KB;
+        q1.X = (const uint16_t*)X; q1.perm = perm; q1.topk = topk; q1.items = tails; q1.n_items = n_tails;
+        q1.I = I; q1.H = hbuf; q1.wts = wts; q1.status = status;
+        q1.pqs = (const uint16_t*)fc1_pre_quant_scale;
+        q1.act = gated ? 0 : activation;
+        const int64_t fc1_groups = gated ? I / 64 : ceil_div(I, 128);
+        constexpr int kTailMt = kTileTailRows / 8;
+        st = gated ? launch_moe_persist_mt<true>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, false, f16, s)
+                   : launch_moe_persist_mt<false>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, false, f16, s);
+        if (st != NVFP4_OK) return st;
         TcMoeParams t2 = t1;
         t2.fc1 = false; t2.act = 0; t2.half_stride = 0;
         t2.X = hbuf; t2.w = (const uint8_t*)fc2; t2.w_stride = nvfp4_repack_size(H, I);
         t2.N = H; t2.K = I; t2.Yp = yp; t2.H = nullptr;
         if ((st = launch_tc_moe(t2, s)) != NVFP4_OK) return st;
+        MoeLinParams q2{};
+        q2.w = (const uint8_t*)fc2; q2.w_stride = nvfp4_repack_size(H, I);
+        q2.N = H; q2.K = I; q2.KB = round_up(I, kBlockK) / kBlockK;
+        q2.splits = 1; q2.kbs = (int)q2.KB;
+        q2.X = hbuf; q2.perm = perm; q2.topk = topk; q2.items = tails; q2.n_items = n_tails;
+        q2.I = I; q2.Yp = yp; q2.wts = wts; q2.status = status;
+        q2.early = 1;          // the routing tables are complete several launches back
+        const unsigned fc2_groups = (unsigned)ceil_div(H, 128);
+        st = launch_moe_persist_mt<false>(kTailMt, q2, (int)fc2_groups, fc2_groups * E, true, f16, s);
+        if (st != NVFP4_OK) return st;
     } else {
         const int64_t est_items = moe_est_items(L, n, E);
         MoeLinParams p1{};
