@@ -193,6 +193,8 @@ size_t nvfp4_w4a16_gemm_workspace(int64_t M, int64_t N, int64_t K, int has_pre_q
  * (only if that kernel itself allows its dependents to start early), and read
  * X / write Y only after it has.  So a kernel that rewrites the repacked
  * weight must not be such an early-release kernel directly before the GEMM.
+ * The tile kernels are launched in stream order but allow the kernel after
+ * them to start early (it still waits for them before touching their output).
  */
 nvfp4_status nvfp4_w4a16_gemm(const void* X, const void* repacked, const void* pre_quant_scale,
                               int64_t M, int64_t N, int64_t K, void* Y,

@@ -169,6 +169,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // A kernel launched after this one with programmatic dependent launch may
+    // start now (its CTAs fill SMs as this grid's last wave drains); it waits
+    // for this kernel (griddepcontrol.wait) before it reads what this writes.
+    // Launches of the tile kernels themselves are ordinary stream launches.
+    if (tid == 0) pdl_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t idesc = umma_idesc(128, kBN, F16);
 

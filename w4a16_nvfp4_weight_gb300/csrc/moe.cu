@@ -914,7 +914,11 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
         // lane 0 has armed the stage's barrier; lane 0 alone waits on barriers
         // and the warp follows its verdict.
         const unsigned all = 0xffffffffu;
+        // early: 0 = wait first; 1 = the first weight stages before the wait;
+        // 2 = nothing read depends on the preceding kernel: wait only at the
+        // end, so that this kernel completes after it
         bool waited = early == 0;
+        const bool late = early == 2;
         if (waited) {
             pdl_wait_previous();
             pdl_launch_dependents();
@@ -992,7 +996,7 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
                              xsrc + stage_kx(i), (uint32_t)(stage_nb(i) * kBlockK * 2), &full[s]);
             };
             int i = 0;
-            if (!waited) {
+            if (!waited && !late) {
                 // weights (and the table, above) before the wait, activations
                 // after it; no stage has been issued yet (gs == 0)
                 const int pre = min(nst, kStages);
@@ -1026,8 +1030,10 @@ moe_persist_kernel(const MoeLinParams p, int ncg, int early) {
         __syncwarp();
     } else {
         // ---------------- consumers
-        pdl_wait_previous();
-        pdl_launch_dependents();
+        if (early != 2) {
+            pdl_wait_previous();
+            pdl_launch_dependents();
+        }
         const int g = lane >> 2, q = lane & 3, c = lane & 3;
         const int64_t units = (int64_t)(*p.n_items) * ncg;
         const uint8_t* const a0 = ring + warp * kAtomBytes;
@@ -1266,7 +1272,7 @@ int persist_ctas_per_sm(size_t smem) {
 }
 
 template <int MT, bool GATED, bool F16, bool AWQ>
-nvfp4_status launch_moe_persist_typed(const MoeLinParams& p, int ncg, int64_t max_units, bool early, cudaStream_t s) {
+nvfp4_status launch_moe_persist_typed(const MoeLinParams& p, int ncg, int64_t max_units, int early, cudaStream_t s) {
     const size_t smem = persist_smem(MT, GATED, GATED && p.half_stride != 0);
     cudaError_t e = cudaFuncSetAttribute(moe_persist_kernel<MT, GATED, F16, AWQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1275,12 +1281,12 @@ nvfp4_status launch_moe_persist_typed(const MoeLinParams& p, int ncg, int64_t ma
     const int64_t grid = std::min<int64_t>(max_units, (int64_t)per_sm * sm_count());
     return launch_chained(moe_persist_kernel<MT, GATED, F16, AWQ>, dim3((unsigned)std::max<int64_t>(grid, 1)),
                           dim3(kThreads), smem, s, GATED ? "MoE FC1 (persistent): launch" : "MoE FC2 (persistent): launch",
-                          p, ncg, early ? 1 : 0);
+                          p, ncg, early);
 }
 
 // The persistent instance for the activation type and AWQ choice.
 template <int MT, bool GATED>
-nvfp4_status launch_moe_persist(const MoeLinParams& p, int ncg, int64_t max_units, bool early, bool f16,
+nvfp4_status launch_moe_persist(const MoeLinParams& p, int ncg, int64_t max_units, int early, bool f16,
                                 cudaStream_t s) {
     if (p.pqs != nullptr)
         return f16 ? launch_moe_persist_typed<MT, GATED, true, true>(p, ncg, max_units, early, s)
@@ -1343,7 +1349,7 @@ nvfp4_status launch_moe_linear_mt(int mt, const MoeLinParams& p, unsigned gx, un
 }
 
 template <bool GATED>
-nvfp4_status launch_moe_persist_mt(int mt, const MoeLinParams& p, int ncg, int64_t max_units, bool early, bool f16,
+nvfp4_status launch_moe_persist_mt(int mt, const MoeLinParams& p, int ncg, int64_t max_units, int early, bool f16,
                                    cudaStream_t s) {
     return mt == 1   ? launch_moe_persist<1, GATED>(p, ncg, max_units, early, f16, s)
            : mt == 2 ? launch_moe_persist<2, GATED>(p, ncg, max_units, early, f16, s)
@@ -1641,8 +1647,11 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         q1.act = gated ? 0 : activation;
         const int64_t fc1_groups = gated ? I / 64 : ceil_div(I, 128);
         constexpr int kTailMt = kTileTailRows / 8;
-        st = gated ? launch_moe_persist_mt<true>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, false, f16, s)
-                   : launch_moe_persist_mt<false>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, false, f16, s);
+        // it reads nothing the FC1 tiles write, so it may run beside their last
+        // wave (the tile kernel releases its dependents at once); it waits for
+        // the tiles only before it ends (late mode 2)
+        st = gated ? launch_moe_persist_mt<true>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, 2, f16, s)
+                   : launch_moe_persist_mt<false>(kTailMt, q1, (int)fc1_groups, fc1_groups * E, 2, f16, s);
         if (st != NVFP4_OK) return st;
         TcMoeParams t2 = t1;
         t2.fc1 = false; t2.act = 0; t2.half_stride = 0;
@@ -1657,7 +1666,8 @@ nvfp4_status moe_impl(const void* X, const float* router_logits, const void* fc1
         q2.I = I; q2.Yp = yp; q2.wts = wts; q2.status = status;
         q2.early = 1;          // the routing tables are complete several launches back
         const unsigned fc2_groups = (unsigned)ceil_div(H, 128);
-        st = launch_moe_persist_mt<false>(kTailMt, q2, (int)fc2_groups, fc2_groups * E, true, f16, s);
+        // H is complete before the FC2 tiles start: beside their last wave too
+        st = launch_moe_persist_mt<false>(kTailMt, q2, (int)fc2_groups, fc2_groups * E, 2, f16, s);
         if (st != NVFP4_OK) return st;
     } else {
         const int64_t est_items = moe_est_items(L, n, E);
