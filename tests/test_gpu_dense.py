@@ -332,6 +332,27 @@ def test_lm_head_full_size_sampled():
         gu.compare(yb[:, rows], ref, f"LM head M={M}")
 
 
+@pytest.mark.parametrize("M,K,N", [(1000, 512, 8192), (600, 256, 1000)])
+def test_gemm_tile_output_only_4_byte_aligned(M, K, N):
+    """Y needs only 4-byte alignment: a tile GEMM into a view 4 bytes past an
+    aligned buffer takes the element-wise stores and gives the same bits as
+    into an aligned Y (the first shape plans the shared-memory tile kernel, the
+    second a tile kernel with N % 8 == 0 but a ragged last column block)."""
+    plan = nv.gemm_plan(M, N, K)
+    assert plan["kernel"] in ("tile_smem", "tile_tmem")
+    packed, scales, d = synth.weight_only(K, N, 31)
+    w = nv.repack(gu.u8(packed), gu.u8(scales), float(d), N, K)
+    x = gu.bits_to_bf16_tensor(synth.normal_bf16(synth.rng(32), (M, K)))
+    y0 = nv.gemm(x, w)
+    buf = torch.full((M * N + 2,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y1 = buf[2:].view(M, N)
+    assert y1.data_ptr() % 16 == 4
+    nv.gemm(x, w, out=y1)
+    gu.check_device_status()
+    assert np.array_equal(gu.tensor_to_bits(y0), gu.tensor_to_bits(y1))
+    assert torch.all(buf[:2] == 7.0)
+
+
 def test_gemm_bitwise_deterministic_across_runs():
     """Many waves of split-K clusters (ring reuse in every CTA): repeated runs must
     agree bit for bit -- the split-K reduction has a fixed order."""

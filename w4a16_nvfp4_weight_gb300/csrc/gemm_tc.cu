@@ -96,6 +96,37 @@ __device__ __forceinline__ float plain_act_tc(float v, int act) {
     return silu_tc(v);
 }
 
+// Warp-cooperative store of a block of 32 rows x 32 words: lane l holds the 32
+// consecutive 32-bit words of row l, bound for dst (16-byte aligned; null: row l
+// is not stored); only the first `valid` words of each row are stored (a
+// multiple of 4, the same for the whole warp).  The rows pass through a
+// 32 x 33-word tile in shared memory so that each 16-byte store belongs to a run
+// of 8 lanes writing 128 contiguous bytes of one row -- four rows per store
+// instruction instead of 16 bytes of each of 32 rows.
+__device__ __forceinline__ void store_rows32(uint32_t* tile, const uint32_t (&w)[32], uint32_t* dst, int valid,
+                                             int lane) {
+    #pragma unroll
+    for (int i = 0; i < 32; ++i) tile[lane * 33 + i] = w[i];
+    __syncwarp();
+    const int c = (lane & 7) * 4;
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = i * 4 + (lane >> 3);
+        uint32_t* d = reinterpret_cast<uint32_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), r));
+        const uint32_t* s = tile + r * 33 + c;
+        if (d != nullptr && c < valid) *reinterpret_cast<uint4*>(d + c) = make_uint4(s[0], s[1], s[2], s[3]);
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ uint32_t pack_act2(uint32_t a, uint32_t b, bool f16) {
+    return f16 ? ((uint32_t)f32_to_act_bits<true>(__uint_as_float(a)) |
+                  ((uint32_t)f32_to_act_bits<true>(__uint_as_float(b)) << 16))
+               : ((uint32_t)f32_to_act_bits<false>(__uint_as_float(a)) |
+                  ((uint32_t)f32_to_act_bits<false>(__uint_as_float(b)) << 16));
+}
+
 template <int SUBM, TcMode MODE, bool F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
@@ -300,45 +331,66 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
             for (int mi = 0; mi < SUBM; ++mi) {
                 const int64_t m = mrow + mi * 128;
                 const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + mi * kBN;
+                // Rows leave through store_rows32 (a 32 x 33-word tile per warp
+                // in the activation ring, idle once every MMA has completed).
+                uint32_t* tile = reinterpret_cast<uint32_t*>(a_ring) + (size_t)dw * (32 * 33);
                 if constexpr (MODE == TcMode::kDense) {
-                    const bool vec_ok = (p.N % 8) == 0;
-                    #pragma unroll 1
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const int col = half * 128 + c16 * 16;
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(trow + col, v);
-                        tmem_ld_wait();
-                        if (m >= m_end) continue;
-                        const int64_t n = n0 + col;
-                        if (p.partial != nullptr) {
-                            // split-K: FP32 partial rows, summed in split order afterwards
-                            float* prow = p.partial + ((int64_t)blockIdx.z * p.M + m) * p.N;
-                            if (vec_ok && n + 16 <= p.N) {
+                    // whole-row stores need 16-byte aligned rows: N % 8 == 0 and Y aligned
+                    const bool vec_ok = (p.N % 8) == 0 && (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
+                    if (p.partial != nullptr) {
+                        // split-K: FP32 partial rows, summed in split order afterwards
+                        float* prow = p.partial + ((int64_t)blockIdx.z * p.M + m) * p.N;
+                        #pragma unroll 1
+                        for (int c32 = 0; c32 < 4; ++c32) {
+                            const int col = half * 128 + c32 * 32;
+                            const int64_t n = n0 + col;
+                            uint32_t v[16], u[16];
+                            tmem_ld_32x32b_x16(trow + col, v);
+                            tmem_ld_32x32b_x16(trow + col + 16, u);
+                            tmem_ld_wait();
+                            if (n >= p.N) continue;
+                            if ((p.N % 8) == 0) {
+                                uint32_t w[32];
                                 #pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    *reinterpret_cast<uint4*>(prow + n + 4 * i) =
-                                        make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                            } else {
-                                for (int i = 0; i < 16 && n + i < p.N; ++i) prow[n + i] = __uint_as_float(v[i]);
+                                for (int i = 0; i < 16; ++i) { w[i] = v[i]; w[16 + i] = u[i]; }
+                                store_rows32(tile, w, m < m_end ? reinterpret_cast<uint32_t*>(prow + n) : nullptr,
+                                             (int)(p.N - n < 32 ? p.N - n : 32), lane);
+                            } else if (m < m_end) {
+                                #pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (n + i < p.N) prow[n + i] = __uint_as_float(i < 16 ? v[i] : u[i - 16]);
                             }
-                            continue;
                         }
-                        uint32_t packed[8];
-                        #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            packed[i] = (uint32_t)f32_to_act_bits<F16>(__uint_as_float(v[2 * i])) |
-                                        ((uint32_t)f32_to_act_bits<F16>(__uint_as_float(v[2 * i + 1])) << 16);
+                    } else {
                         uint16_t* yrow = p.Y + m * p.N;
-                        if (vec_ok && n + 16 <= p.N) {
-                            *reinterpret_cast<uint4*>(yrow + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                            *reinterpret_cast<uint4*>(yrow + n + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                        } else {
-                            for (int i = 0; i < 16 && n + i < p.N; ++i)
-                                yrow[n + i] = (uint16_t)(packed[i >> 1] >> ((i & 1) * 16));
+                        #pragma unroll 1
+                        for (int c64 = 0; c64 < 2; ++c64) {
+                            const int col = half * 128 + c64 * 64;
+                            const int64_t n = n0 + col;
+                            uint32_t w[32];
+                            #pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t v[16];
+                                tmem_ld_32x32b_x16(trow + col + 16 * q, v);
+                                tmem_ld_wait();
+                                #pragma unroll
+                                for (int i = 0; i < 8; ++i) w[8 * q + i] = pack_act2(v[2 * i], v[2 * i + 1], F16);
+                            }
+                            if (n >= p.N) continue;
+                            if (vec_ok) {
+                                store_rows32(tile, w, m < m_end ? reinterpret_cast<uint32_t*>(yrow + n) : nullptr,
+                                             (int)((p.N - n) / 2 < 32 ? (p.N - n) / 2 : 32), lane);
+                            } else if (m < m_end) {
+                                #pragma unroll
+                                for (int i = 0; i < 64; ++i)
+                                    if (n + i < p.N) yrow[n + i] = (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+                            }
                         }
                     }
                 } else if constexpr (MODE == TcMode::kMoeFc1) {
                     // columns [0,128) are gate, [128,256) up; this warp does 64 of the 128
+                    // (per-lane 32-byte stores: staging these 128-byte row pieces
+                    // through shared memory measured slower)
                     #pragma unroll 1
                     for (int c16 = 0; c16 < 4; ++c16) {
                         const int col = half * 64 + c16 * 16;
@@ -352,7 +404,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                         for (int i = 0; i < 8; ++i) {
                             const float h0 = silu_tc(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
                             const float h1 = silu_tc(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                            packed[i] = (uint32_t)f32_to_act_bits<F16>(h0) | ((uint32_t)f32_to_act_bits<F16>(h1) << 16);
+                            packed[i] = pack_act2(__float_as_uint(h0), __float_as_uint(h1), F16);
                         }
                         uint16_t* hrow = p.Y + m * p.I + n0 + col;      // I and n0 are multiples of 64
                         *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -361,41 +413,57 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcKParams p) {
                 } else if constexpr (MODE == TcMode::kMoeFc1Plain) {
                     // h = RN(act(v)) for 128 of the tile's 256 columns (N = I, a multiple of 64)
                     #pragma unroll 1
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const int col = half * 128 + c16 * 16;
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(trow + col, v);
-                        tmem_ld_wait();
+                    for (int c64 = 0; c64 < 2; ++c64) {
+                        const int col = half * 128 + c64 * 64;
                         const int64_t n = n0 + col;
-                        if (m >= m_end || n >= p.N) continue;
-                        uint32_t packed[8];
+                        uint32_t w[32];
                         #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float h0 = plain_act_tc(__uint_as_float(v[2 * i]), p.act);
-                            const float h1 = plain_act_tc(__uint_as_float(v[2 * i + 1]), p.act);
-                            packed[i] = (uint32_t)f32_to_act_bits<F16>(h0) | ((uint32_t)f32_to_act_bits<F16>(h1) << 16);
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t v[16];
+                            tmem_ld_32x32b_x16(trow + col + 16 * q, v);
+                            tmem_ld_wait();
+                            #pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float h0 = plain_act_tc(__uint_as_float(v[2 * i]), p.act);
+                                const float h1 = plain_act_tc(__uint_as_float(v[2 * i + 1]), p.act);
+                                w[8 * q + i] = pack_act2(__float_as_uint(h0), __float_as_uint(h1), F16);
+                            }
                         }
-                        uint16_t* hrow = p.Y + m * p.N + n;
-                        *reinterpret_cast<uint4*>(hrow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        *reinterpret_cast<uint4*>(hrow + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        if (n >= p.N) continue;
+                        store_rows32(tile, w, m < m_end ? reinterpret_cast<uint32_t*>(p.Y + m * p.N + n) : nullptr, 32,
+                                     lane);
                     }
                 } else {
-                    const int32_t slot = m < m_end ? p.perm[m] : 0;
-                    const float w = m < m_end ? p.wts[slot] : 0.0f;
+                    // p * y rows per routing slot, through the shared-memory tile as
+                    // store_rows32 does, with the row's slot shuffled instead of a
+                    // pointer (N a multiple of 16)
+                    const int32_t slot = m < m_end ? p.perm[m] : -1;
+                    const float wt = m < m_end ? p.wts[slot] : 0.0f;
+                    float* ftile = reinterpret_cast<float*>(tile);
                     #pragma unroll 1
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const int col = half * 128 + c16 * 16;
-                        uint32_t v[16];
+                    for (int c32 = 0; c32 < 4; ++c32) {
+                        const int col = half * 128 + c32 * 32;
+                        uint32_t v[16], u[16];
                         tmem_ld_32x32b_x16(trow + col, v);
+                        tmem_ld_32x32b_x16(trow + col + 16, u);
                         tmem_ld_wait();
-                        const int64_t n = n0 + col;
-                        if (m >= m_end || n >= p.N) continue;
-                        float* yrow = p.Yp + (int64_t)slot * p.N + n;    // N a multiple of 64
                         #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            *reinterpret_cast<float4*>(yrow + 4 * i) =
-                                make_float4(w * __uint_as_float(v[4 * i]), w * __uint_as_float(v[4 * i + 1]),
-                                            w * __uint_as_float(v[4 * i + 2]), w * __uint_as_float(v[4 * i + 3]));
+                        for (int i = 0; i < 16; ++i) {
+                            ftile[lane * 33 + i] = wt * __uint_as_float(v[i]);
+                            ftile[lane * 33 + 16 + i] = wt * __uint_as_float(u[i]);
+                        }
+                        __syncwarp();
+                        const int64_t n = n0 + col + (lane & 7) * 4;
+                        #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = i * 4 + (lane >> 3);
+                            const int32_t sl = __shfl_sync(0xffffffffu, slot, r);
+                            const float* src = ftile + r * 33 + (lane & 7) * 4;
+                            if (sl >= 0 && n < p.N)
+                                *reinterpret_cast<float4*>(p.Yp + (int64_t)sl * p.N + n) =
+                                    make_float4(src[0], src[1], src[2], src[3]);
+                        }
+                        __syncwarp();
                     }
                 }
             }
